@@ -1,0 +1,184 @@
+/*
+ * nvfp4.h -- C ABI of libnvfp4: the NVFP4 linear-layer hot path on one
+ * NVIDIA B300 (sm_103a).
+ *
+ * The method (sources):
+ *  [NVB] NVIDIA technical blog "NVFP4 Trains with Precision of 16-Bit and
+ *        Speed and Efficiency of 4-Bit" (Chinese edition), section "NVFP4
+ *        quantization recipe for pre-training": 16-element micro-blocks with
+ *        one shared scale (bullet 1), E4M3 block scales (bullet 2), a
+ *        Hadamard transform on GEMM inputs (bullet 3), 2D block quantisation
+ *        of weights so forward and backward agree (bullet 4), stochastic
+ *        rounding of gradients (bullet 5); Figure 1 (GEMMs dominate).
+ *  [SAI] prism.simon-ai.net article 7890 "From MVFP4 to the essence of
+ *        compute precision": section "Core architectural changes of the MVFP4
+ *        format" (per-tensor FP32 scale over the E4M3 block scales), section
+ *        "Training stability and protection of sensitive layers" (16x16
+ *        weight blocks, 256 values per scale), section "Techniques against
+ *        outliers and rounding error" (random Hadamard transform preserves the
+ *        vector norm; stochastic rounding, 0.3 -> 1 with probability 30%).
+ *
+ * Numeric specification (the readings the pages leave open, fixed here):
+ *  - amax: max |x| over the tensor (or over the 16-point RHT of every 16-chunk
+ *    along k when an RHT mask is given).  NaN/Inf make the tensor invalid.
+ *  - S_enc = fp32(2688 / amax) (2688 = 448 * 6, the E4M3 and E2M1 maxima);
+ *    amax == 0 gives S_enc = 1; an overflowing S_enc saturates to FLT_MAX.
+ *  - block decode scale s_b = E4M3_RNE_satfinite(fp32(fp32(amax_b / 6) * S_enc));
+ *    encode factor r_b = fp32(S_enc / s_b) (0 when s_b == 0, FLT_MAX on
+ *    overflow).
+ *  - element: v = fp32(x * r_b); RNE: nearest E2M1 value, ties to the even
+ *    code, saturating at +-6, sign kept (so small negatives give code 0x8);
+ *    SR: round |v| up from the grid value below to the one above iff
+ *    u16 < floor(frac * 2^16), frac = (|v| - lo)/(hi - lo), where u16 is the
+ *    element's 16-bit slice of Philox4x32-10 (key = seed, counter =
+ *    (idx / 8, stream_id), slice idx % 8 = word (idx%8)/2, low half first),
+ *    idx = r * k + c in the logical operand.
+ *  - RHT-16: y = H16 diag(s) x / 4, Sylvester order, s_j = -1 for set bit j of
+ *    the 16-bit mask; evaluated sign flip, butterflies h = 1, 2, 4, 8 in fp32,
+ *    then * 0.25.  Applied along k only.
+ *  - dequantised value = fp32(fp32(q * s_b) * fp32(1 / S_enc)).
+ *  - GEMM: D[m,n] = alpha * sum_k qa*sa*qb*sb with FP32 accumulation,
+ *    alpha = fp32(1 / (S_enc_A * S_enc_B)); output FP32 or BF16 (RNE).
+ *
+ * Layouts.  A quantised operand is logical [rows x k], K-major:
+ *  - codes:  rows x (k/2) bytes, row-major; element c of a row sits in byte
+ *            c/2, the lower index in the low nibble.
+ *  - scales: one E4M3 byte per (row, 16-column block), stored in the layout
+ *            the block-scaled tensor-core MMA reads: rows padded to 128 and
+ *            block columns padded to 4; 512-byte tiles, tile (row/128,
+ *            col/4) at ((row/128) * ceil(k/64) + col/4) * 512, and inside a
+ *            tile (row%32)*16 + ((row/32)%4)*4 + col%4.  Padding bytes are 0.
+ *            Size: nvfp4_scale_bytes(rows, k).
+ *  - global_scale: one float (S_enc) in device memory.
+ *
+ * Conventions for every call:
+ *  - All pointers are DEVICE pointers owned by the caller; the library
+ *    allocates no memory.  Buffers must not overlap unless stated.
+ *  - Calls are asynchronous on `stream` and never synchronise with the host
+ *    (except nvfp4_get_status).
+ *  - Arguments are validated on the host before anything is launched; an
+ *    invalid call returns an error and launches nothing.
+ *  - Errors found on the device (non-finite amax reaching a quantiser, a
+ *    pipeline wait that timed out) are recorded in a device status word,
+ *    read and cleared by nvfp4_get_status().
+ *  - No C++ exception crosses this interface.
+ */
+#ifndef NVFP4_H
+#define NVFP4_H
+
+#include <stddef.h>
+#include <stdint.h>
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    NVFP4_OK = 0,
+    NVFP4_ERR_INVALID_ARG = 1,      /* null pointer, negative size, bad enum, aliasing   */
+    NVFP4_ERR_UNSUPPORTED_SHAPE = 2,/* k not a multiple of 16 (32 for the GEMM), ...     */
+    NVFP4_ERR_MISALIGNED = 3,       /* pointer or leading dimension not 16-byte aligned  */
+    NVFP4_ERR_NONFINITE = 4,        /* amax was NaN or Inf (device-side, via get_status) */
+    NVFP4_ERR_TIMEOUT = 5,          /* a bounded device wait expired (device-side)       */
+    NVFP4_ERR_CUDA = 6              /* a CUDA runtime call failed                        */
+} nvfp4_status;
+
+typedef enum { NVFP4_RNE = 0, NVFP4_SR = 1 } nvfp4_round;
+
+/* A bf16 tensor seen as the logical operand [rows x cols] (cols = k, the
+ * GEMM reduction dimension).  transposed == 0: element (r, c) is at
+ * ptr[r * ld + c] (ld >= cols).  transposed == 1: the array is stored as
+ * [cols x rows] and element (r, c) is at ptr[c * ld + r] (ld >= rows) -- the
+ * transpose-on-load used for the weight-gradient GEMM, where k is the token
+ * dimension.  ptr must be 16-byte aligned and ld a multiple of 8.            */
+typedef struct {
+    const void* ptr;
+    int64_t rows, cols, ld;
+    int transposed;
+} nvfp4_bf16_view;
+
+/* A quantised operand (see Layouts).  block2d records the block shape it was
+ * made with (0: 1x16, 1: 16x16); the GEMM does not depend on it.            */
+typedef struct {
+    uint8_t* codes;
+    uint8_t* scales;
+    float* global_scale;
+    int64_t rows, k;
+    int block2d;
+} nvfp4_q;
+
+/* Per-tensor amax ([SAI] two-level scale; step 1 of the path).
+ * Writes max |x| of the logical operand (rht_mask == 0) or max |RHT16(x)|
+ * over 16-chunks along k (rht_mask != 0, 16-bit mask) to *amax_dev.
+ * x.cols must be a multiple of 16 when rht_mask != 0.  NaN inputs give a NaN
+ * amax, Inf an Inf (no error here; the quantisers report it).               */
+nvfp4_status nvfp4_amax(nvfp4_bf16_view x, uint32_t rht_mask, float* amax_dev,
+                        cudaStream_t stream);
+
+/* 1x16 quantisation ([NVB] bullets 1, 2, 5; [SAI] global scale).
+ * x: logical [rows x k], k % 16 == 0.  amax_dev: the tensor's amax as written
+ * by nvfp4_amax (same view, same RHT setting); NULL makes the call compute it
+ * first, using out->global_scale as the temporary.  round: RNE or SR (seed,
+ * stream_id select the Philox stream; ignored for RNE).  out: rows and k must
+ * equal x's; codes rows*k/2 bytes, scales nvfp4_scale_bytes(rows, k) bytes,
+ * global_scale 1 float; all written (scale padding with 0).                 */
+nvfp4_status nvfp4_quantize_1d(nvfp4_bf16_view x, const float* amax_dev, nvfp4_round round,
+                               uint64_t seed, uint64_t stream_id, nvfp4_q* out,
+                               cudaStream_t stream);
+
+/* 16x16 quantisation of a weight ([NVB] bullet 4; [SAI] 16x16 blocks).
+ * One scale per 16 rows x 16 columns (replicated into every row's slot of the
+ * scale layout).  out_t (nullable) receives the transposed operand
+ * [k x rows] made from the same codes and scales, so that the backward GEMM
+ * sees exactly the forward's quantised weight; it needs rows % 16 == 0.
+ * Stochastic rounding draws its bits by the index in x's logical layout, and
+ * out_t holds the same codes transposed.                                    */
+nvfp4_status nvfp4_quantize_2d(nvfp4_bf16_view w, const float* amax_dev, nvfp4_round round,
+                               uint64_t seed, uint64_t stream_id, nvfp4_q* out,
+                               nvfp4_q* out_t, cudaStream_t stream);
+
+/* 16-point random Hadamard transform fused with quantisation ([NVB] bullet 3;
+ * [SAI] Hadamard transform).  Each 16-chunk along k is replaced by
+ * H16 diag(s) x / 4 before amax_b and encoding.  amax_dev must be the amax of
+ * the transformed tensor (nvfp4_amax with the same mask) or NULL.
+ * out->block2d selects 1x16 (0) or 16x16 (1) blocks.  The same mask must be
+ * used for both operands of a GEMM so that their dot products are kept.     */
+nvfp4_status nvfp4_rht_quantize(nvfp4_bf16_view x, uint32_t rht_mask, const float* amax_dev,
+                                nvfp4_round round, uint64_t seed, uint64_t stream_id,
+                                nvfp4_q* out, cudaStream_t stream);
+
+/* Dequantisation ([SAI] MXFP4 example: value = scale x code; with the global
+ * scale divided out).  Writes q as fp32 (out_is_bf16 == 0) or bf16 (RNE) into
+ * out[r * ld + c]; ld >= q->k, out 16-byte aligned, ld*elem a multiple of 16. */
+nvfp4_status nvfp4_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int64_t ld,
+                              cudaStream_t stream);
+
+/* Block-scaled FP4 GEMM on the tensor cores ([NVB] Figure 1 and bullet 1).
+ * D[m, n] = alpha * sum_k A[m,k] B[n,k] for A = a (M x K) and B = b (N x K),
+ * both K-major; FP32 accumulation; alpha = 1/(S_A S_B) from the operands'
+ * global scales.  d: M x N row-major with leading dimension ldd (elements),
+ * fp32 or bf16 (d_is_bf16).  Needs a->k == b->k, K % 32 == 0, ldd >= N,
+ * ldd * elem % 16 == 0, 16-byte aligned codes/scales/d.  M, N >= 1 arbitrary. */
+nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf16,
+                        int64_t ldd, cudaStream_t stream);
+
+/* Host helper: the 16-bit RHT sign mask of a seed = low 16 bits of word 0 of
+ * Philox4x32-10(counter = 0, key = seed).                                   */
+uint32_t nvfp4_rht_mask_from_seed(uint64_t seed);
+
+/* Synchronises `stream`, returns the device-side status recorded since the
+ * last call (NVFP4_ERR_TIMEOUT before NVFP4_ERR_NONFINITE before NVFP4_OK,
+ * NVFP4_ERR_CUDA if the stream reports a CUDA error) and clears it.        */
+nvfp4_status nvfp4_get_status(cudaStream_t stream);
+
+/* Size in bytes of the swizzled scale buffer of a [rows x k] operand.       */
+size_t nvfp4_scale_bytes(int64_t rows, int64_t k);
+
+/* Static text of a status code.                                             */
+const char* nvfp4_status_string(nvfp4_status s);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* NVFP4_H */

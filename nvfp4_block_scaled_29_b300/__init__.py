@@ -1,0 +1,212 @@
+"""Python binding of libnvfp4 (the NVFP4 linear-layer path on one B300).
+
+Argument marshalling only: every step of the path runs in the CUDA kernels of
+``libnvfp4.so`` (built in-tree by ``build.py``).  PyTorch provides device
+memory and streams.  There is no CPU fallback: importing this package on a
+machine where the library cannot be loaded raises, and every call checks the
+status the C ABI returns.
+
+The functions carry the C names of ``include/nvfp4.h``:
+
+  nvfp4_amax, nvfp4_quantize_1d, nvfp4_quantize_2d, nvfp4_rht_quantize,
+  nvfp4_dequantize, nvfp4_gemm, nvfp4_rht_mask_from_seed, nvfp4_get_status,
+  nvfp4_scale_bytes
+
+Sources of the method: NVIDIA blog "NVFP4 Trains with Precision of 16-Bit and
+Speed and Efficiency of 4-Bit" (recipe bullets 1-5, Figure 1) and the
+prism.simon-ai.net article 7890 (two-level scale, 16x16 weight blocks,
+Hadamard transform, stochastic rounding).
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+
+NVFP4_OK = 0
+NVFP4_ERR_INVALID_ARG = 1
+NVFP4_ERR_UNSUPPORTED_SHAPE = 2
+NVFP4_ERR_MISALIGNED = 3
+NVFP4_ERR_NONFINITE = 4
+NVFP4_ERR_TIMEOUT = 5
+NVFP4_ERR_CUDA = 6
+NVFP4_RNE = 0
+NVFP4_SR = 1
+
+
+class Nvfp4Error(RuntimeError):
+    def __init__(self, status: int, what: str):
+        super().__init__(f"{what}: {status_string(status)} (status {status})")
+        self.status = status
+
+
+class Bf16View(ctypes.Structure):
+    _fields_ = [("ptr", ctypes.c_void_p), ("rows", ctypes.c_int64), ("cols", ctypes.c_int64),
+                ("ld", ctypes.c_int64), ("transposed", ctypes.c_int)]
+
+
+class QStruct(ctypes.Structure):
+    _fields_ = [("codes", ctypes.c_void_p), ("scales", ctypes.c_void_p),
+                ("global_scale", ctypes.c_void_p), ("rows", ctypes.c_int64),
+                ("k", ctypes.c_int64), ("block2d", ctypes.c_int)]
+
+
+def _load():
+    if not os.path.exists(LIB_PATH):
+        raise ImportError(f"libnvfp4.so is not built ({LIB_PATH}); run "
+                          "`python -m nvfp4_block_scaled_29_b300.build` (needs nvcc)")
+    L = ctypes.CDLL(LIB_PATH)
+    st = ctypes.c_int
+    vp = ctypes.c_void_p
+    u64 = ctypes.c_uint64
+    L.nvfp4_amax.argtypes = [Bf16View, ctypes.c_uint32, vp, vp]
+    L.nvfp4_amax.restype = st
+    L.nvfp4_quantize_1d.argtypes = [Bf16View, vp, ctypes.c_int, u64, u64, ctypes.POINTER(QStruct), vp]
+    L.nvfp4_quantize_1d.restype = st
+    L.nvfp4_quantize_2d.argtypes = [Bf16View, vp, ctypes.c_int, u64, u64, ctypes.POINTER(QStruct),
+                                    ctypes.POINTER(QStruct), vp]
+    L.nvfp4_quantize_2d.restype = st
+    L.nvfp4_rht_quantize.argtypes = [Bf16View, ctypes.c_uint32, vp, ctypes.c_int, u64, u64,
+                                     ctypes.POINTER(QStruct), vp]
+    L.nvfp4_rht_quantize.restype = st
+    L.nvfp4_dequantize.argtypes = [ctypes.POINTER(QStruct), vp, ctypes.c_int, ctypes.c_int64, vp]
+    L.nvfp4_dequantize.restype = st
+    L.nvfp4_gemm.argtypes = [ctypes.POINTER(QStruct), ctypes.POINTER(QStruct), vp, ctypes.c_int,
+                             ctypes.c_int64, vp]
+    L.nvfp4_gemm.restype = st
+    L.nvfp4_rht_mask_from_seed.argtypes = [u64]
+    L.nvfp4_rht_mask_from_seed.restype = ctypes.c_uint32
+    L.nvfp4_get_status.argtypes = [vp]
+    L.nvfp4_get_status.restype = st
+    L.nvfp4_scale_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    L.nvfp4_scale_bytes.restype = ctypes.c_size_t
+    L.nvfp4_status_string.argtypes = [st]
+    L.nvfp4_status_string.restype = ctypes.c_char_p
+    return L
+
+
+lib = _load()
+
+
+def status_string(s: int) -> str:
+    return lib.nvfp4_status_string(s).decode()
+
+
+def _check(status: int, what: str, raise_on_error: bool = True) -> int:
+    if status != NVFP4_OK and raise_on_error:
+        raise Nvfp4Error(status, what)
+    return status
+
+
+def _stream(stream) -> int:
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _ptr(t) -> int | None:
+    return None if t is None else t.data_ptr()
+
+
+# ----------------------------------------------------------------- views ---
+def bf16_view(x: torch.Tensor, transposed: bool = False) -> Bf16View:
+    """View a 2-D bf16 tensor (stored row-major with unit column stride) as
+    the logical operand [rows x cols]; with transposed=True the logical operand
+    is x^T (x stored as [k x rows])."""
+    if x.dim() != 2 or x.stride(1) != 1 or x.element_size() != 2:
+        raise ValueError("expected a 2-D 16-bit tensor with unit column stride")
+    r, c = x.shape
+    if transposed:
+        return Bf16View(x.data_ptr(), c, r, x.stride(0), 1)
+    return Bf16View(x.data_ptr(), r, c, x.stride(0), 0)
+
+
+class QTensor:
+    """A quantised operand in device memory (torch-allocated): codes
+    [rows, k/2] uint8, swizzled scales (nvfp4_scale_bytes) uint8, global
+    encode scale [1] float32."""
+
+    def __init__(self, rows: int, k: int, block2d: bool = False, device="cuda"):
+        self.rows, self.k, self.block2d = rows, k, block2d
+        self.codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=device)
+        self.scales = torch.empty((max(1, nvfp4_scale_bytes(rows, k)),), dtype=torch.uint8, device=device)
+        self.global_scale = torch.empty((1,), dtype=torch.float32, device=device)
+
+    def c(self) -> QStruct:
+        return QStruct(self.codes.data_ptr(), self.scales.data_ptr(), self.global_scale.data_ptr(),
+                       self.rows, self.k, int(self.block2d))
+
+
+def _as_view(x, transposed):
+    return x if isinstance(x, Bf16View) else bf16_view(x, transposed)
+
+
+# ------------------------------------------------------------ the calls ----
+def nvfp4_amax(x, rht_mask: int = 0, amax: torch.Tensor | None = None, *, transposed=False,
+               stream=None, check=True) -> torch.Tensor:
+    v = _as_view(x, transposed)
+    if amax is None:
+        amax = torch.empty((1,), dtype=torch.float32, device="cuda")
+    _check(lib.nvfp4_amax(v, rht_mask, amax.data_ptr(), _stream(stream)), "nvfp4_amax", check)
+    return amax
+
+
+def nvfp4_quantize_1d(x, amax: torch.Tensor | None, rnd: int, seed: int, stream_id: int,
+                      out: QTensor, *, transposed=False, stream=None, check=True) -> int:
+    q = out.c()
+    return _check(lib.nvfp4_quantize_1d(_as_view(x, transposed), _ptr(amax), rnd, seed, stream_id,
+                                        ctypes.byref(q), _stream(stream)), "nvfp4_quantize_1d", check)
+
+
+def nvfp4_quantize_2d(w, amax: torch.Tensor | None, rnd: int, seed: int, stream_id: int,
+                      out: QTensor, out_t: QTensor | None = None, *, transposed=False, stream=None,
+                      check=True) -> int:
+    q = out.c()
+    qt = out_t.c() if out_t is not None else None
+    return _check(lib.nvfp4_quantize_2d(_as_view(w, transposed), _ptr(amax), rnd, seed, stream_id,
+                                        ctypes.byref(q), ctypes.byref(qt) if qt is not None else None,
+                                        _stream(stream)), "nvfp4_quantize_2d", check)
+
+
+def nvfp4_rht_quantize(x, rht_mask: int, amax: torch.Tensor | None, rnd: int, seed: int,
+                       stream_id: int, out: QTensor, *, transposed=False, stream=None,
+                       check=True) -> int:
+    q = out.c()
+    return _check(lib.nvfp4_rht_quantize(_as_view(x, transposed), rht_mask, _ptr(amax), rnd, seed,
+                                         stream_id, ctypes.byref(q), _stream(stream)),
+                  "nvfp4_rht_quantize", check)
+
+
+def nvfp4_dequantize(q: QTensor, out: torch.Tensor, *, stream=None, check=True) -> int:
+    if out.dtype not in (torch.float32, torch.bfloat16) or out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be a 2-D float32 or bfloat16 tensor with unit column stride")
+    qs = q.c()
+    return _check(lib.nvfp4_dequantize(ctypes.byref(qs), out.data_ptr(), int(out.dtype == torch.bfloat16),
+                                       out.stride(0), _stream(stream)), "nvfp4_dequantize", check)
+
+
+def nvfp4_gemm(a: QTensor, b: QTensor, d: torch.Tensor, *, stream=None, check=True) -> int:
+    if d.dtype not in (torch.float32, torch.bfloat16) or d.dim() != 2 or d.stride(1) != 1:
+        raise ValueError("d must be a 2-D float32 or bfloat16 tensor with unit column stride")
+    qa, qb = a.c(), b.c()
+    return _check(lib.nvfp4_gemm(ctypes.byref(qa), ctypes.byref(qb), d.data_ptr(),
+                                 int(d.dtype == torch.bfloat16), d.stride(0), _stream(stream)),
+                  "nvfp4_gemm", check)
+
+
+def nvfp4_rht_mask_from_seed(seed: int) -> int:
+    return int(lib.nvfp4_rht_mask_from_seed(seed))
+
+
+def nvfp4_get_status(stream=None) -> int:
+    return int(lib.nvfp4_get_status(_stream(stream)))
+
+
+def nvfp4_scale_bytes(rows: int, k: int) -> int:
+    return int(lib.nvfp4_scale_bytes(rows, k))

@@ -1,0 +1,292 @@
+// gemm.cuh -- block-scaled NVFP4 GEMM on the 5th-generation tensor cores.
+//
+//   D[m, n] = alpha * sum_k (qa[m,k] * sa[m,k/16]) * (qb[n,k] * sb[n,k/16])
+//
+// with E2M1 codes qa/qb, E4M3 block scales sa/sb (one per 16 elements along
+// k), FP32 accumulation in tensor memory and alpha = 1 / (S_A * S_B) applied
+// in the epilogue (FP32 or BF16 output).  Source: NVIDIA blog "NVFP4 Trains
+// with Precision of 16-Bit and Speed and Efficiency of 4-Bit", Figure 1 (GEMMs
+// of the linear layers dominate) and recipe bullets 1-2 (16-element blocks
+// with E4M3 scales, natively supported by Blackwell tensor cores).
+//
+// Design (sm_103a, one CTA per SM, persistent over 128 x 256 output tiles):
+//  * warp 0   : TMA producer.  Per 256-wide k block it loads the A tile
+//               (128 rows x 128 B, 128-byte swizzle), the B tile (256 rows x
+//               128 B) and the matching 512-byte scale tiles (1D bulk copies)
+//               into a 4-stage shared-memory ring.
+//  * warp 1   : allocates TMEM; one lane copies the scale tiles to TMEM
+//               (tcgen05.cp 32x128b.warpx4) and issues 4 MMAs
+//               (tcgen05.mma kind::mxf4nvf4 block_scale scale_vec::4X, K = 64)
+//               per stage, releasing the stage with tcgen05.commit.
+//  * warps 2-5: epilogue.  Each warp drains its 32-lane quarter of the
+//               128 x 256 FP32 accumulator with tcgen05.ld, scales by alpha,
+//               converts and stores.  The accumulator is released after the
+//               last TMEM read, before the last stores, so the next tile's
+//               MMAs start while the stores drain.
+// TMEM: columns [0, 256) accumulator; [256, 448) the per-stage scale slots
+// (16 columns of A scales + 32 of B scales per stage).
+// Every mbarrier wait is bounded (2 s); on expiry the kernel records
+// NVFP4_DEV_TIMEOUT, drains its own copies and MMAs, frees TMEM and returns.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include "ptx.cuh"
+#include "status.cuh"
+
+namespace nvfp4 {
+namespace gemm {
+
+constexpr int BM = 128;
+constexpr int BN = 256;
+constexpr int BK = 256;                       // k elements per stage (128 bytes of codes)
+constexpr int STAGES = 4;
+constexpr int A_BYTES = BM * BK / 2;          // 16 KB
+constexpr int B_BYTES = BN * BK / 2;          // 32 KB
+constexpr int SFA_BYTES = (BM / 128) * (BK / 64) * 512;   // 2 KB
+constexpr int SFB_BYTES = (BN / 128) * (BK / 64) * 512;   // 4 KB
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int SMEM_BYTES = STAGES * STAGE_BYTES + 1024 /*align*/ + 256 /*barriers*/;
+constexpr int THREADS = 192;
+constexpr int TMEM_COLS = 512;
+constexpr int TMEM_SF_BASE = 256;
+constexpr int SF_COLS_PER_STAGE = 48;
+static_assert(STAGE_BYTES % 1024 == 0, "stage buffers must stay 1024-byte aligned");
+static_assert(TMEM_SF_BASE + STAGES * SF_COLS_PER_STAGE <= TMEM_COLS, "TMEM budget");
+
+struct Args {
+    const uint8_t* sfa;        // swizzled scales of A (rows padded to 128)
+    const uint8_t* sfb;
+    const float* gs_a;         // S_enc of A and B (device)
+    const float* gs_b;
+    void* d;
+    int64_t ldd;
+    int d_bf16;
+    int M, N, K;
+    int m_tiles, n_tiles;
+    int k_blocks;              // ceil(K / BK)
+    int k_steps;               // ceil(K / 64): MMAs along k
+    int sf_col_tiles;          // ceil(K / 64): 512-byte scale tiles per 128-row group
+    int b_row_tiles;           // ceil(N / 128)
+};
+
+// Instruction descriptor of kind::mxf4nvf4: dense, A and B E2M1 (format 1),
+// both K-major, UE4M3 scales, scale-factor ids 0, N >> 3 at bit 17,
+// M >> 4 at bit 24.
+__host__ __device__ constexpr uint32_t make_idesc() {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
+}
+
+__device__ __forceinline__ void store_chunk(const Args& a, int64_t row, int64_t col0,
+                                            const uint32_t* acc, float alpha) {
+    if (row >= a.M) return;
+    float v[32];
+#pragma unroll
+    for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(acc[j]), alpha);
+    const bool full = col0 + 32 <= a.N;
+    if (a.d_bf16) {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(a.d) + row * a.ldd + col0;
+        if (full) {
+            uint32_t p[16];
+#pragma unroll
+            for (int j = 0; j < 16; ++j) {
+                __nv_bfloat162 h = __floats2bfloat162_rn(v[2 * j], v[2 * j + 1]);
+                p[j] = *reinterpret_cast<uint32_t*>(&h);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) d4[j] = make_uint4(p[4 * j], p[4 * j + 1], p[4 * j + 2], p[4 * j + 3]);
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < a.N) {
+                    __nv_bfloat16 h = __float2bfloat16_rn(v[j]);
+                    dst[j] = *reinterpret_cast<uint16_t*>(&h);
+                }
+        }
+    } else {
+        float* dst = reinterpret_cast<float*>(a.d) + row * a.ldd + col0;
+        if (full) {
+            float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+            for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);
+        } else {
+            for (int j = 0; j < 32; ++j)
+                if (col0 + j < a.N) dst[j] = v[j];
+        }
+    }
+}
+
+__global__ void __launch_bounds__(THREADS, 1)
+k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+             const Args args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(smem + STAGES * STAGE_BYTES);
+    uint64_t* empty_bar = full_bar + STAGES;
+    uint64_t* acc_full = empty_bar + STAGES;
+    uint64_t* acc_empty = acc_full + 1;
+    uint64_t* drain_bar = acc_empty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int num_tiles = args.m_tiles * args.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 4 * 32);
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+    }
+    if (warp == 1) {
+        tmem_alloc(tmem_holder, TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            uint32_t fills[STAGES] = {0, 0, 0, 0};
+            bool ok = true;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+                const int m_blk = tile % args.m_tiles, n_blk = tile / args.m_tiles;
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    uint8_t* ssfa = sb + B_BYTES;
+                    uint8_t* ssfb = ssfa + SFA_BYTES;
+                    const int atoms = min(4, args.sf_col_tiles - kb * 4);
+                    const int b_tiles = min(2, args.b_row_tiles - n_blk * 2);
+                    const uint32_t bytes = A_BYTES + B_BYTES + atoms * 512 * (1 + b_tiles);
+                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                    tma_load_2d(sa, &tma_a, &full_bar[stage], kb * (BK / 2), m_blk * BM);
+                    tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN);
+                    bulk_load(ssfa, args.sfa + ((int64_t)m_blk * args.sf_col_tiles + kb * 4) * 512,
+                              atoms * 512, &full_bar[stage]);
+                    for (int j = 0; j < b_tiles; ++j)
+                        bulk_load(ssfb + j * (BK / 64) * 512,
+                                  args.sfb + ((int64_t)(n_blk * 2 + j) * args.sf_col_tiles + kb * 4) * 512,
+                                  atoms * 512, &full_bar[stage]);
+                    fills[stage] += 1;
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                // let every copy this thread issued land before the CTA exits
+                for (int s = 0; s < STAGES; ++s)
+                    if (fills[s]) mbar_wait_bounded(&full_bar[s], (fills[s] - 1) & 1u, nullptr);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------------- MMA issuer ----
+        if (lane == 0) {
+            constexpr uint32_t idesc = make_idesc();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool issued = false;
+            int local = 0;
+            for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
+                if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t ssfa = sb + B_BYTES;
+                    const uint32_t ssfb = ssfa + SFA_BYTES;
+                    const uint32_t t_sf = tmem_base + TMEM_SF_BASE + stage * SF_COLS_PER_STAGE;
+                    const int nks = min(BK / 64, args.k_steps - kb * (BK / 64));
+                    for (int ks = 0; ks < nks; ++ks) {
+                        tc_cp_32x128b_warpx4(t_sf + ks * 4, smem_desc(ssfa + ks * 512, 0, 128, 0));
+                        tc_cp_32x128b_warpx4(t_sf + 16 + ks * 8, smem_desc(ssfb + ks * 512, 0, 128, 0));
+                        tc_cp_32x128b_warpx4(t_sf + 16 + ks * 8 + 4,
+                                             smem_desc(ssfb + (BK / 64) * 512 + ks * 512, 0, 128, 0));
+                    }
+                    for (int ks = 0; ks < nks; ++ks) {
+                        const uint64_t adesc = smem_desc(sa + ks * 32, 16, 1024, 2);
+                        const uint64_t bdesc = smem_desc(sb + ks * 32, 16, 1024, 2);
+                        tc_mma_nvf4(tmem_base, adesc, bdesc, idesc, t_sf + ks * 4, t_sf + 16 + ks * 8,
+                                    (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit(&empty_bar[stage]);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit(acc_full);
+            }
+            if (!ok && issued) {
+                tc_commit(drain_bar);
+                mbar_wait_bounded(drain_bar, 0, nullptr);
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------- epilogue ----
+        const int quarter = warp & 3;
+        const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
+        int local = 0;
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
+            // every lane waits, so the warp stays converged for tcgen05.ld
+            if (!mbar_wait_bounded(acc_full, (uint32_t)local & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int m_blk = tile % args.m_tiles, n_blk = tile / args.m_tiles;
+            const int64_t row = (int64_t)m_blk * BM + quarter * 32 + lane;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16);
+            uint32_t acc[32];
+            for (int c = 0; c < BN / 32; ++c) {
+                tmem_ld_32x32b_x32(t_row + c * 32, acc);
+                tmem_ld_wait();
+                if (c == BN / 32 - 1) {
+                    tc_fence_before();
+                    mbar_arrive(acc_empty);
+                }
+                const int64_t col0 = (int64_t)n_blk * BN + c * 32;
+                if (col0 < args.N) store_chunk(args, row, col0, acc, alpha);
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm
+}  // namespace nvfp4

@@ -1,0 +1,425 @@
+// nvfp4.cu -- the C ABI of libnvfp4 (declared in include/nvfp4.h).
+//
+// One translation unit: it includes every kernel header, validates arguments
+// on the host, chooses launch shapes and encodes the TMA tensor maps.  The
+// library allocates no memory; the only state is the device status word and
+// small per-device caches of launch attributes.
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <atomic>
+#include <cstdint>
+#include <cstring>
+
+#include "../../include/nvfp4.h"
+#include "codec.cuh"
+#include "gemm.cuh"
+#include "quantize.cuh"
+#include "status.cuh"
+
+namespace {
+
+using namespace nvfp4;
+
+constexpr int kMaxDevices = 64;
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+int64_t cdiv(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+int device_sm_count() {
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return 148;
+    int v = cache[dev].load(std::memory_order_relaxed);
+    if (v > 0) return v;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || v <= 0)
+        v = 148;
+    cache[dev].store(v, std::memory_order_relaxed);
+    return v;
+}
+
+nvfp4_status launch_status() {
+    return cudaGetLastError() == cudaSuccess ? NVFP4_OK : NVFP4_ERR_CUDA;
+}
+
+int grid_for(int64_t items, int threads, int per_sm) {
+    const int64_t need = cdiv(items, threads);
+    const int64_t cap = (int64_t)device_sm_count() * per_sm;
+    return (int)std::max<int64_t>(1, std::min(need, cap));
+}
+
+// ------------------------------------------------------------- validation --
+nvfp4_status check_view(const nvfp4_bf16_view& x, bool need_k16) {
+    if (x.rows < 0 || x.cols < 0) return NVFP4_ERR_INVALID_ARG;
+    if (x.transposed != 0 && x.transposed != 1) return NVFP4_ERR_INVALID_ARG;
+    if (need_k16 && (x.cols % 16) != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (x.rows == 0 || x.cols == 0) return NVFP4_OK;
+    if (x.ptr == nullptr) return NVFP4_ERR_INVALID_ARG;
+    const int64_t min_ld = x.transposed ? x.rows : x.cols;
+    if (x.ld < min_ld) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(x.ptr, 16) || (x.ld % 8) != 0) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+nvfp4_status check_q(const nvfp4_q* q, int64_t rows, int64_t k) {
+    if (q == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (q->rows != rows || q->k != k) return NVFP4_ERR_INVALID_ARG;
+    if (q->global_scale == nullptr || !aligned(q->global_scale, 4)) return NVFP4_ERR_INVALID_ARG;
+    if (rows == 0 || k == 0) return NVFP4_OK;
+    if (q->codes == nullptr || q->scales == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(q->codes, 16) || !aligned(q->scales, 16)) return NVFP4_ERR_MISALIGNED;
+    return NVFP4_OK;
+}
+
+// ------------------------------------------------------------------ amax ---
+nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cudaStream_t st) {
+    if (cudaMemsetAsync(out, 0, sizeof(float), st) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (x.rows == 0 || x.cols == 0) return NVFP4_OK;
+    const uint16_t* p = static_cast<const uint16_t*>(x.ptr);
+    const int64_t srows = x.transposed ? x.cols : x.rows;
+    const int64_t scols = x.transposed ? x.rows : x.cols;
+    if (mask == 0) {
+        if (x.ld == scols || srows == 1) {
+            const int64_t len = srows * scols;
+            k_amax_plain<<<grid_for(cdiv(len, 32), kQuantThreads, 8), kQuantThreads, 0, st>>>(
+                p, 1, len, x.ld, out);
+        } else {
+            const int g = (int)std::min<int64_t>(srows, (int64_t)device_sm_count() * 8);
+            k_amax_plain<<<g, kQuantThreads, 0, st>>>(p, srows, scols, x.ld, out);
+        }
+    } else if (!x.transposed) {
+        k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
+            p, x.rows, x.cols, x.ld, mask, out);
+    } else {
+        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 8) * (x.cols / 16), kQuantThreads, 8), kQuantThreads,
+                          0, st>>>(p, x.cols, x.rows, x.ld, mask, out);
+    }
+    return launch_status();
+}
+
+// -------------------------------------------------------------- quantise ---
+template <bool RHT, bool SR>
+void launch_q1d(const QuantArgs& a, bool transposed, cudaStream_t st) {
+    const int64_t nkb = a.k / 16;
+    const int64_t ngroups = cdiv(nkb, 4);
+    const int64_t rows_pad = cdiv(a.rows, 128) * 128;
+    if (!transposed) {
+        k_quant1d_rows<RHT, SR><<<grid_for(rows_pad * ngroups, kQuantThreads, 8), kQuantThreads, 0,
+                                  st>>>(a);
+    } else {
+        k_quant1d_cols<RHT, SR><<<grid_for((rows_pad / 2) * ngroups, kQuantThreads, 8),
+                                  kQuantThreads, 0, st>>>(a);
+    }
+}
+
+template <bool RHT, bool SR>
+void launch_q2d(const QuantArgs& a, bool emit_t, cudaStream_t st) {
+    const dim3 grid((unsigned)cdiv(a.k, 128), (unsigned)(cdiv(a.rows, 128) * 2));
+    if (emit_t) {
+        if constexpr (!RHT) k_quant2d<false, SR, true><<<grid, k2DThreads, 0, st>>>(a);
+    } else {
+        k_quant2d<RHT, SR, false><<<grid, k2DThreads, 0, st>>>(a);
+    }
+}
+
+nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float* amax_dev,
+                           nvfp4_round round, uint64_t seed, uint64_t stream_id, nvfp4_q* out,
+                           nvfp4_q* out_t, bool block2d, cudaStream_t st) {
+    nvfp4_status s = check_view(x, true);
+    if (s != NVFP4_OK) return s;
+    if (mask > 0xFFFFu) return NVFP4_ERR_INVALID_ARG;
+    if (round != NVFP4_RNE && round != NVFP4_SR) return NVFP4_ERR_INVALID_ARG;
+    if ((s = check_q(out, x.rows, x.cols)) != NVFP4_OK) return s;
+    if (out_t != nullptr) {
+        if (!block2d || mask != 0) return NVFP4_ERR_INVALID_ARG;
+        if ((s = check_q(out_t, x.cols, x.rows)) != NVFP4_OK) return s;
+        if (x.rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (block2d && x.transposed) {
+        if (mask != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+        if (x.rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    }
+    if (amax_dev != nullptr && (amax_dev == out->global_scale ||
+                                (out_t != nullptr && amax_dev == out_t->global_scale)))
+        return NVFP4_ERR_INVALID_ARG;
+    if (amax_dev != nullptr && !aligned(amax_dev, 4)) return NVFP4_ERR_MISALIGNED;
+
+    // global scale source
+    const float* src = amax_dev;
+    int src_is_senc = 0;
+    if (amax_dev == nullptr) {
+        if ((s = launch_amax(x, mask, out->global_scale, st)) != NVFP4_OK) return s;
+        k_amax_to_senc<<<1, 1, 0, st>>>(out->global_scale);
+        src = out->global_scale;
+        src_is_senc = 1;
+    }
+    if (x.rows == 0 || x.cols == 0) {
+        // nothing to encode: publish S_enc only
+        k_publish_senc<<<1, 1, 0, st>>>(src, src_is_senc, out->global_scale,
+                                        out_t ? out_t->global_scale : nullptr);
+        return launch_status();
+    }
+
+    QuantArgs a{};
+    a.x = static_cast<const uint16_t*>(x.ptr);
+    a.ld = x.ld;
+    a.scale_src = src;
+    a.src_is_senc = src_is_senc;
+    a.gs_out = out->global_scale;
+    a.gs_out2 = out_t ? out_t->global_scale : nullptr;
+    a.rht_mask = mask;
+    a.seed = seed;
+    a.stream_id = stream_id;
+    const bool sr = round == NVFP4_SR;
+
+    if (!block2d) {
+        a.rows = x.rows;
+        a.k = x.cols;
+        a.codes = out->codes;
+        a.scales = out->scales;
+        a.write_primary = 1;
+        if (mask) {
+            if (sr) launch_q1d<true, true>(a, x.transposed, st);
+            else launch_q1d<true, false>(a, x.transposed, st);
+        } else {
+            if (sr) launch_q1d<false, true>(a, x.transposed, st);
+            else launch_q1d<false, false>(a, x.transposed, st);
+        }
+        return launch_status();
+    }
+    if (!x.transposed) {
+        a.rows = x.rows;
+        a.k = x.cols;
+        a.codes = out->codes;
+        a.scales = out->scales;
+        a.write_primary = 1;
+        a.codes_t = out_t ? out_t->codes : nullptr;
+        a.scales_t = out_t ? out_t->scales : nullptr;
+        a.idx_transposed = 0;
+        const bool emit = out_t != nullptr;
+        if (mask) {
+            if (sr) launch_q2d<true, true>(a, false, st);
+            else launch_q2d<true, false>(a, false, st);
+        } else {
+            if (sr) launch_q2d<false, true>(a, emit, st);
+            else launch_q2d<false, false>(a, emit, st);
+        }
+        return launch_status();
+    }
+    // 16x16 on a transposed view: quantise the stored [k x rows] array; its
+    // primary output is the caller's out_t, its transposed emit the caller's out.
+    a.rows = x.cols;
+    a.k = x.rows;
+    a.write_primary = out_t != nullptr;
+    a.codes = out_t ? out_t->codes : nullptr;
+    a.scales = out_t ? out_t->scales : nullptr;
+    a.codes_t = out->codes;
+    a.scales_t = out->scales;
+    a.idx_transposed = 1;
+    if (sr) launch_q2d<false, true>(a, true, st);
+    else launch_q2d<false, false>(a, true, st);
+    return launch_status();
+}
+
+// ----------------------------------------------------------- tensor maps ---
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load();
+    if (f) return f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+        return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f);
+    return f;
+}
+
+// [rows x k/2] bytes of E2M1 codes, box = 128 bytes x box_rows, 128-byte swizzle.
+bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t k, int box_rows) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)(k / 2), (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(k / 2)};
+    const cuuint32_t box[2] = {128u, (cuuint32_t)box_rows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<uint8_t*>(codes), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool gemm_smem_ready() {
+    static std::atomic<int> done[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
+    if (done[dev].load()) return true;
+    if (cudaFuncSetAttribute(gemm::k_gemm_nvfp4, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm::SMEM_BYTES) != cudaSuccess)
+        return false;
+    done[dev].store(1);
+    return true;
+}
+
+// Host Philox4x32-10 (Salmon et al., SC'11), for the RHT sign mask.
+uint32_t host_philox_word0(uint64_t seed) {
+    uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) {
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+        const uint64_t p0 = (uint64_t)0xD2511F53u * c0, p1 = (uint64_t)0xCD9E8D57u * c2;
+        const uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0, n1 = (uint32_t)p1;
+        const uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1, n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    return c0;
+}
+
+}  // namespace
+
+// =================================================================== ABI ===
+extern "C" {
+
+nvfp4_status nvfp4_amax(nvfp4_bf16_view x, uint32_t rht_mask, float* amax_dev,
+                        cudaStream_t stream) {
+    nvfp4_status s = check_view(x, rht_mask != 0);
+    if (s != NVFP4_OK) return s;
+    if (rht_mask > 0xFFFFu || amax_dev == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(amax_dev, 4)) return NVFP4_ERR_MISALIGNED;
+    return launch_amax(x, rht_mask, amax_dev, stream);
+}
+
+nvfp4_status nvfp4_quantize_1d(nvfp4_bf16_view x, const float* amax_dev, nvfp4_round round,
+                               uint64_t seed, uint64_t stream_id, nvfp4_q* out,
+                               cudaStream_t stream) {
+    return quantize_impl(x, 0, amax_dev, round, seed, stream_id, out, nullptr, false, stream);
+}
+
+nvfp4_status nvfp4_quantize_2d(nvfp4_bf16_view w, const float* amax_dev, nvfp4_round round,
+                               uint64_t seed, uint64_t stream_id, nvfp4_q* out, nvfp4_q* out_t,
+                               cudaStream_t stream) {
+    return quantize_impl(w, 0, amax_dev, round, seed, stream_id, out, out_t, true, stream);
+}
+
+nvfp4_status nvfp4_rht_quantize(nvfp4_bf16_view x, uint32_t rht_mask, const float* amax_dev,
+                                nvfp4_round round, uint64_t seed, uint64_t stream_id,
+                                nvfp4_q* out, cudaStream_t stream) {
+    if (rht_mask == 0 || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (out->block2d != 0 && out->block2d != 1) return NVFP4_ERR_INVALID_ARG;
+    return quantize_impl(x, rht_mask, amax_dev, round, seed, stream_id, out, nullptr,
+                         out->block2d == 1, stream);
+}
+
+nvfp4_status nvfp4_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int64_t ld,
+                              cudaStream_t stream) {
+    if (q == nullptr || (out_is_bf16 != 0 && out_is_bf16 != 1)) return NVFP4_ERR_INVALID_ARG;
+    if (q->rows < 0 || q->k < 0) return NVFP4_ERR_INVALID_ARG;
+    if (q->k % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    nvfp4_status s = check_q(q, q->rows, q->k);
+    if (s != NVFP4_OK) return s;
+    if (q->rows == 0 || q->k == 0) return NVFP4_OK;
+    if (out == nullptr || ld < q->k) return NVFP4_ERR_INVALID_ARG;
+    const int64_t esz = out_is_bf16 ? 2 : 4;
+    if (!aligned(out, 16) || (ld * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
+    const int g = grid_for(q->rows * (q->k / 16), kQuantThreads, 8);
+    if (out_is_bf16)
+        k_dequant<true><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->global_scale,
+                                                          q->rows, q->k, out, ld);
+    else
+        k_dequant<false><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->global_scale,
+                                                           q->rows, q->k, out, ld);
+    return launch_status();
+}
+
+nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf16, int64_t ldd,
+                        cudaStream_t stream) {
+    if (a == nullptr || b == nullptr || (d_is_bf16 != 0 && d_is_bf16 != 1))
+        return NVFP4_ERR_INVALID_ARG;
+    if (a->rows < 0 || b->rows < 0 || a->k < 0 || a->k != b->k) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = a->rows, N = b->rows, K = a->k;
+    if (K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    nvfp4_status s;
+    if ((s = check_q(a, M, K)) != NVFP4_OK) return s;
+    if ((s = check_q(b, N, K)) != NVFP4_OK) return s;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    const int64_t esz = d_is_bf16 ? 2 : 4;
+    if (d == nullptr || ldd < N) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(d, 16) || (ldd * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
+    if (K == 0) {
+        return cudaMemset2DAsync(d, ldd * esz, 0, N * esz, M, stream) == cudaSuccess ? NVFP4_OK
+                                                                                      : NVFP4_ERR_CUDA;
+    }
+    CUtensorMap ta, tb;
+    if (!make_code_map(&ta, a->codes, M, K, gemm::BM) || !make_code_map(&tb, b->codes, N, K, gemm::BN))
+        return NVFP4_ERR_CUDA;
+    if (!gemm_smem_ready()) return NVFP4_ERR_CUDA;
+    gemm::Args g{};
+    g.sfa = a->scales;
+    g.sfb = b->scales;
+    g.gs_a = a->global_scale;
+    g.gs_b = b->global_scale;
+    g.d = d;
+    g.ldd = ldd;
+    g.d_bf16 = d_is_bf16;
+    g.M = (int)M;
+    g.N = (int)N;
+    g.K = (int)K;
+    g.m_tiles = (int)cdiv(M, gemm::BM);
+    g.n_tiles = (int)cdiv(N, gemm::BN);
+    g.k_blocks = (int)cdiv(K, gemm::BK);
+    g.k_steps = (int)cdiv(K, 64);
+    g.sf_col_tiles = (int)cdiv(K, 64);
+    g.b_row_tiles = (int)cdiv(N, 128);
+    const int64_t tiles = (int64_t)g.m_tiles * g.n_tiles;
+    const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
+    gemm::k_gemm_nvfp4<<<grid, gemm::THREADS, gemm::SMEM_BYTES, stream>>>(ta, tb, g);
+    return launch_status();
+}
+
+uint32_t nvfp4_rht_mask_from_seed(uint64_t seed) { return host_philox_word0(seed) & 0xFFFFu; }
+
+nvfp4_status nvfp4_get_status(cudaStream_t stream) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    uint32_t word = 0;
+    if (cudaMemcpyFromSymbolAsync(&word, g_device_status, sizeof(word), 0, cudaMemcpyDeviceToHost,
+                                  stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    const uint32_t zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_device_status, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice,
+                                stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (word & NVFP4_DEV_TIMEOUT) return NVFP4_ERR_TIMEOUT;
+    if (word & NVFP4_DEV_NONFINITE) return NVFP4_ERR_NONFINITE;
+    return NVFP4_OK;
+}
+
+size_t nvfp4_scale_bytes(int64_t rows, int64_t k) {
+    if (rows <= 0 || k <= 0) return 0;
+    return (size_t)(cdiv(rows, 128) * cdiv(k / 16, 4) * 512);
+}
+
+const char* nvfp4_status_string(nvfp4_status s) {
+    switch (s) {
+        case NVFP4_OK: return "ok";
+        case NVFP4_ERR_INVALID_ARG: return "invalid argument";
+        case NVFP4_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case NVFP4_ERR_MISALIGNED: return "misaligned pointer or leading dimension";
+        case NVFP4_ERR_NONFINITE: return "non-finite amax";
+        case NVFP4_ERR_TIMEOUT: return "device wait timed out";
+        case NVFP4_ERR_CUDA: return "CUDA error";
+    }
+    return "unknown status";
+}
+
+}  // extern "C"

@@ -1,0 +1,589 @@
+// quantize.cuh -- HBM-bound kernels of the NVFP4 path: per-tensor amax,
+// 1x16 and 16x16 quantisation (RNE or Philox stochastic rounding, optional
+// fused 16-point random Hadamard transform, transpose-on-load, transposed
+// emit for weights) and dequantisation.
+//
+// Method: NVIDIA blog "NVFP4 Trains with Precision of 16-Bit and Speed and
+// Efficiency of 4-Bit", recipe bullets 1-5; prism.simon-ai.net article 7890,
+// sections "Core architectural changes of the MVFP4 format" (global FP32
+// scale), "Training stability and protection of sensitive layers" (16x16
+// weight blocks), "Techniques against outliers and rounding error" (RHT, SR).
+//
+// Work decomposition (all kernels are grid-stride, 256 threads per CTA):
+//  * rows variant: one thread owns 4 consecutive 16-element blocks (64
+//    elements) of one logical row: 8 x 16-byte loads, 32 bytes of codes and
+//    one 32-bit word of scales out (the 4 scales of a row are adjacent in the
+//    GEMM layout).
+//  * cols variant (transpose-on-load): one thread owns 2 adjacent logical
+//    rows x 64 logical columns; a warp reads 128 contiguous bytes of a stored
+//    row per load, so the stored tensor is read coalesced.
+//  * 2D variant: a 16-lane half-warp holds one 16x64 strip (one row per
+//    lane); the 16x16 block amax is a 4-step shuffle reduction.  The
+//    transposed operand is emitted from a shared-memory nibble tile.
+#pragma once
+#include <cstdint>
+#include "codec.cuh"
+#include "status.cuh"
+
+namespace nvfp4 {
+
+constexpr int kQuantThreads = 256;
+
+__device__ __forceinline__ uint4 ldg_stream(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
+    uint32_t v;
+    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
+    return v;
+}
+
+__device__ __forceinline__ void unpack8(uint4 w, float* v) {
+    v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
+    v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
+    v[4] = bf16_lo(w.z); v[5] = bf16_hi(w.z);
+    v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
+}
+
+__device__ __forceinline__ uint32_t absmax_bits16(const float* v) {
+    uint32_t m = 0;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
+    return m;
+}
+
+// Reduce a per-thread maximum of non-negative float bit patterns and merge it
+// into *out with one atomic per CTA (unsigned order == float order there).
+__device__ __forceinline__ void block_max_to_global(uint32_t m, float* out) {
+    __shared__ uint32_t red[kQuantThreads / 32];
+    m = __reduce_max_sync(0xFFFFFFFFu, m);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    if (lane == 0) red[warp] = m;
+    __syncthreads();
+    if (warp == 0) {
+        m = lane < (int)(blockDim.x >> 5) ? red[lane] : 0u;
+        m = __reduce_max_sync(0xFFFFFFFFu, m);
+        if (lane == 0 && m) atomicMax(reinterpret_cast<uint32_t*>(out), m);
+    }
+}
+
+// Resolve the global encode scale for a quantiser CTA.  src holds either the
+// amax (src_is_senc == 0; CTA 0 then publishes S_enc to gs_out) or S_enc
+// itself.  gs_out2 (nullable) receives a copy for a second operand made from
+// the same encoding.  Returns false (after recording the error) when the
+// scale is unusable.
+__device__ __forceinline__ bool resolve_scale(const float* src, int src_is_senc, float* gs_out,
+                                              float* gs_out2, float* s_enc) {
+    const float v = *src;
+    float s = v;
+    bool ok = fabsf(v) <= FLT_MAX;
+    if (!src_is_senc) ok = global_encode_scale(v, &s);
+    if (blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
+        const float pub = ok ? s : __int_as_float(0x7FC00000);
+        if (!src_is_senc) {
+            *gs_out = pub;
+            if (!ok) record_device_error(NVFP4_DEV_NONFINITE);
+        }
+        if (gs_out2 != nullptr) *gs_out2 = pub;
+    }
+    *s_enc = s;
+    return ok;
+}
+
+// Publish S_enc for an empty tensor (no quantiser CTA runs).
+__global__ void k_publish_senc(const float* src, int src_is_senc, float* gs_out, float* gs_out2) {
+    float s;
+    resolve_scale(src, src_is_senc, gs_out, gs_out2, &s);
+}
+
+// ============================================================== amax ======
+// max |x| (as bf16 magnitude bits) of a 16-byte aligned span, split over
+// `nt` threads starting at `tid`.
+__device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t len, int64_t tid,
+                                                int64_t nt) {
+    constexpr uint32_t M = 0x7FFF7FFFu;
+    uint32_t m2 = 0, m1 = 0;
+    const int64_t nch = len >> 3;
+    const uint4* v = reinterpret_cast<const uint4*>(base);
+    int64_t i = tid;
+    for (; i + 3 * nt < nch; i += 4 * nt) {
+        const uint4 a = ldg_stream(v + i), b = ldg_stream(v + i + nt);
+        const uint4 c = ldg_stream(v + i + 2 * nt), d = ldg_stream(v + i + 3 * nt);
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M)));
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(b.x & M, b.y & M), __vmaxu2(b.z & M, b.w & M)));
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(c.x & M, c.y & M), __vmaxu2(c.z & M, c.w & M)));
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(d.x & M, d.y & M), __vmaxu2(d.z & M, d.w & M)));
+    }
+    for (; i < nch; i += nt) {
+        const uint4 a = ldg_stream(v + i);
+        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M)));
+    }
+    for (int64_t j = (nch << 3) + tid; j < len; j += nt) m1 = max(m1, (uint32_t)(base[j] & 0x7FFFu));
+    return max(max(m2 & 0xFFFFu, m2 >> 16), m1);
+}
+
+// max |x| of a bf16 array of nrows rows of len elements (leading dimension
+// ld).  One row (contiguous data): the whole grid strides over it; several
+// rows: CTAs stride over rows, threads over a row.
+__global__ void __launch_bounds__(kQuantThreads) k_amax_plain(const uint16_t* __restrict__ p,
+                                                              int64_t nrows, int64_t len,
+                                                              int64_t ld, float* out) {
+    uint32_t m = 0;
+    if (nrows == 1) {
+        m = span_absmax(p, len, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
+                        (int64_t)gridDim.x * blockDim.x);
+    } else {
+        for (int64_t r = blockIdx.x; r < nrows; r += gridDim.x)
+            m = max(m, span_absmax(p + r * ld, len, threadIdx.x, blockDim.x));
+    }
+    block_max_to_global(m << 16, out);
+}
+
+// max |RHT16(x)| over 16-chunks along the stored rows (non-transposed view).
+__global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t* __restrict__ p,
+                                                                 int64_t rows, int64_t k,
+                                                                 int64_t ld, uint32_t mask,
+                                                                 float* out) {
+    uint32_t m = 0;
+    const uint32_t nkb = (uint32_t)(k >> 4);
+    const int64_t total = rows * (int64_t)nkb;
+    for (int64_t b = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; b < total;
+         b += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = b / nkb, kb = b - r * nkb;
+        const uint4* src = reinterpret_cast<const uint4*>(p + r * ld + kb * 16);
+        float v[16];
+        unpack8(ldg_stream(src), v);
+        unpack8(ldg_stream(src + 1), v + 8);
+        rht16(v, mask);
+        m = max(m, absmax_bits16(v));
+    }
+    block_max_to_global(m, out);
+}
+
+// max |RHT16(x)| over 16-chunks down the stored columns (transposed view:
+// the logical k runs along the stored rows).  One thread: 16 stored rows x
+// 8 stored columns.
+__global__ void __launch_bounds__(kQuantThreads) k_amax_rht_cols(const uint16_t* __restrict__ p,
+                                                                 int64_t srows, int64_t scols,
+                                                                 int64_t ld, uint32_t mask,
+                                                                 float* out) {
+    uint32_t m = 0;
+    const int64_t ncb = (scols + 7) >> 3, nkb = srows >> 4;
+    const int64_t total = ncb * nkb;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t kb = it / ncb, cb = it - kb * ncb;
+        const int64_t c0 = cb * 8;
+        const uint16_t* base = p + kb * 16 * ld + c0;
+        float v[8][16];
+        if (c0 + 8 <= scols) {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) {
+                const uint4 w = ldg_stream(base + t * ld);
+                float f[8];
+                unpack8(w, f);
+#pragma unroll
+                for (int c = 0; c < 8; ++c) v[c][t] = f[c];
+            }
+        } else {
+#pragma unroll
+            for (int t = 0; t < 16; ++t)
+#pragma unroll
+                for (int c = 0; c < 8; ++c)
+                    v[c][t] = (c0 + c < scols) ? __uint_as_float((uint32_t)base[t * ld + c] << 16)
+                                               : 0.0f;
+        }
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+            rht16(v[c], mask);
+            m = max(m, absmax_bits16(v[c]));
+        }
+    }
+    block_max_to_global(m, out);
+}
+
+// In-place amax -> S_enc (used when a quantiser computes its own amax).
+__global__ void k_amax_to_senc(float* gs) {
+    float s;
+    if (!global_encode_scale(*gs, &s)) {
+        s = __int_as_float(0x7FC00000);
+        record_device_error(NVFP4_DEV_NONFINITE);
+    }
+    *gs = s;
+}
+
+// ====================================================== quantise 1x16 ======
+struct QuantArgs {
+    const uint16_t* x;
+    int64_t rows, k, ld;        // logical operand [rows x k]; ld of the stored array
+    const float* scale_src;     // amax, or S_enc when src_is_senc
+    int src_is_senc;
+    float* gs_out;
+    float* gs_out2;             // copy of S_enc for the transposed operand (nullable)
+    uint8_t* codes;             // [rows x k/2]
+    uint8_t* scales;            // swizzled
+    uint32_t rht_mask;
+    uint64_t seed, stream_id;
+    // 2D transposed emit (optional)
+    uint8_t* codes_t;           // [k x rows/2]
+    uint8_t* scales_t;
+    int idx_transposed;         // SR index taken as (c * rows + r) (2D on a transposed view)
+    int write_primary;
+};
+
+template <bool RHT, bool SR>
+__device__ __forceinline__ void encode_block16(float* v, float s_enc, uint64_t idx0,
+                                               const QuantArgs& a, uint32_t* sb_out,
+                                               uint32_t* code_lo, uint32_t* code_hi) {
+    if (RHT) rht16(v, a.rht_mask);
+    float r_b;
+    *sb_out = block_scale(__uint_as_float(absmax_bits16(v)), s_enc, &r_b);
+#pragma unroll
+    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], r_b);
+    if (SR) {
+        *code_lo = e2m1x8_sr(v, sr_bits8(idx0 >> 3, a.seed, a.stream_id));
+        *code_hi = e2m1x8_sr(v + 8, sr_bits8((idx0 >> 3) + 1, a.seed, a.stream_id));
+    } else {
+        *code_lo = e2m1x8_rne(v);
+        *code_hi = e2m1x8_rne(v + 8);
+    }
+}
+
+// Non-transposed view: thread item = (row, group of 4 blocks).
+template <bool RHT, bool SR>
+__global__ void __launch_bounds__(kQuantThreads) k_quant1d_rows(QuantArgs a) {
+    float s_enc;
+    if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
+    const int64_t nkb = a.k >> 4;
+    const uint32_t ngroups = (uint32_t)((nkb + 3) >> 2);
+    const int64_t rows_pad = (a.rows + 127) & ~int64_t(127);
+    const int64_t total = rows_pad * ngroups;
+    const bool vec16 = (a.k & 31) == 0;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = it / ngroups;
+        const int64_t g = it - r * ngroups;
+        uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
+        if (r >= a.rows) {
+            *sdst = 0u;
+            continue;
+        }
+        const int nblk = (int)min64(4, nkb - g * 4);
+        const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64);
+        uint4 raw[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b)
+            if (b < nblk) {
+                raw[2 * b] = ldg_stream(src + 2 * b);
+                raw[2 * b + 1] = ldg_stream(src + 2 * b + 1);
+            }
+        uint32_t sw = 0, cw[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            cw[2 * b] = cw[2 * b + 1] = 0u;
+            if (b < nblk) {
+                float v[16];
+                unpack8(raw[2 * b], v);
+                unpack8(raw[2 * b + 1], v + 8);
+                uint32_t sb;
+                encode_block16<RHT, SR>(v, s_enc, (uint64_t)(r * a.k + g * 64 + b * 16), a, &sb,
+                                        &cw[2 * b], &cw[2 * b + 1]);
+                sw |= sb << (8 * b);
+            }
+        }
+        uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
+        if (nblk == 4 && vec16) {
+            reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+            reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+        } else {
+#pragma unroll
+            for (int b = 0; b < 4; ++b)
+                if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+        }
+        *sdst = sw;
+    }
+}
+
+// Transposed view (stored [k x rows]): thread item = (pair of logical rows,
+// group of 4 blocks along the logical k = the stored rows).
+template <bool RHT, bool SR>
+__global__ void __launch_bounds__(kQuantThreads) k_quant1d_cols(QuantArgs a) {
+    float s_enc;
+    if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
+    const int64_t nkb = a.k >> 4;
+    const int64_t ngroups = (nkb + 3) >> 2;
+    const int64_t rows_pad = (a.rows + 127) & ~int64_t(127);
+    const int64_t npairs = rows_pad >> 1;
+    const int64_t total = npairs * ngroups;
+    const bool vec16 = (a.k & 31) == 0;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t g = it / npairs;
+        const int64_t r0 = (it - g * npairs) * 2;
+        if (r0 >= a.rows) {
+            *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0, g * 4, ngroups)) = 0u;
+            *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups)) = 0u;
+            continue;
+        }
+        const bool has2 = r0 + 1 < a.rows;
+        const int nblk = (int)min64(4, nkb - g * 4);
+        uint32_t sw0 = 0, sw1 = 0, c0w[8], c1w[8];
+#pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            c0w[2 * b] = c0w[2 * b + 1] = c1w[2 * b] = c1w[2 * b + 1] = 0u;
+            if (b < nblk) {
+                const uint16_t* src = a.x + (g * 64 + b * 16) * a.ld + r0;
+                uint32_t w[16];
+                if (has2) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) w[t] = ldg_u32(src + t * a.ld);
+                } else {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) w[t] = (uint32_t)src[t * a.ld];
+                }
+                float v0[16], v1[16];
+#pragma unroll
+                for (int t = 0; t < 16; ++t) {
+                    v0[t] = bf16_lo(w[t]);
+                    v1[t] = bf16_hi(w[t]);
+                }
+                const int64_t kc = g * 64 + b * 16;
+                uint32_t sb;
+                encode_block16<RHT, SR>(v0, s_enc, (uint64_t)(r0 * a.k + kc), a, &sb, &c0w[2 * b],
+                                        &c0w[2 * b + 1]);
+                sw0 |= sb << (8 * b);
+                if (has2) {
+                    encode_block16<RHT, SR>(v1, s_enc, (uint64_t)((r0 + 1) * a.k + kc), a, &sb,
+                                            &c1w[2 * b], &c1w[2 * b + 1]);
+                    sw1 |= sb << (8 * b);
+                }
+            }
+        }
+#pragma unroll
+        for (int rr = 0; rr < 2; ++rr) {
+            if (rr == 1 && !has2) {
+                *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups)) = 0u;
+                continue;
+            }
+            const uint32_t* cw = rr ? c1w : c0w;
+            uint8_t* cdst = a.codes + (r0 + rr) * (a.k >> 1) + g * 32;
+            if (nblk == 4 && vec16) {
+                reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if (b < nblk)
+                        reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+            }
+            *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + rr, g * 4, ngroups)) =
+                rr ? sw1 : sw0;
+        }
+    }
+}
+
+// ===================================================== quantise 16x16 ======
+// CTA (128 threads) = 64 stored rows x 128 stored columns.  Warp w owns rows
+// 16w..16w+15; lane l owns row 16w + (l & 15) and columns 64*(l >> 4) ..
+// +63 of the CTA tile.  Grid: x over 128-column tiles, y over 64-row tiles
+// (covering the 128-padded row count).
+constexpr int k2DThreads = 128;
+
+template <bool RHT, bool SR, bool EMIT_T>
+__global__ void __launch_bounds__(k2DThreads) k_quant2d(QuantArgs a) {
+    __shared__ uint8_t tile_codes[64][64];     // [row][byte]: 128 nibbles per row
+    __shared__ uint8_t tile_sb[4][8];          // [row block][k block]
+    float s_enc;
+    if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t nkb = a.k >> 4;
+    const int64_t ngroups = (nkb + 3) >> 2;
+    const int64_t row0 = (int64_t)blockIdx.y * 64;
+    const int64_t r = row0 + warp * 16 + (lane & 15);
+    const int64_t g = (int64_t)blockIdx.x * 2 + (lane >> 4);
+    const bool row_ok = r < a.rows;
+    const bool grp_ok = g < ngroups;
+    const int nblk = grp_ok ? (int)min64(4, nkb - g * 4) : 0;
+
+    float v[4][16];
+    uint32_t lmax[4];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        if (row_ok && b < nblk) {
+            const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64 + b * 16);
+            unpack8(ldg_stream(src), v[b]);
+            unpack8(ldg_stream(src + 1), v[b] + 8);
+            if (RHT) rht16(v[b], a.rht_mask);
+            lmax[b] = absmax_bits16(v[b]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < 16; ++j) v[b][j] = 0.0f;
+            lmax[b] = 0u;
+        }
+    }
+    // 16x16 block amax: reduce over the 16 lanes holding the block's rows.
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+#pragma unroll
+        for (int off = 1; off < 16; off <<= 1)
+            lmax[b] = max(lmax[b], __shfl_xor_sync(0xFFFFFFFFu, lmax[b], off));
+    }
+    uint32_t sw = 0, cw[8];
+#pragma unroll
+    for (int b = 0; b < 4; ++b) {
+        float r_b;
+        const uint32_t sb = (b < nblk) ? block_scale(__uint_as_float(lmax[b]), s_enc, &r_b) : 0u;
+        if (b >= nblk) r_b = 0.0f;
+        sw |= sb << (8 * b);
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[b][j] = __fmul_rn(v[b][j], r_b);
+        if (SR) {
+            uint32_t lo = 0, hi = 0;
+            if (row_ok && b < nblk) {
+                const int64_t c0 = g * 64 + b * 16;
+                if (a.idx_transposed) {
+                    // index in the transposed logical layout: (r, c) -> c * rows + r
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) {
+                        const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
+                        const uint4 rb = sr_bits8(idx >> 3, a.seed, a.stream_id);
+                        const uint32_t sel = (uint32_t)(idx & 7u) >> 1;
+                        const uint32_t w = sel == 0 ? rb.x : sel == 1 ? rb.y : sel == 2 ? rb.z : rb.w;
+                        const uint32_t u = (idx & 1u) ? (w >> 16) : (w & 0xFFFFu);
+                        const uint32_t q = e2m1_sr(v[b][j], u);
+                        if (j < 8) lo |= q << (4 * j);
+                        else hi |= q << (4 * (j - 8));
+                    }
+                } else {
+                    const uint64_t idx0 = (uint64_t)(r * a.k + c0);
+                    lo = e2m1x8_sr(v[b], sr_bits8(idx0 >> 3, a.seed, a.stream_id));
+                    hi = e2m1x8_sr(v[b] + 8, sr_bits8((idx0 >> 3) + 1, a.seed, a.stream_id));
+                }
+            }
+            cw[2 * b] = lo;
+            cw[2 * b + 1] = hi;
+        } else {
+            cw[2 * b] = e2m1x8_rne(v[b]);
+            cw[2 * b + 1] = e2m1x8_rne(v[b] + 8);
+        }
+    }
+    // primary operand
+    if (a.write_primary && grp_ok) {
+        uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
+        if (r < ((a.rows + 127) & ~int64_t(127))) *sdst = row_ok ? sw : 0u;
+        if (row_ok) {
+            uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
+            if (nblk == 4 && (a.k & 31) == 0) {
+                reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            } else {
+#pragma unroll
+                for (int b = 0; b < 4; ++b)
+                    if (b < nblk)
+                        reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+            }
+        }
+    }
+    if (!EMIT_T) return;
+    // transposed operand: rows = k, k = a.rows (a multiple of 16 here)
+    {
+        uint4* trow = reinterpret_cast<uint4*>(&tile_codes[warp * 16 + (lane & 15)][32 * (lane >> 4)]);
+        const bool live = row_ok && grp_ok;
+        trow[0] = live ? make_uint4(cw[0], cw[1], cw[2], cw[3]) : make_uint4(0, 0, 0, 0);
+        trow[1] = live ? make_uint4(cw[4], cw[5], cw[6], cw[7]) : make_uint4(0, 0, 0, 0);
+        if ((lane & 15) == 0) {
+#pragma unroll
+            for (int b = 0; b < 4; ++b) tile_sb[warp][(lane >> 4) * 4 + b] = (sw >> (8 * b)) & 0xFFu;
+        }
+    }
+    __syncthreads();
+    const int64_t ct = (int64_t)blockIdx.x * 128 + threadIdx.x;   // row of the transposed operand
+    const int64_t kt = a.rows;                                     // its k
+    const int64_t ngroups_t = ((kt >> 4) + 3) >> 2;
+    const int64_t ct_pad = (a.k + 127) & ~int64_t(127);
+    if (ct >= ct_pad) return;
+    const int64_t gt = row0 >> 6;                                  // 4 blocks of 16 rows
+    if (gt >= ngroups_t) return;                                   // beyond the padded columns
+    uint32_t* sdst_t = reinterpret_cast<uint32_t*>(a.scales_t + scale_offset(ct, gt * 4, ngroups_t));
+    if (ct >= a.k) {
+        *sdst_t = 0u;
+        return;
+    }
+    const int c_local = threadIdx.x;                               // 0..127
+    const int kb_local = c_local >> 4;
+    *sdst_t = (uint32_t)tile_sb[0][kb_local] | ((uint32_t)tile_sb[1][kb_local] << 8) |
+              ((uint32_t)tile_sb[2][kb_local] << 16) | ((uint32_t)tile_sb[3][kb_local] << 24);
+    if (row0 >= a.rows) return;
+    uint32_t out[8];
+#pragma unroll
+    for (int wv = 0; wv < 8; ++wv) {
+        uint32_t word = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const uint8_t byte = tile_codes[wv * 8 + j][c_local >> 1];
+            const uint32_t nib = (c_local & 1) ? (byte >> 4) : (byte & 0xFu);
+            word |= nib << (4 * j);
+        }
+        out[wv] = word;
+    }
+    const int64_t rows_here = min64(64, a.rows - row0);     // multiple of 16
+    uint8_t* cdst = a.codes_t + ct * (kt >> 1) + (row0 >> 1);
+    if (rows_here == 64 && (kt & 31) == 0) {
+        reinterpret_cast<uint4*>(cdst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
+        reinterpret_cast<uint4*>(cdst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
+    } else {
+        for (int q = 0; q < rows_here / 16; ++q)
+            reinterpret_cast<uint2*>(cdst)[q] = make_uint2(out[2 * q], out[2 * q + 1]);
+    }
+}
+
+// ======================================================== dequantise ======
+template <bool BF16>
+__global__ void __launch_bounds__(kQuantThreads) k_dequant(const uint8_t* __restrict__ codes,
+                                                           const uint8_t* __restrict__ scales,
+                                                           const float* __restrict__ gs,
+                                                           int64_t rows, int64_t k, void* out,
+                                                           int64_t ld) {
+    const float inv = __frcp_rn(*gs);
+    const int64_t nkb = k >> 4;
+    const int64_t ngroups = (nkb + 3) >> 2;
+    const int64_t total = rows * nkb;
+    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
+         it += (int64_t)gridDim.x * blockDim.x) {
+        const int64_t r = it / nkb, kb = it - r * nkb;
+        const uint2 c = *reinterpret_cast<const uint2*>(codes + r * (k >> 1) + kb * 8);
+        const float sb = e4m3_value(scales[scale_offset(r, kb, ngroups)]);
+        float o[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) {
+            const uint32_t q = ((j < 8 ? c.x : c.y) >> (4 * (j & 7))) & 0xFu;
+            const float mag = (q & 7u) < 4u ? __fmul_rn((float)(q & 7u), 0.5f)
+                              : (q & 7u) < 6u ? (float)((q & 7u) - 2u)
+                              : (q & 7u) == 6u ? 4.0f : 6.0f;
+            const float qv = (q & 8u) ? -mag : mag;
+            o[j] = __fmul_rn(__fmul_rn(qv, sb), inv);
+        }
+        if (BF16) {
+            uint32_t p[8];
+#pragma unroll
+            for (int j = 0; j < 8; ++j) {
+                const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+                p[j] = *reinterpret_cast<const uint32_t*>(&h);
+            }
+            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + r * ld + kb * 16);
+            dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+            dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+        } else {
+            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ld + kb * 16);
+#pragma unroll
+            for (int j = 0; j < 4; ++j) dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+        }
+    }
+}
+
+}  // namespace nvfp4

@@ -1,0 +1,104 @@
+"""Host-side checks of the C ABI that need no GPU: the library loads, exports
+every entry point declared in include/nvfp4.h, the pure host helpers agree
+with the oracle, and argument validation rejects bad calls before anything
+is launched (validation runs before any CUDA call)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+
+import oracle
+
+
+@pytest.fixture(scope="module")
+def nv():
+    from nvfp4_block_scaled_29_b300 import build
+    build.build()
+    import nvfp4_block_scaled_29_b300 as m
+    return m
+
+
+def _declared_functions():
+    text = open(os.path.join(ROOT, "include", "nvfp4.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(nvfp4_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_header_declares_the_path_calls():
+    names = _declared_functions()
+    for required in ["nvfp4_amax", "nvfp4_quantize_1d", "nvfp4_quantize_2d", "nvfp4_rht_quantize",
+                     "nvfp4_dequantize", "nvfp4_gemm"]:
+        assert required in names
+
+
+def test_library_exports_every_declared_symbol(nv):
+    lib = ctypes.CDLL(nv.LIB_PATH)
+    for name in _declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_rht_mask_from_seed_matches_oracle(nv):
+    for seed in [0, 1, 2002, 2**40 + 3, 2**64 - 1]:
+        assert nv.nvfp4_rht_mask_from_seed(seed) == oracle.rht_mask_from_seed(seed)
+
+
+def test_scale_bytes_matches_oracle(nv):
+    for rows, k in [(1, 16), (128, 64), (129, 80), (8192, 5120), (20480, 8192), (5, 1040)]:
+        assert nv.nvfp4_scale_bytes(rows, k) == oracle.scale_bytes(rows, k)
+    assert nv.nvfp4_scale_bytes(0, 64) == 0
+
+
+def test_status_strings(nv):
+    for s in range(7):
+        assert nv.status_string(s) and "unknown" not in nv.status_string(s)
+
+
+def _view(nv, ptr, rows, cols, ld, tr=0):
+    return nv.Bf16View(ptr, rows, cols, ld, tr)
+
+
+def _q(nv, rows, k, codes=0x1000, scales=0x2000, gs=0x3000):
+    return nv.QStruct(codes, scales, gs, rows, k, 0)
+
+
+def test_validation_rejects_bad_calls(nv):
+    L = nv.lib
+    good = _view(nv, 0x10000, 32, 64, 64)
+    q = _q(nv, 32, 64)
+    # k not a multiple of 16
+    assert L.nvfp4_quantize_1d(_view(nv, 0x10000, 32, 40, 40), None, 0, 0, 0,
+                               ctypes.byref(_q(nv, 32, 40)), None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    # misaligned input pointer / leading dimension
+    assert L.nvfp4_quantize_1d(_view(nv, 0x10002, 32, 64, 64), None, 0, 0, 0, ctypes.byref(q),
+                               None) == nv.NVFP4_ERR_MISALIGNED
+    assert L.nvfp4_quantize_1d(_view(nv, 0x10000, 32, 64, 68), None, 0, 0, 0, ctypes.byref(q),
+                               None) == nv.NVFP4_ERR_MISALIGNED
+    # ld smaller than the row
+    assert L.nvfp4_quantize_1d(_view(nv, 0x10000, 32, 64, 32), None, 0, 0, 0, ctypes.byref(q),
+                               None) == nv.NVFP4_ERR_INVALID_ARG
+    # output shape mismatch, null output, bad rounding mode
+    assert L.nvfp4_quantize_1d(good, None, 0, 0, 0, ctypes.byref(_q(nv, 16, 64)), None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_1d(good, None, 0, 0, 0, None, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_1d(good, None, 7, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    # amax aliasing the output global scale
+    assert L.nvfp4_quantize_1d(good, ctypes.c_void_p(0x3000), 0, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    # RHT mask out of range / zero for rht_quantize
+    assert L.nvfp4_rht_quantize(good, 0x10000, None, 0, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_rht_quantize(good, 0, None, 0, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    # 2D transposed emit needs rows % 16 == 0
+    bad_rows = _view(nv, 0x10000, 24, 64, 64)
+    assert L.nvfp4_quantize_2d(bad_rows, None, 0, 0, 0, ctypes.byref(_q(nv, 24, 64)),
+                               ctypes.byref(_q(nv, 64, 24)), None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    # GEMM: k mismatch, K % 32, misaligned output leading dimension
+    a, b = _q(nv, 128, 256), _q(nv, 256, 256)
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(_q(nv, 256, 224)), 0x4000, 0, 256, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_gemm(ctypes.byref(_q(nv, 128, 48)), ctypes.byref(_q(nv, 256, 48)), 0x4000, 0, 256, None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 1, 260, None) == nv.NVFP4_ERR_MISALIGNED
+    assert L.nvfp4_gemm(ctypes.byref(a), ctypes.byref(b), 0x4000, 0, 128, None) == nv.NVFP4_ERR_INVALID_ARG
+    # dequantize: misaligned output
+    assert L.nvfp4_dequantize(ctypes.byref(q), ctypes.c_void_p(0x4004), 0, 64, None) == nv.NVFP4_ERR_MISALIGNED
+    # amax: null output
+    assert L.nvfp4_amax(good, 0, None, None) == nv.NVFP4_ERR_INVALID_ARG

@@ -1,0 +1,287 @@
+"""GPU path vs CPU oracle on the same seeded inputs, element by element.
+
+Sizes span several tiles and ragged tails; quantised codes and scales must
+be bit-exact, GEMM outputs within |y - y_ref| <= 2e-5 * sum_k |a_k b_k|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_util import (assert_q_equal, dev_bf16, expected_transpose, gemm_bound_check,
+                      gpu_quantize)
+
+pytestmark = pytest.mark.gpu
+
+MASK = 0x9D2B
+
+
+@pytest.fixture(scope="module")
+def nv():
+    import nvfp4_block_scaled_29_b300 as m
+    assert torch.cuda.is_available()
+    return m
+
+
+def _data(rows, k, seed, kind="normal"):
+    if kind == "t":
+        return synth.student_t_bf16((rows, k), seed, 3, 1e-3)
+    return synth.normal_bf16((rows, k), seed, 1.0, 0.002, 60.0)
+
+
+# ------------------------------------------------------------------- amax --
+@pytest.mark.parametrize("rows,k", [(1, 16), (7, 48), (130, 272), (512, 1024), (3, 4096)])
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("mask", [0, MASK])
+def test_amax(nv, rows, k, transposed, mask):
+    x = _data(rows, k, rows * 31 + k)
+    stored = x.T.copy() if transposed else x                 # stored array of the view
+    ld = ((stored.shape[1] + 7) // 8) * 8 + (8 if rows % 2 else 0)
+    d = dev_bf16(stored, ld)
+    a = nv.nvfp4_amax(d, mask, transposed=transposed)
+    torch.cuda.synchronize()
+    assert float(a.cpu()[0]) == oracle.amax(stored, transposed=transposed, rht_mask=mask)
+
+
+def test_amax_nan_and_inf(nv):
+    x = _data(64, 64, 5)
+    x[10, 17] = 0x7F80                                        # +Inf
+    a = nv.nvfp4_amax(dev_bf16(x))
+    assert float(a.cpu()[0]) == float("inf")
+    x[3, 3] = 0xFFC1                                          # NaN
+    a = nv.nvfp4_amax(dev_bf16(x))
+    assert np.isnan(float(a.cpu()[0]))
+
+
+def test_nonfinite_amax_is_reported(nv):
+    x = _data(32, 64, 6)
+    x[1, 1] = 0x7F80
+    d = dev_bf16(x)
+    q = nv.QTensor(32, 64)
+    a = nv.nvfp4_amax(d)
+    nv.nvfp4_quantize_1d(d, a, nv.NVFP4_RNE, 0, 0, q)
+    assert nv.nvfp4_get_status() == nv.NVFP4_ERR_NONFINITE
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK                # read clears it
+    assert np.isnan(float(q.global_scale.cpu()[0]))
+
+
+# ------------------------------------------------------- 1x16 quantisation --
+SHAPES_1D = [(1, 16), (3, 48), (100, 80), (128, 256), (130, 272), (257, 1040), (64, 4096)]
+
+
+@pytest.mark.parametrize("rows,k", SHAPES_1D)
+@pytest.mark.parametrize("transposed", [False, True])
+@pytest.mark.parametrize("sr", [False, True])
+@pytest.mark.parametrize("mask", [0, MASK])
+def test_quantize_1d(nv, rows, k, transposed, sr, mask):
+    x = _data(rows, k, 1000 + rows + k, "t" if sr else "normal")   # logical [rows x k]
+    stored = x.T.copy() if transposed else x
+    ld = ((stored.shape[1] + 7) // 8) * 8 + 8
+    d = dev_bf16(stored, ld)
+    q, _, _ = gpu_quantize(nv, d, transposed=transposed, mask=mask, sr=sr, seed=77, sid=5)
+    ref = oracle.quantize(stored, transposed=transposed, rht_mask=mask, sr=sr, seed=77, stream_id=5)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, f"1d {rows}x{k} t={transposed} sr={sr} rht={mask}")
+
+
+@pytest.mark.parametrize("transposed", [False, True])
+def test_quantize_own_amax(nv, transposed):
+    """amax == NULL: the call computes the amax itself."""
+    x = _data(96, 128, 3)
+    stored = x.T.copy() if transposed else x
+    q, _, _ = gpu_quantize(nv, dev_bf16(stored), transposed=transposed, own_amax=True)
+    ref = oracle.quantize(stored, transposed=transposed)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "own amax")
+    q, _, _ = gpu_quantize(nv, dev_bf16(stored), transposed=transposed, own_amax=True, mask=MASK, sr=True, seed=3)
+    ref = oracle.quantize(stored, transposed=transposed, rht_mask=MASK, sr=True, seed=3)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "own amax rht sr")
+
+
+def test_quantize_edge_values(nv):
+    """Zero blocks, ties of the E2M1 grid, signed zeros and a zero tensor."""
+    rows, k = 32, 64
+    base = np.zeros((rows, k), np.float32)
+    base[0, :16] = [6, 0.25 * 6 / 6, 0.75, 1.25, 1.75, 2.5, 3.5, 5, -0.0, -0.1, 0.1, 4, 3, 2, 1, 0.5]
+    base[1, 16:32] = -np.linspace(0, 6, 16)
+    base[2, :] = 1e-3
+    base[3, :] = -1e-30
+    x = synth._to_bf16_bits(base)
+    q, _, _ = gpu_quantize(nv, dev_bf16(x))
+    ref = oracle.quantize(x)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "edge values")
+    z = np.zeros((16, 32), np.uint16)
+    q, _, _ = gpu_quantize(nv, dev_bf16(z))
+    ref = oracle.quantize(z)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "zero tensor")
+
+
+def test_quantize_tiny_amax(nv):
+    """amax in the bf16 subnormal range: S_enc saturates to FLT_MAX."""
+    x = np.zeros((16, 32), np.uint16)
+    x[0, 0] = 0x0001
+    x[5, 7] = 0x8003
+    q, _, _ = gpu_quantize(nv, dev_bf16(x))
+    ref = oracle.quantize(x)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "tiny amax")
+
+
+# ------------------------------------------------------ 16x16 quantisation --
+SHAPES_2D = [(16, 16), (32, 48), (48, 80), (128, 256), (144, 272), (256, 1040), (80, 192)]
+
+
+@pytest.mark.parametrize("rows,k", SHAPES_2D)
+@pytest.mark.parametrize("sr", [False, True])
+@pytest.mark.parametrize("emit_t", [False, True])
+def test_quantize_2d(nv, rows, k, sr, emit_t):
+    w = synth.normal_bf16((rows, k), 2000 + rows + k, 0.02)
+    q, qt, _ = gpu_quantize(nv, dev_bf16(w, k + 8), block2d=True, sr=sr, seed=9, sid=2, emit_t=emit_t)
+    ref = oracle.quantize(w, block2d=True, sr=sr, seed=9, stream_id=2)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, f"2d {rows}x{k} sr={sr}")
+    if emit_t:
+        codes_t, scales_t = expected_transpose(ref)
+        assert_q_equal(qt, codes_t, scales_t, ref.s_enc, f"2d-T {rows}x{k} sr={sr}")
+
+
+@pytest.mark.parametrize("rows,k", [(37, 64), (5, 16), (130, 96)])
+def test_quantize_2d_ragged_rows(nv, rows, k):
+    w = synth.normal_bf16((rows, k), 3000 + rows, 0.02)
+    q, _, _ = gpu_quantize(nv, dev_bf16(w), block2d=True)
+    ref = oracle.quantize(w, block2d=True)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "2d ragged")
+
+
+@pytest.mark.parametrize("sr", [False, True])
+def test_quantize_2d_transposed_view(nv, sr):
+    """16x16 blocks of W^T read from W stored [k x rows]; out_t is W itself."""
+    stored = synth.normal_bf16((96, 160), 41, 0.02)      # logical operand [160 x 96]
+    q, qt, _ = gpu_quantize(nv, dev_bf16(stored), transposed=True, block2d=True, sr=sr, seed=4,
+                            emit_t=True)
+    ref = oracle.quantize(stored, transposed=True, block2d=True, sr=sr, seed=4)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "2d transposed view")
+    codes_t, scales_t = expected_transpose(ref)
+    assert_q_equal(qt, codes_t, scales_t, ref.s_enc, "2d transposed view, out_t")
+
+
+@pytest.mark.parametrize("rows,k", [(32, 64), (144, 272)])
+@pytest.mark.parametrize("sr", [False, True])
+def test_rht_quantize_2d(nv, rows, k, sr):
+    w = synth.normal_bf16((rows, k), 4000 + rows, 0.02, 0.01, 30.0)
+    q, _, _ = gpu_quantize(nv, dev_bf16(w), block2d=True, mask=MASK, sr=sr, seed=1)
+    ref = oracle.quantize(w, block2d=True, rht_mask=MASK, sr=sr, seed=1)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "rht 2d")
+
+
+def test_dequant_consistency_2d(nv):
+    """dequant(W^T q) == dequant(W q)^T bit for bit (forward and backward see
+    the same quantised weight)."""
+    w = synth.normal_bf16((64, 128), 77, 0.02)
+    q, qt, _ = gpu_quantize(nv, dev_bf16(w), block2d=True, sr=True, seed=8, emit_t=True)
+    a = torch.empty((64, 128), dtype=torch.float32, device="cuda")
+    b = torch.empty((128, 64), dtype=torch.float32, device="cuda")
+    nv.nvfp4_dequantize(q, a)
+    nv.nvfp4_dequantize(qt, b)
+    torch.cuda.synchronize()
+    assert torch.equal(a.T.cpu(), b.cpu())
+
+
+# ---------------------------------------------------------- dequantise ----
+@pytest.mark.parametrize("rows,k", [(1, 16), (100, 80), (257, 1040)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_dequantize(nv, rows, k, bf16):
+    codes, scales = synth.random_operand(rows, k, rows + k, 0x01, 0x7E)
+    q = oracle.Quantized(codes, scales, np.float32(3.7e2), rows, k)
+    g = nv.QTensor(rows, k)
+    g.codes.copy_(torch.from_numpy(codes))
+    g.scales.copy_(torch.from_numpy(q.scales))
+    g.global_scale.fill_(float(q.s_enc))
+    ld = k + 8
+    out = torch.empty((rows, ld), dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")[:, :k]
+    nv.nvfp4_dequantize(g, out)
+    torch.cuda.synchronize()
+    ref = oracle.dequantize(q, out_bf16=bf16)
+    got = out.cpu().view(torch.int16).numpy().view(np.uint16) if bf16 else out.cpu().numpy()
+    np.testing.assert_array_equal(got, ref)
+
+
+# -------------------------------------------------------------------- GEMM --
+def _upload_operand(nv, codes, scales_plain, s_enc, rows, k):
+    g = nv.QTensor(rows, k)
+    g.codes.copy_(torch.from_numpy(codes))
+    sw = oracle.swizzle_scales(scales_plain, rows, k)
+    g.scales.copy_(torch.from_numpy(sw))
+    g.global_scale.fill_(float(s_enc))
+    return g, sw
+
+
+@pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (200, 300, 96), (1, 1, 32),
+                                   (130, 260, 320), (384, 256, 1024), (128, 128, 4160)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_gemm_random_operands(nv, M, N, K, bf16):
+    ca, sa = synth.random_operand(M, K, M + 7 * K)
+    cb, sb = synth.random_operand(N, K, N + 13 * K)
+    SA, SB = np.float32(2.5), np.float32(0.375)
+    ga, swa = _upload_operand(nv, ca, sa, SA, M, K)
+    gb, swb = _upload_operand(nv, cb, sb, SB, N, K)
+    d = torch.empty((M, ((N + 7) // 8) * 8 + 8), dtype=torch.bfloat16 if bf16 else torch.float32,
+                    device="cuda")[:, :N]
+    d.fill_(float("nan"))
+    nv.nvfp4_gemm(ga, gb, d)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK
+    y_ref, ab = oracle.gemm_full(ca, swa, SA, cb, swb, SB, M, N, K)
+    gemm_bound_check(d.float().cpu().numpy(), y_ref, ab, bf16, f"gemm {M}x{N}x{K} bf16={bf16}")
+
+
+def test_gemm_integer_exact(nv):
+    """Scales 1.0 and codes in {0, +1, -1}: an exact integer GEMM."""
+    rng = np.random.default_rng(5)
+    M, N, K = 256, 256, 512
+    pick = np.array([0, 2, 10], np.uint8)
+    av, bv = rng.integers(0, 3, (M, K)), rng.integers(0, 3, (N, K))
+    pack = lambda v: (pick[v[:, 0::2]] | (pick[v[:, 1::2]] << 4)).astype(np.uint8)
+    ga, _ = _upload_operand(nv, pack(av), np.full((M, K // 16), 0x38, np.uint8), 1.0, M, K)
+    gb, _ = _upload_operand(nv, pack(bv), np.full((N, K // 16), 0x38, np.uint8), 1.0, N, K)
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    nv.nvfp4_gemm(ga, gb, d)
+    torch.cuda.synchronize()
+    sv = np.array([0, 1, -1])
+    ref = sv[av].astype(np.int64) @ sv[bv].astype(np.int64).T
+    np.testing.assert_array_equal(d.cpu().numpy(), ref.astype(np.float32))
+
+
+def test_gemm_scale_rows_are_distinct(nv):
+    """Each row of A and of B gets its own scale (power of two by row): a
+    wrong scale layout in shared or tensor memory shows up as a wrong row or
+    column of D."""
+    M, N, K = 256, 256, 256
+    rng = np.random.default_rng(6)
+    ca = np.full((M, K // 2), 0x22, np.uint8)                 # all elements 1.0
+    cb = np.full((N, K // 2), 0x22, np.uint8)
+    ea = rng.integers(0x20, 0x50, size=(M, 1)).repeat(K // 16, 1).astype(np.uint8)
+    eb = rng.integers(0x20, 0x50, size=(N, 1)).repeat(K // 16, 1).astype(np.uint8)
+    ea[:, 3] = 0x38                                           # one block of each row at 1.0
+    ga, swa = _upload_operand(nv, ca, ea, 1.0, M, K)
+    gb, swb = _upload_operand(nv, cb, eb, 1.0, N, K)
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    nv.nvfp4_gemm(ga, gb, d)
+    torch.cuda.synchronize()
+    y_ref, ab = oracle.gemm_full(ca, swa, 1.0, cb, swb, 1.0, M, N, K)
+    gemm_bound_check(d.cpu().numpy(), y_ref, ab, False, "per-row scales")
+
+
+# --------------------------------------------------- tiny forward linear ---
+def test_tiny_forward_linear(nv):
+    """The tiny forward workload end to end: X [128 x 256] 1x16 RNE, W
+    [256 x 256] 16x16, Y = X W^T with FP32 accumulation and FP32 output."""
+    x, w = synth.tiny_forward(0)
+    dx, dw = dev_bf16(x), dev_bf16(w)
+    qx, _, _ = gpu_quantize(nv, dx)
+    qw, _, _ = gpu_quantize(nv, dw, block2d=True)
+    y = torch.empty((128, 256), dtype=torch.float32, device="cuda")
+    nv.nvfp4_gemm(qx, qw, y)
+    torch.cuda.synchronize()
+    ox, ow = oracle.quantize(x), oracle.quantize(w, block2d=True)
+    assert_q_equal(qx, ox.codes, ox.scales, ox.s_enc, "X")
+    assert_q_equal(qw, ow.codes, ow.scales, ow.s_enc, "W")
+    yr, ab = oracle.gemm_full(ox.codes, ox.scales, ox.s_enc, ow.codes, ow.scales, ow.s_enc, 128, 256, 256)
+    gemm_bound_check(y.cpu().numpy(), yr, ab, False, "tiny forward")
