@@ -153,7 +153,12 @@ class Step:
         host["dw"].copy_(self.dw.view(torch_int16(self.torch)), non_blocking=True)
 
     def flush_l2(self):
+        """Untimed preamble of a step: overwrite 256 MiB (> 126 MB of L2), then
+        hold the stream in a short device spin so the host enqueues the whole
+        step before the GPU reaches it (launch gaps then never enter the
+        events' intervals)."""
         self.flush_buf.fill_(1)
+        self.torch.cuda._sleep(3_000_000)
 
     def run(self, timed: bool):
         nv, a, ev = self.nv, self.amax, self.ev
@@ -189,6 +194,20 @@ class Step:
         return [self.ev[2 * j].elapsed_time(self.ev[2 * j + 1]) for j in range(self.n_ev // 2)]
 
 
+# single calls of the step, for kernel-level profiling (bench.py --profile-case)
+PROFILE_CASES = {
+    "gemm_fwd": lambda s: s.nv.nvfp4_gemm(s.qx, s.qw, s.y),
+    "gemm_dgrad": lambda s: s.nv.nvfp4_gemm(s.qdy, s.qwt, s.dx),
+    "gemm_wgrad": lambda s: s.nv.nvfp4_gemm(s.qdyt, s.qxt, s.dw),
+    "amax_dy": lambda s: s.nv.nvfp4_amax(s.dy, 0, s.amax[2:3]),
+    "q1d_x": lambda s: s.nv.nvfp4_quantize_1d(s.x, s.amax[0:1], s.nv.NVFP4_RNE, 0, 0, s.qx),
+    "q1d_dy_sr": lambda s: s.nv.nvfp4_quantize_1d(s.dy, s.amax[2:3], s.nv.NVFP4_SR, SR_SEED, 1, s.qdy),
+    "q2d_w": lambda s: s.nv.nvfp4_quantize_2d(s.w, s.amax[1:2], s.nv.NVFP4_RNE, 0, 0, s.qw, s.qwt),
+    "rhtq_dyt_sr": lambda s: s.nv.nvfp4_rht_quantize(s.dy, s.mask, s.amax[3:4], s.nv.NVFP4_SR,
+                                                      SR_SEED, 2, s.qdyt, transposed=True),
+    "amax_rht_dyt": lambda s: s.nv.nvfp4_amax(s.dy, s.mask, s.amax[3:4], transposed=True),
+}
+
 GEMM_IDX = (4, 7, 12)
 QUANT_IDX = tuple(j for j in range(13) if j not in GEMM_IDX)
 
@@ -206,14 +225,13 @@ def make_host_inputs():
 
 
 # ----------------------------------------------------------- CPU oracle ----
-def oracle_step_sample(threads: int | None = None):
+def oracle_step_sample(threads: int | None = None, rows: int = 16, pts: int = 256):
     """Time the CPU oracle on a bounded sample of the step and extrapolate
-    to one full step.  Sample: 16 rows of every quantised operand (of the
-    8192..20480 rows) and 256 output points of each GEMM (full K)."""
+    to one full step.  Sample: `rows` rows of every quantised operand (of the
+    8192..20480 rows) and `pts` output points of each GEMM (full K)."""
     import oracle
     import synth
 
-    rows = 16
     rng = np.random.default_rng(0)
     x = synth.activations(SEED_X, tokens=rows * 64)           # shape-compatible slices
     w = synth.weights(SEED_W, ffn=rows * 64)
@@ -238,7 +256,6 @@ def oracle_step_sample(threads: int | None = None):
         full_elems = full_rows * k_full
         t_quant += t_amax * full_elems / arr.size + t_q * full_elems / (rows * k_here)
     t_gemm = 0.0
-    pts = 256
     for (M, N, K) in [(TOKENS, FFN, HIDDEN), (TOKENS, HIDDEN, FFN), (FFN, HIDDEN, TOKENS)]:
         ca, sa = synth.random_operand(64, K, 1)
         cb, sb = synth.random_operand(64, K, 2)
@@ -289,6 +306,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
+                    help="after one full untimed step, launch only this call --steps times "
+                         "(a target for ncu -k; prints nothing)")
     args = ap.parse_args()
     if args.impl == "reference":
         return run_reference(args)
@@ -313,6 +333,15 @@ def main():
     host["dw"] = torch.empty((FFN, HIDDEN), dtype=torch.int16).pin_memory()
     step = Step(nv, torch, host)
     torch.cuda.synchronize()
+    if args.profile_case:
+        step.run(timed=False)
+        for _ in range(args.steps):
+            PROFILE_CASES[args.profile_case](step)
+        torch.cuda.synchronize()
+        st = nv.nvfp4_get_status()
+        if st != nv.NVFP4_OK:
+            raise SystemExit(f"device status: {nv.status_string(st)}")
+        return 0
 
     for _ in range(max(3, args.warmup)):
         step.flush_l2()
@@ -410,7 +439,7 @@ def main():
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        out["cpu_baseline"] = oracle_step_sample()
+        out["cpu_baseline"] = oracle_step_sample(rows=96, pts=2048)
         out["cpu_baseline"].pop("seconds_per_step_extrapolated", None)
     if rank == 0:
         print(json.dumps(out))

@@ -255,13 +255,32 @@ bool make_code_map(CUtensorMap* m, const uint8_t* codes, int64_t rows, int64_t k
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows x cols] bf16 output, box = 64 columns x 32 rows, 128-byte swizzle.
+bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    const cuuint32_t box[2] = {64u, 32u};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, d, dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+int gemm_smem_request(bool tma_epi) {
+    return tma_epi ? gemm::SMEM_LIMIT : gemm::smem_bytes_for(false);
+}
+
 bool gemm_smem_ready() {
     static std::atomic<int> done[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load()) return true;
-    if (cudaFuncSetAttribute(gemm::k_gemm_nvfp4, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gemm::SMEM_BYTES) != cudaSuccess)
+    if (cudaFuncSetAttribute(gemm::k_gemm_nvfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm_smem_request(true)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm::k_gemm_nvfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm_smem_request(false)) != cudaSuccess)
         return false;
     done[dev].store(1);
     return true;
@@ -359,9 +378,11 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
         return cudaMemset2DAsync(d, ldd * esz, 0, N * esz, M, stream) == cudaSuccess ? NVFP4_OK
                                                                                       : NVFP4_ERR_CUDA;
     }
-    CUtensorMap ta, tb;
+    CUtensorMap ta, tb, td;
     if (!make_code_map(&ta, a->codes, M, K, gemm::BM) || !make_code_map(&tb, b->codes, N, K, gemm::BN))
         return NVFP4_ERR_CUDA;
+    std::memset(&td, 0, sizeof(td));
+    if (d_is_bf16 && !make_out_map(&td, d, M, N, ldd)) return NVFP4_ERR_CUDA;
     if (!gemm_smem_ready()) return NVFP4_ERR_CUDA;
     gemm::Args g{};
     g.sfa = a->scales;
@@ -382,7 +403,10 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
     g.b_row_tiles = (int)cdiv(N, 128);
     const int64_t tiles = (int64_t)g.m_tiles * g.n_tiles;
     const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
-    gemm::k_gemm_nvfp4<<<grid, gemm::THREADS, gemm::SMEM_BYTES, stream>>>(ta, tb, g);
+    if (d_is_bf16)
+        gemm::k_gemm_nvfp4<true><<<grid, gemm::THREADS, gemm_smem_request(true), stream>>>(ta, tb, td, g);
+    else
+        gemm::k_gemm_nvfp4<false><<<grid, gemm::THREADS, gemm_smem_request(false), stream>>>(ta, tb, td, g);
     return launch_status();
 }
 
