@@ -84,31 +84,28 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float* v) {
 
 // Stochastic E2M1 rounding of one value with 16 random bits.  With lo <= |v|
 // < hi the neighbouring grid values, the code moves up iff
-// u16 < floor(frac * 2^16), frac = (|v| - lo) / (hi - lo).  Every step is
-// exact: |v| - lo by Sterbenz (or lo == 0), the spacing is a power of two.
+// u16 < F = floor(frac * 2^16), frac = (|v| - lo) / (hi - lo).  Branch-free
+// on the bit pattern of |v| (exponent e, 23-bit mantissa m):
+//   |v| >= 1   : lo = 2^e * (1 + m22/2), code_lo = 2 (e + 1) + m22, and frac
+//                is the 22 mantissa bits below m22, so F = bits 21..6;
+//   0.5..1     : lo = 0.5, code_lo = 1, frac = m / 2^23, so F = bits 22..7;
+//   |v| < 0.5  : lo = 0, code_lo = 0, frac = 2|v|, F = floor(|v| * 2^17)
+//                (an exact power-of-two scaling);
+//   |v| >= 6   : saturates to code 7.
 __device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u16) {
-    uint32_t sign = (__float_as_uint(v) >> 28) & 8u;
-    float a = fabsf(v);
-    if (a >= 6.0f) return sign | 7u;
-    uint32_t code;
-    float lo, inv_step;
-    if (a < 2.0f) {                    // grid 0, 0.5, 1, 1.5, (2): spacing 0.5
-        code = (uint32_t)__fmul_rz(a, 2.0f);
-        lo = __fmul_rn((float)code, 0.5f);
-        inv_step = 2.0f;
-    } else if (a < 4.0f) {             // grid 2, 3, (4): spacing 1
-        uint32_t f = (uint32_t)a;
-        code = f + 2u;
-        lo = (float)f;
-        inv_step = 1.0f;
-    } else {                           // grid 4, 6: spacing 2
-        code = 6u;
-        lo = 4.0f;
-        inv_step = 0.5f;
-    }
-    float frac = __fmul_rn(__fsub_rn(a, lo), inv_step);
-    uint32_t F = (uint32_t)__fmul_rz(frac, 65536.0f);
-    return sign | (code + (u16 < F ? 1u : 0u));
+    const uint32_t bits = __float_as_uint(v);
+    const uint32_t sign = (bits >> 28) & 8u;
+    const uint32_t ab = bits & 0x7FFFFFFFu;
+    const uint32_t code_n = ((ab >> 23) - 126u) * 2u + ((ab >> 22) & 1u);
+    const uint32_t f_n = (ab >> 6) & 0xFFFFu;
+    const uint32_t f_h = (ab >> 7) & 0xFFFFu;
+    const uint32_t f_s = (uint32_t)__fmul_rz(__uint_as_float(ab), 131072.0f);
+    const bool ge1 = ab >= 0x3F800000u, ge05 = ab >= 0x3F000000u;
+    uint32_t code = ge1 ? code_n : (ge05 ? 1u : 0u);
+    const uint32_t F = ge1 ? f_n : (ge05 ? f_h : f_s);
+    code += (u16 < F) ? 1u : 0u;
+    code = (ab >= 0x40C00000u) ? 7u : code;
+    return sign | code;
 }
 
 // ---------------------------------------------------------------- Philox --
@@ -121,9 +118,10 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1
             k0 += 0x9E3779B9u;
             k1 += 0xBB67AE85u;
         }
-        const uint32_t hi0 = __umulhi(0xD2511F53u, c.x), lo0 = 0xD2511F53u * c.x;
-        const uint32_t hi1 = __umulhi(0xCD9E8D57u, c.z), lo1 = 0xCD9E8D57u * c.z;
-        c = make_uint4(hi1 ^ c.y ^ k0, lo1, hi0 ^ c.w ^ k1, lo0);
+        const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u;
+        const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57u;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
+                       (uint32_t)p0);
     }
     return c;
 }
@@ -135,17 +133,40 @@ __device__ __forceinline__ uint4 sr_bits8(uint64_t g, uint64_t seed, uint64_t st
                          (uint32_t)seed, (uint32_t)(seed >> 32));
 }
 
+// Stochastic rounding realised as "add random bits below the kept precision,
+// then truncate": with rp = 65535 - u16 placed just below the kept bits of
+// |v| (the 16 bits that hold floor(frac * 2^16)), a carry reaches the kept
+// bits exactly when floor(frac * 2^16) > u16, i.e. the rule above.  The kept
+// precision is bit 22 for |v| >= 1 (spacing 2^(e-1)) and bit 23 for
+// 0.5 <= |v| < 1 (spacing 0.5); |v| < 0.5 (grid 0, 0.5) is first moved to
+// [0.5, 1) by a round-toward-zero add of 0.5, which keeps floor(frac * 2^16),
+// and moved back by an exact subtraction.  The result is the chosen grid
+// value (exact, sign kept), so RNE conversion returns its code unchanged;
+// |v| is clamped to 8 first (anything >= 6 saturates to 6).
+__device__ __forceinline__ float sr_grid_value(float v, uint32_t rp) {
+    const uint32_t bits = __float_as_uint(v);
+    const float a = fminf(__uint_as_float(bits & 0x7FFFFFFFu), 8.0f);
+    const uint32_t ab = __float_as_uint(a);
+    const bool ge1 = ab >= 0x3F800000u, ge05 = ab >= 0x3F000000u;
+    const float a2 = ge05 ? a : __fadd_rz(a, 0.5f);
+    const uint32_t sh = ge1 ? 6u : 7u;
+    const uint32_t keep = ge1 ? 0xFFC00000u : 0xFF800000u;
+    float q = __uint_as_float((__float_as_uint(a2) + (rp << sh)) & keep);
+    q = ge05 ? q : __fsub_rn(q, 0.5f);
+    return __uint_as_float(__float_as_uint(q) | (bits & 0x80000000u));
+}
+
 // Eight values -> eight SR codes (element 0 in the lowest nibble), r = the
-// Philox block of these 8 elements.
+// Philox block of these 8 elements (slice j: word j/2, low half first).
 __device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 r) {
-    const uint32_t w[4] = {r.x, r.y, r.z, r.w};
-    uint32_t out = 0;
+    const uint32_t w[4] = {~r.x, ~r.y, ~r.z, ~r.w};      // both halves become 65535 - u16
+    float g[8];
 #pragma unroll
     for (int j = 0; j < 8; ++j) {
-        uint32_t u = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
-        out |= e2m1_sr(v[j], u) << (4 * j);
+        const uint32_t rp = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
+        g[j] = sr_grid_value(v[j], rp);
     }
-    return out;
+    return e2m1x8_rne(g);
 }
 
 // -------------------------------------------------------------- RHT-16 ----

@@ -256,7 +256,7 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, uint64_t i
 
 // Non-transposed view: thread item = (row, group of 4 blocks).
 template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads) k_quant1d_rows(QuantArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_rows(QuantArgs a) {
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
     const int64_t nkb = a.k >> 4;
@@ -312,7 +312,7 @@ __global__ void __launch_bounds__(kQuantThreads) k_quant1d_rows(QuantArgs a) {
 // Transposed view (stored [k x rows]): thread item = (pair of logical rows,
 // group of 4 blocks along the logical k = the stored rows).
 template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads) k_quant1d_cols(QuantArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(QuantArgs a) {
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
     const int64_t nkb = a.k >> 4;
