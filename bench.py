@@ -79,7 +79,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "200"],
+                 "--format=csv,noheader,nounits", "-lms", "100"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -301,7 +301,7 @@ def run_reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
@@ -423,11 +423,13 @@ def main():
         "gemm_tflops": gemm_tflops,
         "quantize_gbs": quant_gbs,
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
-                     "frac": gemm_tflops / fp4_peak, "traffic": traffic.get("gemm"),
+                     "frac": gemm_tflops / fp4_peak, "traffic": traffic.get("gemm_fwd"),
+                     "traffic_note": "forward-GEMM launch (8192x20480x5120); achieved is the mean of the 3 GEMMs",
                      "kernel": "k_gemm_nvfp4",
                      "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s x 6 (nominal dense FP4:BF16)"},
         "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm_peak, "unit": "GB/s",
-                              "frac": quant_gbs / hbm_peak, "traffic": traffic.get("quantize"),
+                              "frac": quant_gbs / hbm_peak, "traffic": traffic.get("quant_sr_dy"),
+                              "traffic_note": "1x16 SR quantise of dY (one launch)",
                               "peak_source": f"{peak_src} HBM copy"},
         "phase_ms": dict(zip(["amax_x", "q1d_x", "amax_w", "q2d_w", "gemm_fwd", "amax_dy", "q1d_dy_sr",
                               "gemm_dgrad", "amax_rht_dyt", "rhtq_dyt_sr", "amax_rht_xt", "rhtq_xt",
@@ -449,12 +451,17 @@ def main():
 
 
 def load_traffic():
-    """Per-launch DRAM bytes from the committed ncu summary, if present."""
-    p = os.path.join(ROOT, "profiles", "traffic.json")
+    """Per-launch DRAM bytes (read + write) from the committed ncu summaries
+    (profiles/dram_traffic.txt: `key bytes note...` lines), if present."""
+    p = os.path.join(ROOT, "profiles", "dram_traffic.txt")
+    out = {}
     if os.path.exists(p):
         with open(p) as f:
-            return json.load(f)
-    return {}
+            for line in f:
+                t = line.split()
+                if len(t) >= 2 and not line.startswith("#"):
+                    out[t[0]] = int(t[1])
+    return out
 
 
 if __name__ == "__main__":

@@ -231,13 +231,13 @@ class Quantized:
     """A quantised operand: codes [rows x k/2], plain scales [rows x k/16],
     swizzled scales, and the global encode scale S_enc."""
 
-    def __init__(self, codes, scales_plain, s_enc, rows, k):
+    def __init__(self, codes, scales_plain, s_enc, rows, k, swizzle=True):
         self.codes = codes
         self.scales_plain = scales_plain
         self.s_enc = s_enc
         self.rows = rows
         self.k = k
-        self.scales = swizzle_scales(scales_plain, rows, k)
+        self.scales = swizzle_scales(scales_plain, rows, k) if swizzle else None
 
 
 def _row_chunks(rows: int, threads: int, align: int):
@@ -248,12 +248,15 @@ def _row_chunks(rows: int, threads: int, align: int):
 
 def quantize(x: np.ndarray, *, transposed: bool = False, rht_mask: int = 0, block2d: bool = False,
              amax_v: float | None = None, sr: bool = False, seed: int = 0, stream_id: int = 0,
-             threads: int | None = None, rows_range=None) -> Quantized:
+             threads: int | None = None, rows_range=None, ranges=None,
+             swizzle: bool = True) -> Quantized:
     """Steps 1-6: quantise the logical operand of bf16 array x.
 
-    amax_v defaults to ``amax(x, transposed, rht_mask)``.  ``rows_range``
-    restricts the rows computed (the other rows of the outputs stay 0), which
-    the full-size parity tests use to check sampled rows only."""
+    amax_v defaults to ``amax(x, transposed, rht_mask)``.  ``rows_range`` (or
+    a list ``ranges`` of (lo, hi)) restricts the rows computed -- the other
+    rows of the outputs stay 0 -- which the full-size parity tests use to
+    check sampled rows only.  swizzle=False skips building the swizzled
+    scale buffer."""
     rows, k, ld = _view_dims(x, transposed)
     if amax_v is None:
         amax_v = amax(x, transposed, rht_mask)
@@ -262,9 +265,13 @@ def quantize(x: np.ndarray, *, transposed: bool = False, rht_mask: int = 0, bloc
         raise ValueError("non-finite amax")
     codes = np.zeros((rows, k // 2), dtype=np.uint8)
     scales = np.zeros((rows, k // 16), dtype=np.uint8)
-    r_lo, r_hi = rows_range if rows_range is not None else (0, rows)
+    if ranges is None:
+        ranges = [rows_range if rows_range is not None else (0, rows)]
     align = 16 if block2d else 1
-    chunks = [(r_lo + a, r_lo + b) for a, b in _row_chunks(r_hi - r_lo, threads or default_threads(), align)]
+    chunks = []
+    for r_lo, r_hi in ranges:
+        chunks += [(r_lo + a, r_lo + b)
+                   for a, b in _row_chunks(r_hi - r_lo, threads or default_threads(), align)]
 
     def run(ch):
         return lib().orc_quantize(_p(x, ctypes.c_uint16), rows, k, ld, int(transposed), rht_mask,
@@ -278,7 +285,7 @@ def quantize(x: np.ndarray, *, transposed: bool = False, rht_mask: int = 0, bloc
             rcs = list(ex.map(run, chunks))
     if any(rcs):
         raise ValueError("non-finite amax")
-    return Quantized(codes, scales, s_enc, rows, k)
+    return Quantized(codes, scales, s_enc, rows, k, swizzle=swizzle)
 
 
 def dequantize(q: Quantized, out_bf16: bool = False) -> np.ndarray:
