@@ -1,0 +1,359 @@
+// gemm2sm.cuh -- the block-scaled NVFP4 GEMM on CTA pairs (tcgen05
+// cta_group::2): one MMA instruction computes a 256 x 256 x 64 product on
+// the tensor cores of two SMs.
+//
+// Same product and numerics as gemm.cuh (NVIDIA blog "NVFP4 Trains with
+// Precision of 16-Bit and Speed and Efficiency of 4-Bit", Figure 1 and
+// recipe bullets 1-2): D = alpha * sum_k (qa sa)(qb sb), FP32 accumulation.
+//
+// Why pairs: a single-CTA 128 x 256 tile must stream A (128 rows) and all of
+// B (256 rows) through each SM's shared memory.  With a CTA pair each SM
+// holds its own 128 rows of A and only half of B (128 rows); the MMA reads
+// the peer's half across the pair.  Shared-memory fill per SM per k block
+// drops from 54 KB to 38 KB for the same FLOPs.
+//
+// Cluster of 2 CTAs (rank 0 = leader).  Per CTA:
+//  * warp 0   : TMA producer for its own A tile (rows of its m tile), its
+//               half of the B tile, its A scales and both halves of B's
+//               scales (each SM needs all of B's scales in its own TMEM).
+//  * warps 6-9: scale-factor warps: shared memory -> own TMEM slot
+//               (tcgen05.st), then arrive on the LEADER's scale barrier.
+//  * warp 1   : (leader only) issues tcgen05.mma.cta_group::2 M=256 N=256
+//               K=64, 4 per stage; tcgen05.commit multicasts the stage
+//               release to both CTAs' empty barriers and the tile's end to
+//               both CTAs' accumulator barriers.
+//  * warps 2-5: epilogue of the CTA's own 128 accumulator rows; they release
+//               the accumulator on the LEADER's barrier.
+// TMEM (each CTA, allocated collectively): [0, 256) accumulator, [256, 496)
+// scale slots of the 5-stage ring.  Every wait is bounded as in gemm.cuh.
+#pragma once
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include "gemm.cuh"
+#include "ptx.cuh"
+#include "status.cuh"
+
+namespace nvfp4 {
+namespace gemm2 {
+
+using gemm::Args;
+using gemm::BK;
+using gemm::BN;
+constexpr int HALF = 128;                               // rows of A and of B per CTA
+constexpr int A_BYTES = HALF * BK / 2;                  // 16 KB
+constexpr int B_BYTES = HALF * BK / 2;                  // 16 KB
+constexpr int SFA_BYTES = (BK / 64) * 512;              // 2 KB
+constexpr int SFB_BYTES = 2 * (BK / 64) * 512;          // 4 KB: both 128-row halves
+constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+constexpr int STAGES = 5;
+// epilogue staging: per epilogue warp two 32-row x 64-column BF16 blocks
+// (4 KB each, 128-byte swizzle), double-buffered against the TMA stores
+constexpr int EPI_BLOCK = 32 * 64 * 2;
+constexpr int EPI_WARP_BYTES = 2 * EPI_BLOCK;
+constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
+constexpr int THREADS = gemm::THREADS;
+constexpr int TMEM_COLS = gemm::TMEM_COLS;
+constexpr int TMEM_SF_BASE = gemm::TMEM_SF_BASE;
+constexpr int SF_COLS = gemm::SF_COLS_PER_STAGE;
+static_assert(STAGE_BYTES % 1024 == 0, "stage buffers must stay 1024-byte aligned");
+__host__ __device__ constexpr int smem_bytes_for(bool tma_epi) {
+    return STAGES * STAGE_BYTES + (tma_epi ? EPI_BYTES : 0) + gemm::BAR_BYTES + 1024;
+}
+static_assert(smem_bytes_for(true) <= gemm::SMEM_LIMIT, "shared memory budget");
+static_assert(TMEM_SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+
+// kind::mxf4nvf4 instruction descriptor for M = 256 (a CTA pair), N = 256.
+__host__ __device__ constexpr uint32_t make_idesc() {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+template <bool TMA_EPI>
+__global__ void __launch_bounds__(THREADS, 1)
+k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
+                 const __grid_constant__ CUtensorMap tma_d, const Args args) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                               ~uintptr_t(1023));
+    {
+        uint32_t dyn;
+        asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
+        const uint32_t pad = (uint32_t)(smem - smem_raw);
+        if (pad + (uint32_t)(smem_bytes_for(TMA_EPI) - 1024) > dyn) {
+            if (threadIdx.x == 0) record_device_error(NVFP4_DEV_TIMEOUT);
+            return;
+        }
+    }
+    uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
+    uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + (TMA_EPI ? EPI_BYTES : 0));
+    uint64_t* sf_bar = full_bar + STAGES;          // leader: scales of both CTAs in TMEM
+    uint64_t* empty_bar = sf_bar + STAGES;         // stage consumed by the pair MMA
+    uint64_t* acc_full = empty_bar + STAGES;
+    uint64_t* acc_empty = acc_full + 1;            // leader: both epilogues drained TMEM
+    uint64_t* drain_bar = acc_empty + 1;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain_bar + 1);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t leader = lane == 0 ? 1u : 0u;
+    const int rank = (int)(cluster_ctarank() & 1u);
+    const int m_units = args.m_tiles / 2;
+    const int num_units = m_units * args.n_tiles;
+    const int unit0 = (int)blockIdx.x / 2, unit_step = (int)gridDim.x / 2;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(&full_bar[s], 1);
+            mbar_init(&sf_bar[s], 8);              // 4 scale warps x 2 CTAs
+            mbar_init(&empty_bar[s], 1);
+        }
+        mbar_init(acc_full, 1);
+        mbar_init(acc_empty, 8);                   // 4 epilogue warps x 2 CTAs
+        mbar_init(drain_bar, 1);
+        *abort_flag = 0;
+        fence_barrier_init();
+        fence_proxy_async_smem();
+        tma_prefetch_desc(&tma_a);
+        tma_prefetch_desc(&tma_b);
+        if (TMA_EPI) tma_prefetch_desc(&tma_d);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_holder, TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                            // both CTAs' barriers exist
+    tc_fence_after();
+    const uint32_t tmem_base = *tmem_holder;
+    const uint32_t sf_bar_leader = mapa_shared(smem_addr(sf_bar), 0);
+    const uint32_t acc_empty_leader = mapa_shared(smem_addr(acc_empty), 0);
+
+    if (warp == 0) {
+        // ------------------------------------------------ TMA producer ----
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t fills[STAGES] = {};
+        bool ok = true;
+        for (int u = unit0; u < num_units && ok; u += unit_step) {
+            const int m_blk = (u % m_units) * 2 + rank, n_blk = u / m_units;
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                if (leader) {
+                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    uint8_t* sb = sa + A_BYTES;
+                    uint8_t* ssfa = sb + B_BYTES;
+                    uint8_t* ssfb = ssfa + SFA_BYTES;
+                    const int atoms = min(4, args.sf_col_tiles - kb * 4);
+                    const int b_tiles = min(2, args.b_row_tiles - n_blk * 2);
+                    const uint32_t bytes = A_BYTES + B_BYTES + atoms * 512 * (1 + b_tiles);
+                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                    tma_load_2d(sa, &tma_a, &full_bar[stage], kb * (BK / 2), m_blk * HALF);
+                    tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN + rank * HALF);
+                    bulk_load(ssfa, args.sfa + ((int64_t)m_blk * args.sf_col_tiles + kb * 4) * 512,
+                              atoms * 512, &full_bar[stage]);
+                    for (int j = 0; j < b_tiles; ++j)
+                        bulk_load(ssfb + j * (BK / 64) * 512,
+                                  args.sfb + ((int64_t)(n_blk * 2 + j) * args.sf_col_tiles + kb * 4) * 512,
+                                  atoms * 512, &full_bar[stage]);
+                }
+                __syncwarp();
+                fills[stage] += 1;
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+        if (!ok) {
+            for (int s = 0; s < STAGES; ++s)
+                if (fills[s]) mbar_wait_bounded(&full_bar[s], (fills[s] - 1) & 1u, nullptr);
+        } else {
+            // the pair MMA has finished reading every stage of this CTA
+            for (int s = 0; s < STAGES; ++s)
+                if (fills[s]) mbar_wait_bounded(&empty_bar[s], (fills[s] - 1) & 1u, abort_flag);
+        }
+    } else if (warp >= 6) {
+        // --------------------------------------------- scale-factor warps --
+        const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
+        int stage = 0;
+        uint32_t phase = 0;
+        bool ok = true;
+        for (int u = unit0; u < num_units && ok; u += unit_step) {
+            for (int kb = 0; kb < args.k_blocks; ++kb) {
+                if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                const uint32_t ssfa = smem_addr(smem + stage * STAGE_BYTES + A_BYTES + B_BYTES);
+                const uint32_t ssfb = ssfa + SFA_BYTES;
+                uint32_t r[48];
+#pragma unroll
+                for (int ks = 0; ks < 4; ++ks) {
+                    const uint4 a = lds128(ssfa + ks * 512 + lane * 16);
+                    r[ks * 4 + 0] = a.x; r[ks * 4 + 1] = a.y; r[ks * 4 + 2] = a.z; r[ks * 4 + 3] = a.w;
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const uint4 b = lds128(ssfb + h * 2048 + ks * 512 + lane * 16);
+                        const int c = 16 + ks * 8 + h * 4;
+                        r[c + 0] = b.x; r[c + 1] = b.y; r[c + 2] = b.z; r[c + 3] = b.w;
+                    }
+                }
+                const uint32_t t = tmem_base + lane_base + TMEM_SF_BASE + stage * SF_COLS;
+                tmem_st_32x32b_x16(t, r);
+                tmem_st_32x32b_x16(t + 16, r + 16);
+                tmem_st_32x32b_x16(t + 32, r + 32);
+                tmem_st_wait();
+                tc_fence_before();
+                __syncwarp();
+                if (leader) mbar_arrive_cluster(sf_bar_leader + stage * 8);
+                if (++stage == STAGES) {
+                    stage = 0;
+                    phase ^= 1u;
+                }
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------ MMA issuer (leader CTA) ----
+        if (rank == 0) {
+            constexpr uint32_t idesc = make_idesc();
+            int stage = 0;
+            uint32_t phase = 0;
+            bool ok = true;
+            bool issued = false;
+            int local = 0;
+            for (int u = unit0; u < num_units && ok; u += unit_step, ++local) {
+                if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                for (int kb = 0; kb < args.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(&sf_bar[stage], phase, abort_flag)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_addr(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    const uint32_t t_sf = tmem_base + TMEM_SF_BASE + stage * SF_COLS;
+                    const int nks = min(BK / 64, args.k_steps - kb * (BK / 64));
+#pragma unroll
+                    for (int ks = 0; ks < BK / 64; ++ks) {
+                        const uint64_t adesc = smem_desc(sa + ks * 32, 16, 1024, 2);
+                        const uint64_t bdesc = smem_desc(sb + ks * 32, 16, 1024, 2);
+                        tc_mma_nvf4_pair_if(leader & (ks < nks ? 1u : 0u), tmem_base, adesc, bdesc, idesc,
+                                            t_sf + ks * 4, t_sf + 16 + ks * 8, (kb | ks) != 0 ? 1u : 0u);
+                    }
+                    issued = true;
+                    tc_commit_pair_mc_if(leader, &empty_bar[stage], (uint16_t)0x3);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                tc_commit_pair_mc_if(leader, acc_full, (uint16_t)0x3);
+            }
+            if (!ok && issued) {
+                tc_commit_pair_mc_if(leader, drain_bar, (uint16_t)0x1);
+                mbar_wait_bounded(drain_bar, 0, nullptr);
+            }
+        }
+        __syncwarp();
+    } else {
+        // --------------------------------------------------- epilogue ----
+        // The CTA's 128 x 256 accumulator half is drained into registers as
+        // BF16 in two 128-column halves (64 packed words per thread) and is
+        // released after the second half's TMEM loads; the output streams out
+        // through two 4 KB staging blocks per warp.
+        const int quarter = warp & 3;
+        const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
+        const uint32_t stg = smem_addr(epi_stage) + (uint32_t)(warp - 2) * EPI_WARP_BYTES;
+        int local = 0;
+        for (int u = unit0; u < num_units; u += unit_step, ++local) {
+            if (!mbar_wait_bounded(acc_full, (uint32_t)local & 1u, abort_flag)) break;
+            tc_fence_after();
+            const int m_blk = (u % m_units) * 2 + rank, n_blk = u / m_units;
+            const int64_t row = (int64_t)m_blk * HALF + quarter * 32 + lane;
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16);
+            if (TMA_EPI) {
+                const int y = m_blk * HALF + quarter * 32;
+#pragma unroll
+                for (int h = 0; h < 2; ++h) {
+                    // 128 accumulator columns -> 64 packed BF16 pairs
+                    uint32_t packed[BN / 4];
+                    uint32_t acc[32];
+#pragma unroll
+                    for (int c = 0; c < BN / 64; ++c) {
+                        tmem_ld_32x32b_x32(t_row + (h * (BN / 64) + c) * 32, acc);
+                        tmem_ld_wait();
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            __nv_bfloat162 hv = __floats2bfloat162_rn(
+                                __fmul_rn(__uint_as_float(acc[2 * j]), alpha),
+                                __fmul_rn(__uint_as_float(acc[2 * j + 1]), alpha));
+                            packed[c * 16 + j] = *reinterpret_cast<uint32_t*>(&hv);
+                        }
+                    }
+                    if (h == 1) {                               // accumulator fully read
+                        tc_fence_before();
+                        __syncwarp();
+                        if (leader) mbar_arrive_cluster(acc_empty_leader);
+                    }
+#pragma unroll
+                    for (int bb = 0; bb < 2; ++bb) {
+                        const int b = h * 2 + bb;
+                        const uint32_t buf = stg + (uint32_t)(b & 1) * EPI_BLOCK;
+                        if (leader) bulk_wait_read_le1();      // the buffer's last store has read it
+                        __syncwarp();
+                        const uint32_t rowp = buf + (uint32_t)lane * 128;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q) {
+                            const uint32_t unit = (uint32_t)q ^ (uint32_t)(lane & 7);
+                            sts128(rowp + unit * 16, packed[bb * 32 + q * 4], packed[bb * 32 + q * 4 + 1],
+                                   packed[bb * 32 + q * 4 + 2], packed[bb * 32 + q * 4 + 3]);
+                        }
+                        fence_proxy_async_smem();
+                        __syncwarp();
+                        if (leader) {
+                            const int x = n_blk * BN + b * 64;
+                            if (x < args.N && y < args.M)
+                                tma_store_2d(&tma_d, epi_stage + (warp - 2) * EPI_WARP_BYTES + (b & 1) * EPI_BLOCK,
+                                             x, y);
+                            bulk_commit_group();
+                        }
+                    }
+                }
+            } else {
+                uint32_t acc[32];
+                for (int c = 0; c < BN / 32; ++c) {
+                    tmem_ld_32x32b_x32(t_row + c * 32, acc);
+                    tmem_ld_wait();
+                    if (c == BN / 32 - 1) {
+                        tc_fence_before();
+                        __syncwarp();
+                        if (leader) mbar_arrive_cluster(acc_empty_leader);
+                    }
+                    const int64_t col0 = (int64_t)n_blk * BN + c * 32;
+                    if (col0 < args.N) gemm::store_chunk(args, row, col0, acc, alpha);
+                }
+            }
+        }
+        if (TMA_EPI && leader) bulk_wait_all();
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();                            // the pair finishes together
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+}  // namespace gemm2
+}  // namespace nvfp4

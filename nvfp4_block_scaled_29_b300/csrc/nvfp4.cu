@@ -14,6 +14,7 @@
 #include "../../include/nvfp4.h"
 #include "codec.cuh"
 #include "gemm.cuh"
+#include "gemm2sm.cuh"
 #include "quantize.cuh"
 #include "status.cuh"
 
@@ -272,18 +273,97 @@ int gemm_smem_request(bool tma_epi) {
     return tma_epi ? gemm::SMEM_LIMIT : gemm::smem_bytes_for(false);
 }
 
+template <bool TMA, int CM>
+bool set_gemm_attrs() {
+    return cudaFuncSetAttribute(gemm::k_gemm_nvfp4<TMA, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                gemm_smem_request(TMA)) == cudaSuccess;
+}
+
 bool gemm_smem_ready() {
     static std::atomic<int> done[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load()) return true;
-    if (cudaFuncSetAttribute(gemm::k_gemm_nvfp4<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gemm_smem_request(true)) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm::k_gemm_nvfp4<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gemm_smem_request(false)) != cudaSuccess)
+    if (!set_gemm_attrs<true, 1>() || !set_gemm_attrs<false, 1>() ||
+        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm2::smem_bytes_for(true)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm2::smem_bytes_for(false)) != cudaSuccess)
         return false;
     done[dev].store(1);
     return true;
+}
+
+// Launch one GEMM instantiation; CM = 2 uses clusters of two CTAs along M.
+template <bool TMA, int CM>
+nvfp4_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                         const gemm::Args& g, cudaStream_t stream) {
+    const int64_t units = (int64_t)(g.m_tiles / CM) * g.n_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(gemm::THREADS);
+    cfg.dynamicSmemBytes = (size_t)gemm_smem_request(TMA);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    int grid_units = device_sm_count() / CM;
+    if (CM > 1) {
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = CM;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        // clusters that fit at once (one CTA per SM; SMs pair within a GPC)
+        static std::atomic<int> cache[kMaxDevices];
+        int dev = 0;
+        cudaGetDevice(&dev);
+        int n = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
+        if (n <= 0) {
+            cfg.gridDim = dim3((unsigned)(grid_units * CM));
+            if (cudaOccupancyMaxActiveClusters(&n, gemm::k_gemm_nvfp4<TMA, CM>, &cfg) != cudaSuccess ||
+                n <= 0)
+                return NVFP4_ERR_CUDA;
+            if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n);
+        }
+        grid_units = n;
+    }
+    grid_units = (int)std::min<int64_t>(grid_units, units);
+    cfg.gridDim = dim3((unsigned)(grid_units * CM));
+    if (cudaLaunchKernelEx(&cfg, gemm::k_gemm_nvfp4<TMA, CM>, ta, tb, td, g) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
+}
+
+// Launch the CTA-pair GEMM (clusters of 2 along M).
+template <bool TMA>
+nvfp4_status launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
+                              const gemm::Args& g, cudaStream_t stream) {
+    const int64_t units = (int64_t)(g.m_tiles / 2) * g.n_tiles;
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(gemm2::THREADS);
+    cfg.dynamicSmemBytes = (size_t)gemm2::smem_bytes_for(TMA);
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static std::atomic<int> cache[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    int n = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
+    if (n <= 0) {
+        cfg.gridDim = dim3((unsigned)(device_sm_count() / 2 * 2));
+        if (cudaOccupancyMaxActiveClusters(&n, gemm2::k_gemm_nvfp4_2sm<TMA>, &cfg) != cudaSuccess || n <= 0)
+            return NVFP4_ERR_CUDA;
+        if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n);
+    }
+    const int clusters = (int)std::min<int64_t>(n, units);
+    cfg.gridDim = dim3((unsigned)(clusters * 2));
+    if (cudaLaunchKernelEx(&cfg, gemm2::k_gemm_nvfp4_2sm<TMA>, ta, tb, td, g) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
 }
 
 // Host Philox4x32-10 (Salmon et al., SC'11), for the RHT sign mask.
@@ -378,8 +458,13 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
         return cudaMemset2DAsync(d, ldd * esz, 0, N * esz, M, stream) == cudaSuccess ? NVFP4_OK
                                                                                       : NVFP4_ERR_CUDA;
     }
+    // when the M tiles pair up, CTA pairs run 256-row MMAs (each CTA holds
+    // half of every B tile); otherwise one CTA per 128 x 256 tile
+    const int64_t m_tiles = cdiv(M, gemm::BM);
+    const int cm = (m_tiles % 2 == 0) ? 2 : 1;
     CUtensorMap ta, tb, td;
-    if (!make_code_map(&ta, a->codes, M, K, gemm::BM) || !make_code_map(&tb, b->codes, N, K, gemm::BN))
+    if (!make_code_map(&ta, a->codes, M, K, gemm::BM) ||
+        !make_code_map(&tb, b->codes, N, K, cm == 2 ? gemm::BN / 2 : gemm::BN))
         return NVFP4_ERR_CUDA;
     std::memset(&td, 0, sizeof(td));
     if (d_is_bf16 && !make_out_map(&td, d, M, N, ldd)) return NVFP4_ERR_CUDA;
@@ -401,12 +486,13 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
     g.k_steps = (int)cdiv(K, 64);
     g.sf_col_tiles = (int)cdiv(K, 64);
     g.b_row_tiles = (int)cdiv(N, 128);
-    const int64_t tiles = (int64_t)g.m_tiles * g.n_tiles;
-    const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
-    if (d_is_bf16)
-        gemm::k_gemm_nvfp4<true><<<grid, gemm::THREADS, gemm_smem_request(true), stream>>>(ta, tb, td, g);
+    nvfp4_status st;
+    if (cm == 2)
+        st = d_is_bf16 ? launch_gemm_pair<true>(ta, tb, td, g, stream)
+                       : launch_gemm_pair<false>(ta, tb, td, g, stream);
     else
-        gemm::k_gemm_nvfp4<false><<<grid, gemm::THREADS, gemm_smem_request(false), stream>>>(ta, tb, td, g);
+        st = d_is_bf16 ? launch_gemm<true, 1>(ta, tb, td, g, stream) : launch_gemm<false, 1>(ta, tb, td, g, stream);
+    if (st != NVFP4_OK) return st;
     return launch_status();
 }
 

@@ -109,6 +109,11 @@ __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
 }
 
+// Wait until at most one committed bulk-store group is still reading shared memory.
+__device__ __forceinline__ void bulk_wait_read_le1() {
+    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
+}
+
 // Wait until all committed bulk stores have completed.
 __device__ __forceinline__ void bulk_wait_all() {
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
@@ -118,6 +123,58 @@ __device__ __forceinline__ void sts128(uint32_t saddr, uint32_t a, uint32_t b, u
     asm volatile("st.shared.v4.u32 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
+}
+
+// ------------------------------------------------------------- clusters ----
+__device__ __forceinline__ uint32_t cluster_ctarank() {
+    uint32_t r;
+    asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+    return r;
+}
+
+// All threads of every CTA of the cluster: release our writes, acquire theirs.
+__device__ __forceinline__ void cluster_sync_all() {
+    asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" :::
+                     "memory");
+}
+
+// Address of the same shared-memory object in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t mapa_shared(uint32_t saddr, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+    return r;
+}
+
+// Arrive (relaxed, cluster scope) on an mbarrier given by its shared::cluster
+// address (possibly in another CTA of the cluster).  Used only to signal that
+// this thread's tcgen05 TMEM accesses are done: they were completed by
+// tcgen05.wait::st / wait::ld and ordered by tcgen05.fence::before_thread_sync
+// before the arrive, so no memory release is needed -- and a release at
+// cluster scope costs about a microsecond per arrive on this GPU.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
+    asm volatile("mbarrier.arrive.relaxed.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_addr)
+                 : "memory");
+}
+
+// 2D tensor load multicast to the CTAs of `mask`: the same shared-memory
+// offset and the mbarrier at the same offset in each destination CTA.
+__device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* desc, uint64_t* bar,
+                                               int32_t x, int32_t y, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
+        : "memory");
+}
+
+// 1D bulk copy global -> shared multicast to the CTAs of `mask`.
+__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes,
+                                             uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "h"(mask)
+        : "memory");
 }
 
 // 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
@@ -191,6 +248,60 @@ __device__ __forceinline__ void tc_mma_nvf4_if(uint32_t pred, uint32_t d_tmem, u
         "setp.ne.b32 p, %6, 0;\n\t"
         "setp.ne.b32 q, %7, 0;\n\t"
         "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate),
+        "r"(pred)
+        : "memory");
+}
+
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
+// tcgen05 operations issued so far by this thread have completed.
+__device__ __forceinline__ void tc_commit_mc_if(uint32_t pred, uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
+        "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %2;\n\t}" ::"r"(smem_addr(bar)),
+        "r"(pred), "h"(mask)
+        : "memory");
+}
+
+// ---- CTA-pair (cta_group::2) forms: the MMA runs on the tensor cores of
+// both CTAs of a cluster pair; TMEM is allocated collectively by one warp of
+// each CTA.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     smem_addr(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tc_commit_pair_mc_if(uint32_t pred, uint64_t* bar, uint16_t mask) {
+    asm volatile(
+        "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
+        "@P tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
+        " [%0], %2;\n\t}" ::"r"(smem_addr(bar)),
+        "r"(pred), "h"(mask)
+        : "memory");
+}
+
+__device__ __forceinline__ void tc_mma_nvf4_pair_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                    uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 q, %7, 0;\n\t"
+        "@q tcgen05.mma.cta_group::2.kind::mxf4nvf4.block_scale.scale_vec::4X"
         " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
         "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate),
         "r"(pred)
