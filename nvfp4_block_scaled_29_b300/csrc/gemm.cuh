@@ -14,8 +14,8 @@
 // tcgen05 / TMA operations are predicated on one lane):
 //  * warp 0   : TMA producer.  Per 256-wide k block it loads the A tile
 //               (128 rows x 128 B, 128-byte swizzle), the B tile (256 rows x
-//               128 B) and the matching 512-byte scale tiles (1D bulk copies)
-//               into a 4-stage shared-memory ring.
+//               128 B) and the matching 512-byte scale tiles (3D tensor loads
+//               over the scale buffer) into a 3- or 4-stage ring.
 //  * warps 6-9: scale-factor warps, one per TMEM lane quarter.  They copy a
 //               stage's E4M3 scales from shared memory to its TMEM slot with
 //               tcgen05.st, replicating each 32-row scale tile into all four
@@ -152,17 +152,12 @@ __device__ __forceinline__ void stage_bf16_chunk(uint32_t stg, int c, int lane, 
     }
 }
 
-// CM = CTAs per cluster along M (1 or 2).  With CM = 2 the two CTAs of a
-// cluster compute vertically adjacent tiles that share one B tile: each CTA
-// loads half of B (128 rows) and half of B's scale tiles and multicasts them
-// to both, halving B's L2 traffic.  A stage is refilled only after both
-// CTAs' MMAs released it (commits multicast to both empty barriers).
-template <bool TMA_EPI, int CM>
+template <bool TMA_EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-             const __grid_constant__ CUtensorMap tma_d, const Args args) {
+             const __grid_constant__ CUtensorMap tma_d, const __grid_constant__ CUtensorMap tma_sfa,
+             const __grid_constant__ CUtensorMap tma_sfb, const Args args) {
     constexpr int STAGES = stages_for(TMA_EPI);
-    static_assert(CM == 1 || CM == 2, "cluster size along M");
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -188,17 +183,13 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t leader = lane == 0 ? 1u : 0u;
-    const int rank = CM == 2 ? (int)(cluster_ctarank() & 1u) : 0;
-    // work units: one tile (CM = 1) or a vertical pair of tiles (CM = 2)
-    const int m_units = args.m_tiles / CM;
-    const int num_tiles = m_units * args.n_tiles;
-    const int unit0 = (int)blockIdx.x / CM, unit_step = (int)gridDim.x / CM;
+    const int num_tiles = args.m_tiles * args.n_tiles;
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
             mbar_init(&sf_bar[s], 4);
-            mbar_init(&empty_bar[s], CM);
+            mbar_init(&empty_bar[s], 1);
         }
         mbar_init(acc_full, 1);
         mbar_init(acc_empty, 4 * 32);
@@ -208,6 +199,8 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         fence_proxy_async_smem();
         tma_prefetch_desc(&tma_a);
         tma_prefetch_desc(&tma_b);
+        tma_prefetch_desc(&tma_sfa);
+        tma_prefetch_desc(&tma_sfb);
         if (TMA_EPI) tma_prefetch_desc(&tma_d);
     }
     if (warp == 1) {
@@ -216,7 +209,6 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
     }
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync_all();      // peers' barriers exist before any multicast
     tc_fence_after();
     const uint32_t tmem_base = *tmem_holder;
 
@@ -226,8 +218,8 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         uint32_t phase = 0;
         uint32_t fills[STAGES] = {};
         bool ok = true;
-        for (int tile = unit0; tile < num_tiles && ok; tile += unit_step) {
-            const int m_blk = (tile % m_units) * CM + rank, n_blk = tile / m_units;
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
+            const int m_blk = tile % args.m_tiles, n_blk = tile / args.m_tiles;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag)) {
                     ok = false;
@@ -238,28 +230,12 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
                     uint8_t* sb = sa + A_BYTES;
                     uint8_t* ssfa = sb + B_BYTES;
                     uint8_t* ssfb = ssfa + SFA_BYTES;
-                    const int atoms = min(4, args.sf_col_tiles - kb * 4);
-                    const int b_tiles = min(2, args.b_row_tiles - n_blk * 2);
-                    const uint32_t bytes = A_BYTES + B_BYTES + atoms * 512 * (1 + b_tiles);
-                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                    // scale tiles: 3D tensor loads (zero-filled beyond the buffer)
+                    mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
                     tma_load_2d(sa, &tma_a, &full_bar[stage], kb * (BK / 2), m_blk * BM);
-                    bulk_load(ssfa, args.sfa + ((int64_t)m_blk * args.sf_col_tiles + kb * 4) * 512,
-                              atoms * 512, &full_bar[stage]);
-                    if (CM == 1) {
-                        tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN);
-                        for (int j = 0; j < b_tiles; ++j)
-                            bulk_load(ssfb + j * (BK / 64) * 512,
-                                      args.sfb + ((int64_t)(n_blk * 2 + j) * args.sf_col_tiles + kb * 4) * 512,
-                                      atoms * 512, &full_bar[stage]);
-                    } else {
-                        // this CTA's half of B and of B's scales, to both CTAs
-                        tma_load_2d_mc(sb + rank * (B_BYTES / 2), &tma_b, &full_bar[stage], kb * (BK / 2),
-                                       n_blk * BN + rank * 128, (uint16_t)0x3);
-                        if (rank < b_tiles)
-                            bulk_load_mc(ssfb + rank * (BK / 64) * 512,
-                                         args.sfb + ((int64_t)(n_blk * 2 + rank) * args.sf_col_tiles + kb * 4) * 512,
-                                         atoms * 512, &full_bar[stage], (uint16_t)0x3);
-                    }
+                    tma_load_3d(ssfa, &tma_sfa, &full_bar[stage], 0, kb * 4, m_blk);
+                    tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN);
+                    tma_load_3d(ssfb, &tma_sfb, &full_bar[stage], 0, kb * 4, n_blk * 2);
                 }
                 __syncwarp();
                 fills[stage] += 1;
@@ -273,11 +249,6 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
             // let every copy this warp issued land before the CTA exits
             for (int s = 0; s < STAGES; ++s)
                 if (fills[s]) mbar_wait_bounded(&full_bar[s], (fills[s] - 1) & 1u, nullptr);
-        } else if (CM > 1) {
-            // the peer's last commits arrive on our empty barriers: wait for
-            // them so no remote arrival can target this CTA after it exits
-            for (int s = 0; s < STAGES; ++s)
-                if (fills[s]) mbar_wait_bounded(&empty_bar[s], (fills[s] - 1) & 1u, abort_flag);
         }
     } else if (warp >= 6) {
         // --------------------------------------------- scale-factor warps --
@@ -285,7 +256,7 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         int stage = 0;
         uint32_t phase = 0;
         bool ok = true;
-        for (int tile = unit0; tile < num_tiles && ok; tile += unit_step) {
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag)) {
                     ok = false;
@@ -327,7 +298,7 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         bool ok = true;
         bool issued = false;
         int local = 0;
-        for (int tile = unit0; tile < num_tiles && ok; tile += unit_step, ++local) {
+        for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x, ++local) {
             if (!mbar_wait_bounded(acc_empty, ((uint32_t)local & 1u) ^ 1u, abort_flag)) {
                 ok = false;
                 break;
@@ -351,8 +322,7 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
                                    t_sf + ks * 4, t_sf + 16 + ks * 8, (kb | ks) != 0 ? 1u : 0u);
                 }
                 issued = true;
-                if (CM == 1) tc_commit_if(leader, &empty_bar[stage]);
-                else tc_commit_mc_if(leader, &empty_bar[stage], (uint16_t)0x3);
+                tc_commit_if(leader, &empty_bar[stage]);
                 if (++stage == STAGES) {
                     stage = 0;
                     phase ^= 1u;
@@ -371,10 +341,10 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
         const uint32_t stg = smem_addr(epi_stage) + (uint32_t)(warp - 2) * EPI_WARP_BYTES;
         int local = 0;
-        for (int tile = unit0; tile < num_tiles; tile += unit_step, ++local) {
+        for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             if (!mbar_wait_bounded(acc_full, (uint32_t)local & 1u, abort_flag)) break;
             tc_fence_after();
-            const int m_blk = (tile % m_units) * CM + rank, n_blk = tile / m_units;
+            const int m_blk = tile % args.m_tiles, n_blk = tile / args.m_tiles;
             const int64_t row = (int64_t)m_blk * BM + quarter * 32 + lane;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16);
             if (TMA_EPI && local > 0) {
@@ -414,7 +384,6 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
 
     tc_fence_before();
     __syncthreads();
-    if (CM > 1) cluster_sync_all();      // no CTA leaves while its peer may still signal it
     if (warp == 1) {
         tc_fence_after();
         tmem_dealloc(tmem_base, TMEM_COLS);

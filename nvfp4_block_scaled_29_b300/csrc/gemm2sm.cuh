@@ -71,7 +71,8 @@ __host__ __device__ constexpr uint32_t make_idesc() {
 template <bool TMA_EPI>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
-                 const __grid_constant__ CUtensorMap tma_d, const Args args) {
+                 const __grid_constant__ CUtensorMap tma_d, const __grid_constant__ CUtensorMap tma_sfa,
+                 const __grid_constant__ CUtensorMap tma_sfb, const Args args) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                                ~uintptr_t(1023));
@@ -115,6 +116,8 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         fence_proxy_async_smem();
         tma_prefetch_desc(&tma_a);
         tma_prefetch_desc(&tma_b);
+        tma_prefetch_desc(&tma_sfa);
+        tma_prefetch_desc(&tma_sfb);
         if (TMA_EPI) tma_prefetch_desc(&tma_d);
     }
     if (warp == 1) {
@@ -147,18 +150,13 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                     uint8_t* sb = sa + A_BYTES;
                     uint8_t* ssfa = sb + B_BYTES;
                     uint8_t* ssfb = ssfa + SFA_BYTES;
-                    const int atoms = min(4, args.sf_col_tiles - kb * 4);
-                    const int b_tiles = min(2, args.b_row_tiles - n_blk * 2);
-                    const uint32_t bytes = A_BYTES + B_BYTES + atoms * 512 * (1 + b_tiles);
-                    mbar_arrive_expect_tx(&full_bar[stage], bytes);
+                    // scale tiles: 3D tensor loads of A's 4 tiles and both of B's
+                    // 128-row halves (zero-filled beyond the buffer)
+                    mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
                     tma_load_2d(sa, &tma_a, &full_bar[stage], kb * (BK / 2), m_blk * HALF);
                     tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN + rank * HALF);
-                    bulk_load(ssfa, args.sfa + ((int64_t)m_blk * args.sf_col_tiles + kb * 4) * 512,
-                              atoms * 512, &full_bar[stage]);
-                    for (int j = 0; j < b_tiles; ++j)
-                        bulk_load(ssfb + j * (BK / 64) * 512,
-                                  args.sfb + ((int64_t)(n_blk * 2 + j) * args.sf_col_tiles + kb * 4) * 512,
-                                  atoms * 512, &full_bar[stage]);
+                    tma_load_3d(ssfa, &tma_sfa, &full_bar[stage], 0, kb * 4, m_blk);
+                    tma_load_3d(ssfb, &tma_sfb, &full_bar[stage], 0, kb * 4, n_blk * 2);
                 }
                 __syncwarp();
                 fills[stage] += 1;

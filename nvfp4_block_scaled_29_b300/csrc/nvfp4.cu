@@ -269,13 +269,29 @@ bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t l
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// The swizzled scale buffer of a [rows x k] operand as a 3D tensor of u32:
+// [row tiles][512-byte tiles along k][128 words]; box = 4 k tiles (one
+// 256-wide k block) x `box_row_tiles` row tiles.  Out-of-range boxes read 0.
+bool make_scale_map(CUtensorMap* m, const uint8_t* scales, int64_t rows, int64_t k, int box_row_tiles) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const int64_t row_tiles = cdiv(rows, 128), col_tiles = cdiv(k / 16, 4);
+    const cuuint64_t dims[3] = {128u, (cuuint64_t)col_tiles, (cuuint64_t)row_tiles};
+    const cuuint64_t strides[2] = {512u, (cuuint64_t)(col_tiles * 512)};
+    const cuuint32_t box[3] = {128u, 4u, (cuuint32_t)box_row_tiles};
+    const cuuint32_t estr[3] = {1u, 1u, 1u};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(scales), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int gemm_smem_request(bool tma_epi) {
     return tma_epi ? gemm::SMEM_LIMIT : gemm::smem_bytes_for(false);
 }
 
-template <bool TMA, int CM>
+template <bool TMA>
 bool set_gemm_attrs() {
-    return cudaFuncSetAttribute(gemm::k_gemm_nvfp4<TMA, CM>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    return cudaFuncSetAttribute(gemm::k_gemm_nvfp4<TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                 gemm_smem_request(TMA)) == cudaSuccess;
 }
 
@@ -284,7 +300,7 @@ bool gemm_smem_ready() {
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load()) return true;
-    if (!set_gemm_attrs<true, 1>() || !set_gemm_attrs<false, 1>() ||
+    if (!set_gemm_attrs<true>() || !set_gemm_attrs<false>() ||
         cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gemm2::smem_bytes_for(true)) != cudaSuccess ||
         cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -294,49 +310,23 @@ bool gemm_smem_ready() {
     return true;
 }
 
-// Launch one GEMM instantiation; CM = 2 uses clusters of two CTAs along M.
-template <bool TMA, int CM>
-nvfp4_status launch_gemm(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
-                         const gemm::Args& g, cudaStream_t stream) {
-    const int64_t units = (int64_t)(g.m_tiles / CM) * g.n_tiles;
-    cudaLaunchConfig_t cfg = {};
-    cfg.blockDim = dim3(gemm::THREADS);
-    cfg.dynamicSmemBytes = (size_t)gemm_smem_request(TMA);
-    cfg.stream = stream;
-    cudaLaunchAttribute attr[1];
-    int grid_units = device_sm_count() / CM;
-    if (CM > 1) {
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = CM;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        // clusters that fit at once (one CTA per SM; SMs pair within a GPC)
-        static std::atomic<int> cache[kMaxDevices];
-        int dev = 0;
-        cudaGetDevice(&dev);
-        int n = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
-        if (n <= 0) {
-            cfg.gridDim = dim3((unsigned)(grid_units * CM));
-            if (cudaOccupancyMaxActiveClusters(&n, gemm::k_gemm_nvfp4<TMA, CM>, &cfg) != cudaSuccess ||
-                n <= 0)
-                return NVFP4_ERR_CUDA;
-            if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n);
-        }
-        grid_units = n;
-    }
-    grid_units = (int)std::min<int64_t>(grid_units, units);
-    cfg.gridDim = dim3((unsigned)(grid_units * CM));
-    if (cudaLaunchKernelEx(&cfg, gemm::k_gemm_nvfp4<TMA, CM>, ta, tb, td, g) != cudaSuccess)
-        return NVFP4_ERR_CUDA;
+struct GemmMaps {
+    CUtensorMap a, b, d, sfa, sfb;
+};
+
+// Launch the single-CTA GEMM: persistent, one CTA per SM.
+template <bool TMA>
+nvfp4_status launch_gemm(const GemmMaps& mp, const gemm::Args& g, cudaStream_t stream) {
+    const int64_t tiles = (int64_t)g.m_tiles * g.n_tiles;
+    const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
+    gemm::k_gemm_nvfp4<TMA><<<grid, gemm::THREADS, gemm_smem_request(TMA), stream>>>(mp.a, mp.b, mp.d,
+                                                                                   mp.sfa, mp.sfb, g);
     return NVFP4_OK;
 }
 
 // Launch the CTA-pair GEMM (clusters of 2 along M).
 template <bool TMA>
-nvfp4_status launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, const CUtensorMap& td,
-                              const gemm::Args& g, cudaStream_t stream) {
+nvfp4_status launch_gemm_pair(const GemmMaps& mp, const gemm::Args& g, cudaStream_t stream) {
     const int64_t units = (int64_t)(g.m_tiles / 2) * g.n_tiles;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(gemm2::THREADS);
@@ -361,7 +351,8 @@ nvfp4_status launch_gemm_pair(const CUtensorMap& ta, const CUtensorMap& tb, cons
     }
     const int clusters = (int)std::min<int64_t>(n, units);
     cfg.gridDim = dim3((unsigned)(clusters * 2));
-    if (cudaLaunchKernelEx(&cfg, gemm2::k_gemm_nvfp4_2sm<TMA>, ta, tb, td, g) != cudaSuccess)
+    if (cudaLaunchKernelEx(&cfg, gemm2::k_gemm_nvfp4_2sm<TMA>, mp.a, mp.b, mp.d, mp.sfa, mp.sfb, g) !=
+        cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
 }
@@ -462,12 +453,13 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
     // half of every B tile); otherwise one CTA per 128 x 256 tile
     const int64_t m_tiles = cdiv(M, gemm::BM);
     const int cm = (m_tiles % 2 == 0) ? 2 : 1;
-    CUtensorMap ta, tb, td;
-    if (!make_code_map(&ta, a->codes, M, K, gemm::BM) ||
-        !make_code_map(&tb, b->codes, N, K, cm == 2 ? gemm::BN / 2 : gemm::BN))
+    GemmMaps mp;
+    std::memset(&mp, 0, sizeof(mp));
+    if (!make_code_map(&mp.a, a->codes, M, K, gemm::BM) ||
+        !make_code_map(&mp.b, b->codes, N, K, cm == 2 ? gemm::BN / 2 : gemm::BN) ||
+        !make_scale_map(&mp.sfa, a->scales, M, K, 1) || !make_scale_map(&mp.sfb, b->scales, N, K, 2))
         return NVFP4_ERR_CUDA;
-    std::memset(&td, 0, sizeof(td));
-    if (d_is_bf16 && !make_out_map(&td, d, M, N, ldd)) return NVFP4_ERR_CUDA;
+    if (d_is_bf16 && !make_out_map(&mp.d, d, M, N, ldd)) return NVFP4_ERR_CUDA;
     if (!gemm_smem_ready()) return NVFP4_ERR_CUDA;
     gemm::Args g{};
     g.sfa = a->scales;
@@ -488,10 +480,9 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
     g.b_row_tiles = (int)cdiv(N, 128);
     nvfp4_status st;
     if (cm == 2)
-        st = d_is_bf16 ? launch_gemm_pair<true>(ta, tb, td, g, stream)
-                       : launch_gemm_pair<false>(ta, tb, td, g, stream);
+        st = d_is_bf16 ? launch_gemm_pair<true>(mp, g, stream) : launch_gemm_pair<false>(mp, g, stream);
     else
-        st = d_is_bf16 ? launch_gemm<true, 1>(ta, tb, td, g, stream) : launch_gemm<false, 1>(ta, tb, td, g, stream);
+        st = d_is_bf16 ? launch_gemm<true>(mp, g, stream) : launch_gemm<false>(mp, g, stream);
     if (st != NVFP4_OK) return st;
     return launch_status();
 }

@@ -91,6 +91,14 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_
         : "memory");
 }
 
+// Prefetch a 2D tensor tile into L2 (no shared-memory destination).
+__device__ __forceinline__ void tma_prefetch_2d(const void* desc, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
+                     reinterpret_cast<uint64_t>(desc)),
+                 "r"(x), "r"(y)
+                 : "memory");
+}
+
 // 2D tiled tensor store from shared memory (bulk-group completion).
 __device__ __forceinline__ void tma_store_2d(const void* desc, const void* src, int32_t x, int32_t y) {
     asm volatile(
@@ -174,6 +182,16 @@ __device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
         " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
         "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "h"(mask)
+        : "memory");
+}
+
+// 3D tiled tensor load into shared memory, completing on `bar`.
+__device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_t* bar, int32_t x, int32_t y,
+                                            int32_t z) {
+    asm volatile(
+        "cp.async.bulk.tensor.3d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(smem_addr(dst)),
+        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(z), "r"(smem_addr(bar))
         : "memory");
 }
 
