@@ -17,7 +17,9 @@
 //               half of the B tile, its A scales and both halves of B's
 //               scales (each SM needs all of B's scales in its own TMEM).
 //  * warps 6-9: scale-factor warps: shared memory -> own TMEM slot
-//               (tcgen05.st), then arrive on the LEADER's scale barrier.
+//               (tcgen05.st) as soon as the stage's scale tiles land, then,
+//               once the CTA's A/B tiles landed too, arrive on the LEADER's
+//               scale barrier.
 //  * warp 1   : (leader only) issues tcgen05.mma.cta_group::2 M=256 N=256
 //               K=64, 4 per stage; tcgen05.commit multicasts the stage
 //               release to both CTAs' empty barriers and the tile's end to
@@ -87,7 +89,8 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     }
     uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + (TMA_EPI ? EPI_BYTES : 0));
-    uint64_t* sf_bar = full_bar + STAGES;          // leader: scales of both CTAs in TMEM
+    uint64_t* sf_full = full_bar + STAGES;         // the stage's scale tiles landed
+    uint64_t* sf_bar = sf_full + STAGES;           // leader: scales of both CTAs in TMEM
     uint64_t* empty_bar = sf_bar + STAGES;         // stage consumed by the pair MMA
     uint64_t* acc_full = empty_bar + STAGES;
     uint64_t* acc_empty = acc_full + 1;            // leader: both epilogues drained TMEM
@@ -105,6 +108,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     if (threadIdx.x == 0) {
         for (int s = 0; s < STAGES; ++s) {
             mbar_init(&full_bar[s], 1);
+            mbar_init(&sf_full[s], 1);
             mbar_init(&sf_bar[s], 8);              // 4 scale warps x 2 CTAs
             mbar_init(&empty_bar[s], 1);
         }
@@ -150,13 +154,15 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                     uint8_t* sb = sa + A_BYTES;
                     uint8_t* ssfa = sb + B_BYTES;
                     uint8_t* ssfb = ssfa + SFA_BYTES;
-                    // scale tiles: 3D tensor loads of A's 4 tiles and both of B's
-                    // 128-row halves (zero-filled beyond the buffer)
-                    mbar_arrive_expect_tx(&full_bar[stage], STAGE_BYTES);
+                    // scale tiles first (3D tensor loads of A's 4 tiles and both of
+                    // B's 128-row halves, zero-filled beyond the buffer) on their
+                    // own barrier, so the scale warps overlap them with A and B
+                    mbar_arrive_expect_tx(&sf_full[stage], SFA_BYTES + SFB_BYTES);
+                    tma_load_3d(ssfa, &tma_sfa, &sf_full[stage], 0, kb * 4, m_blk);
+                    tma_load_3d(ssfb, &tma_sfb, &sf_full[stage], 0, kb * 4, n_blk * 2);
+                    mbar_arrive_expect_tx(&full_bar[stage], A_BYTES + B_BYTES);
                     tma_load_2d(sa, &tma_a, &full_bar[stage], kb * (BK / 2), m_blk * HALF);
                     tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN + rank * HALF);
-                    tma_load_3d(ssfa, &tma_sfa, &full_bar[stage], 0, kb * 4, m_blk);
-                    tma_load_3d(ssfb, &tma_sfb, &full_bar[stage], 0, kb * 4, n_blk * 2);
                 }
                 __syncwarp();
                 fills[stage] += 1;
@@ -168,7 +174,10 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         }
         if (!ok) {
             for (int s = 0; s < STAGES; ++s)
-                if (fills[s]) mbar_wait_bounded(&full_bar[s], (fills[s] - 1) & 1u, nullptr);
+                if (fills[s]) {
+                    mbar_wait_bounded(&sf_full[s], (fills[s] - 1) & 1u, nullptr);
+                    mbar_wait_bounded(&full_bar[s], (fills[s] - 1) & 1u, nullptr);
+                }
         } else {
             // the pair MMA has finished reading every stage of this CTA
             for (int s = 0; s < STAGES; ++s)
@@ -182,7 +191,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         bool ok = true;
         for (int u = unit0; u < num_units && ok; u += unit_step) {
             for (int kb = 0; kb < args.k_blocks; ++kb) {
-                if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag)) {
+                if (!mbar_wait_bounded(&sf_full[stage], phase, abort_flag)) {
                     ok = false;
                     break;
                 }
@@ -206,6 +215,12 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                 tmem_st_32x32b_x16(t + 32, r + 32);
                 tmem_st_wait();
                 tc_fence_before();
+                // this CTA's A and B tiles of the stage must be in place too:
+                // the leader's MMA reads both CTAs' shared memory
+                if (!mbar_wait_bounded(&full_bar[stage], phase, abort_flag)) {
+                    ok = false;
+                    break;
+                }
                 __syncwarp();
                 if (leader) mbar_arrive_cluster(sf_bar_leader + stage * 8);
                 if (++stage == STAGES) {
