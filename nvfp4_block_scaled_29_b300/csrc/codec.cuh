@@ -134,25 +134,25 @@ __device__ __forceinline__ uint4 sr_bits8(uint64_t g, uint64_t seed, uint64_t st
 }
 
 // Stochastic rounding realised as "add random bits below the kept precision,
-// then truncate": with rp = 65535 - u16 placed just below the kept bits of
-// |v| (the 16 bits that hold floor(frac * 2^16)), a carry reaches the kept
-// bits exactly when floor(frac * 2^16) > u16, i.e. the rule above.  The kept
-// precision is bit 22 for |v| >= 1 (spacing 2^(e-1)) and bit 23 for
-// 0.5 <= |v| < 1 (spacing 0.5); |v| < 0.5 (grid 0, 0.5) is first moved to
-// [0.5, 1) by a round-toward-zero add of 0.5, which keeps floor(frac * 2^16),
-// and moved back by an exact subtraction.  The result is the chosen grid
-// value (exact, sign kept), so RNE conversion returns its code unchanged;
-// |v| is clamped to 8 first (anything >= 6 saturates to 6).
+// then truncate".  On [1, 6) the E2M1 grid is 2^e x {1, 1.5}: the kept bits
+// are the exponent and mantissa bit 22, and the 16 bits below them hold
+// floor(frac * 2^16).  Adding rp = 65535 - u16 there carries into the kept
+// bits exactly when floor(frac * 2^16) > u16, i.e. the rule above.  Values
+// below 1 (grid 0, 0.5, 1: spacing 0.5) are first moved to [1, 2) by a
+// round-toward-zero add of 1.0 -- the truncation is below 2^-17, so
+// floor(frac * 2^16) is unchanged -- and moved back by an exact subtraction.
+// |v| is clamped to 8 first (anything >= 6 saturates to 6).  The result is
+// the chosen grid value (exact, sign kept), so RNE conversion returns its
+// code unchanged.
 __device__ __forceinline__ float sr_grid_value(float v, uint32_t rp) {
     const uint32_t bits = __float_as_uint(v);
-    const float a = fminf(__uint_as_float(bits & 0x7FFFFFFFu), 8.0f);
-    const uint32_t ab = __float_as_uint(a);
-    const bool ge1 = ab >= 0x3F800000u, ge05 = ab >= 0x3F000000u;
-    const float a2 = ge05 ? a : __fadd_rz(a, 0.5f);
-    const uint32_t sh = ge1 ? 6u : 7u;
-    const uint32_t keep = ge1 ? 0xFFC00000u : 0xFF800000u;
-    float q = __uint_as_float((__float_as_uint(a2) + (rp << sh)) & keep);
-    q = ge05 ? q : __fsub_rn(q, 0.5f);
+    const float a = fminf(fabsf(v), 8.0f);
+    const bool lt1 = a < 1.0f;
+    const float a2 = lt1 ? __fadd_rz(a, 1.0f) : a;
+    uint32_t qb;
+    asm("mad.lo.u32 %0, %1, 64, %2;" : "=r"(qb) : "r"(rp), "r"(__float_as_uint(a2)));
+    float q = __uint_as_float(qb & 0xFFC00000u);
+    q = __fsub_rn(q, lt1 ? 1.0f : 0.0f);
     return __uint_as_float(__float_as_uint(q) | (bits & 0x80000000u));
 }
 

@@ -236,13 +236,26 @@ struct QuantArgs {
     int write_primary;
 };
 
+// amax of 16 bf16 values held as 8 packed words: half-word SIMD max of the
+// magnitudes, returned as a float bit pattern.
+__device__ __forceinline__ uint32_t absmax_bits16_packed(uint4 a, uint4 b) {
+    constexpr uint32_t M = 0x7FFF7FFFu;
+    uint32_t m = __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M));
+    m = __vmaxu2(m, __vmaxu2(__vmaxu2(b.x & M, b.y & M), __vmaxu2(b.z & M, b.w & M)));
+    return max(m << 16, m & 0xFFFF0000u);
+}
+
+// Encode one 16-element block.  amax_bits: the block's max |value| as float
+// bits when already known (raw bf16 input), or ~0u to compute it here.
 template <bool RHT, bool SR>
 __device__ __forceinline__ void encode_block16(float* v, float s_enc, uint64_t idx0,
                                                const QuantArgs& a, uint32_t* sb_out,
-                                               uint32_t* code_lo, uint32_t* code_hi) {
+                                               uint32_t* code_lo, uint32_t* code_hi,
+                                               uint32_t amax_bits = ~0u) {
     if (RHT) rht16(v, a.rht_mask);
+    if (RHT || amax_bits == ~0u) amax_bits = absmax_bits16(v);
     float r_b;
-    *sb_out = block_scale(__uint_as_float(absmax_bits16(v)), s_enc, &r_b);
+    *sb_out = block_scale(__uint_as_float(amax_bits), s_enc, &r_b);
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], r_b);
     if (SR) {
@@ -292,7 +305,8 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_rows(QuantArgs a) 
                 unpack8(raw[2 * b + 1], v + 8);
                 uint32_t sb;
                 encode_block16<RHT, SR>(v, s_enc, (uint64_t)(r * a.k + g * 64 + b * 16), a, &sb,
-                                        &cw[2 * b], &cw[2 * b + 1]);
+                                        &cw[2 * b], &cw[2 * b + 1],
+                                        RHT ? ~0u : absmax_bits16_packed(raw[2 * b], raw[2 * b + 1]));
                 sw |= sb << (8 * b);
             }
         }
