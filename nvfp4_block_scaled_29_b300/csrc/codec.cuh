@@ -171,13 +171,20 @@ __device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 r) {
 
 // -------------------------------------------------------------- RHT-16 ----
 // y = H16 diag(s) x / 4 in place: sign flip, butterflies h = 1, 2, 4, 8,
-// exact scaling by 1/4.
+// exact scaling by 1/4.  The sign flip is folded into the first butterfly
+// stage as fused multiply-adds by +-1: fma(s_b, b, s_a * a) rounds
+// s_a a + s_b b once, exactly like the separate negate-then-add.
 __device__ __forceinline__ void rht16(float* v, uint32_t mask) {
 #pragma unroll
-    for (int j = 0; j < 16; ++j)
-        v[j] = __uint_as_float(__float_as_uint(v[j]) ^ (((mask >> j) & 1u) << 31));
+    for (int i = 0; i < 16; i += 2) {
+        const float sa = ((mask >> i) & 1u) ? -1.0f : 1.0f;
+        const float sb = ((mask >> (i + 1)) & 1u) ? -1.0f : 1.0f;
+        const float a = __fmul_rn(v[i], sa), b = v[i + 1];
+        v[i] = __fmaf_rn(sb, b, a);
+        v[i + 1] = __fmaf_rn(-sb, b, a);
+    }
 #pragma unroll
-    for (int h = 1; h < 16; h <<= 1) {
+    for (int h = 2; h < 16; h <<= 1) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & h) continue;

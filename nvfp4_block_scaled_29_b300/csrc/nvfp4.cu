@@ -92,7 +92,7 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
             p, x.rows, x.cols, x.ld, mask, out);
     } else {
-        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 8) * (x.cols / 16), kQuantThreads, 8), kQuantThreads,
+        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 4) * (x.cols / 16), kQuantThreads, 8), kQuantThreads,
                           0, st>>>(p, x.cols, x.rows, x.ld, mask, out);
     }
     return launch_status();

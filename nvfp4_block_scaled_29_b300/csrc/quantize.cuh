@@ -50,7 +50,19 @@ __device__ __forceinline__ void unpack8(uint4 w, float* v) {
     v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
 
+// max |v| over 16 finite values, as float bits (fmax of magnitudes; the
+// inputs of a quantiser are finite because a non-finite amax stops it).
 __device__ __forceinline__ uint32_t absmax_bits16(const float* v) {
+    float m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
+    return __float_as_uint(m);
+}
+
+// max |v| over 16 values as float bits, NaN-propagating (integer max of the
+// magnitude bit patterns): used by the amax kernels, whose inputs may hold
+// NaN or Inf.
+__device__ __forceinline__ uint32_t absmax_bits16_nan(const float* v) {
     uint32_t m = 0;
 #pragma unroll
     for (int j = 0; j < 16; ++j) m = max(m, __float_as_uint(v[j]) & 0x7FFFFFFFu);
@@ -160,48 +172,48 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
         unpack8(ldg_stream(src), v);
         unpack8(ldg_stream(src + 1), v + 8);
         rht16(v, mask);
-        m = max(m, absmax_bits16(v));
+        m = max(m, absmax_bits16_nan(v));
     }
     block_max_to_global(m, out);
 }
 
 // max |RHT16(x)| over 16-chunks down the stored columns (transposed view:
 // the logical k runs along the stored rows).  One thread: 16 stored rows x
-// 8 stored columns.
+// 4 stored columns (8-byte loads; a warp covers 256 contiguous bytes of a row).
 __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_cols(const uint16_t* __restrict__ p,
                                                                  int64_t srows, int64_t scols,
                                                                  int64_t ld, uint32_t mask,
                                                                  float* out) {
     uint32_t m = 0;
-    const int64_t ncb = (scols + 7) >> 3, nkb = srows >> 4;
+    const int64_t ncb = (scols + 3) >> 2, nkb = srows >> 4;
     const int64_t total = ncb * nkb;
     for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
          it += (int64_t)gridDim.x * blockDim.x) {
         const int64_t kb = it / ncb, cb = it - kb * ncb;
-        const int64_t c0 = cb * 8;
+        const int64_t c0 = cb * 4;
         const uint16_t* base = p + kb * 16 * ld + c0;
-        float v[8][16];
-        if (c0 + 8 <= scols) {
+        float v[4][16];
+        if (c0 + 4 <= scols) {
+            uint2 w[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) w[t] = *reinterpret_cast<const uint2*>(base + t * ld);
 #pragma unroll
             for (int t = 0; t < 16; ++t) {
-                const uint4 w = ldg_stream(base + t * ld);
-                float f[8];
-                unpack8(w, f);
-#pragma unroll
-                for (int c = 0; c < 8; ++c) v[c][t] = f[c];
+                v[0][t] = bf16_lo(w[t].x); v[1][t] = bf16_hi(w[t].x);
+                v[2][t] = bf16_lo(w[t].y); v[3][t] = bf16_hi(w[t].y);
             }
         } else {
 #pragma unroll
             for (int t = 0; t < 16; ++t)
 #pragma unroll
-                for (int c = 0; c < 8; ++c)
+                for (int c = 0; c < 4; ++c)
                     v[c][t] = (c0 + c < scols) ? __uint_as_float((uint32_t)base[t * ld + c] << 16)
                                                : 0.0f;
         }
 #pragma unroll
-        for (int c = 0; c < 8; ++c) {
+        for (int c = 0; c < 4; ++c) {
             rht16(v[c], mask);
-            m = max(m, absmax_bits16(v[c]));
+            m = max(m, absmax_bits16_nan(v[c]));
         }
     }
     block_max_to_global(m, out);
