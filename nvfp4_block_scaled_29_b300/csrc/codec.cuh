@@ -51,19 +51,31 @@ __device__ __forceinline__ float e4m3_value(uint32_t c) {
     return __uint_as_float(((e + 120u) << 23) | (m << 20));
 }
 
-// Block decode scale and encode factor from the block amax.
-__device__ __forceinline__ uint32_t block_scale(float amax_b, float s_enc, float* r_b) {
-    float t = __fdiv_rn(amax_b, 6.0f);
-    t = __fmul_rn(t, s_enc);
-    uint32_t sb = e4m3_rne_satfinite(t);
-    float sbv = e4m3_value(sb);
-    float r = 0.0f;
-    if (sbv != 0.0f) {
-        r = __fdiv_rn(s_enc, sbv);
-        if (r > FLT_MAX) r = FLT_MAX;
-    }
-    *r_b = r;
-    return sb;
+// fp32(x / 6) for finite x >= 0, correctly rounded.  Markstein's correction
+// (one residual r = x - 6 q, exact by FMA, then q + r * RN(1/6)) gives the
+// correctly rounded quotient whenever the quotient is not subnormal; an
+// exhaustive comparison over every non-negative finite float confirms it for
+// x >= 2^-122.  Smaller x take the IEEE division.
+__device__ __forceinline__ float div6_rn(float x) {
+    if (x < 0x1p-122f) return __fdiv_rn(x, 6.0f);
+    const float y = 0x1.555556p-3f;                 // RN(1/6)
+    const float q = __fmul_rn(x, y);
+    return __fmaf_rn(__fmaf_rn(-q, 6.0f, x), y, q);
+}
+
+// Block decode scale s_b (E4M3 code) from the block amax:
+// t = fp32(fp32(amax_b / 6) * S_enc), then E4M3 RNE with saturation.
+__device__ __forceinline__ uint32_t block_scale_code(float amax_b, float s_enc) {
+    return e4m3_rne_satfinite(__fmul_rn(div6_rn(amax_b), s_enc));
+}
+
+// Encode factor r_b = fp32(S_enc / s_b) for an E4M3 code (0 for s_b = 0,
+// FLT_MAX on overflow).
+__device__ __forceinline__ float encode_factor(float s_enc, uint32_t sb) {
+    const float sbv = e4m3_value(sb);
+    if (sbv == 0.0f) return 0.0f;
+    const float r = __fdiv_rn(s_enc, sbv);
+    return r > FLT_MAX ? FLT_MAX : r;
 }
 
 // ------------------------------------------------------------------ E2M1 --
@@ -82,90 +94,75 @@ __device__ __forceinline__ uint32_t e2m1x8_rne(const float* v) {
     return out;
 }
 
-// Stochastic E2M1 rounding of one value with 16 random bits.  With lo <= |v|
-// < hi the neighbouring grid values, the code moves up iff
-// u16 < F = floor(frac * 2^16), frac = (|v| - lo) / (hi - lo).  Branch-free
-// on the bit pattern of |v| (exponent e, 23-bit mantissa m):
-//   |v| >= 1   : lo = 2^e * (1 + m22/2), code_lo = 2 (e + 1) + m22, and frac
-//                is the 22 mantissa bits below m22, so F = bits 21..6;
-//   0.5..1     : lo = 0.5, code_lo = 1, frac = m / 2^23, so F = bits 22..7;
-//   |v| < 0.5  : lo = 0, code_lo = 0, frac = 2|v|, F = floor(|v| * 2^17)
-//                (an exact power-of-two scaling);
-//   |v| >= 6   : saturates to code 7.
-__device__ __forceinline__ uint32_t e2m1_sr(float v, uint32_t u16) {
-    const uint32_t bits = __float_as_uint(v);
-    const uint32_t sign = (bits >> 28) & 8u;
-    const uint32_t ab = bits & 0x7FFFFFFFu;
-    const uint32_t code_n = ((ab >> 23) - 126u) * 2u + ((ab >> 22) & 1u);
-    const uint32_t f_n = (ab >> 6) & 0xFFFFu;
-    const uint32_t f_h = (ab >> 7) & 0xFFFFu;
-    const uint32_t f_s = (uint32_t)__fmul_rz(__uint_as_float(ab), 131072.0f);
-    const bool ge1 = ab >= 0x3F800000u, ge05 = ab >= 0x3F000000u;
-    uint32_t code = ge1 ? code_n : (ge05 ? 1u : 0u);
-    const uint32_t F = ge1 ? f_n : (ge05 ? f_h : f_s);
-    code += (u16 < F) ? 1u : 0u;
-    code = (ab >= 0x40C00000u) ? 7u : code;
-    return sign | code;
-}
-
 // ---------------------------------------------------------------- Philox --
 // Philox4x32-10 (Salmon et al., SC'11): multipliers 0xD2511F53, 0xCD9E8D57,
 // key increments 0x9E3779B9, 0xBB67AE85.
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, uint32_t k0, uint32_t k1) {
+// Philox4x32-10 with every output word complemented, with the round keys
+// precomputed: key[2r], key[2r+1] = (k0 + r * 0x9E3779B9, k1 + r *
+// 0xBB67AE85) for rounds r = 0..8, and the complements of the round-9 keys
+// in key[18], key[19] (the complement of the two XOR-ed output words is folded
+// into them; the two low-product words take one NOT each).
+__device__ __forceinline__ uint4 philox4x32_10_not(uint4 c, const uint32_t* key) {
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
-        if (round > 0) {
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
         const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u;
         const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57u;
-        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ k0, (uint32_t)p1, (uint32_t)(p0 >> 32) ^ c.w ^ k1,
-                       (uint32_t)p0);
+        const uint32_t lo1 = (uint32_t)p1, lo0 = (uint32_t)p0;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ key[2 * round], round == 9 ? ~lo1 : lo1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ key[2 * round + 1], round == 9 ? ~lo0 : lo0);
     }
     return c;
 }
 
-// Random bits of the 8 elements idx = 8*g .. 8*g+7 of a quantised operand.
-__device__ __forceinline__ uint4 sr_bits8(uint64_t g, uint64_t seed, uint64_t stream_id) {
-    return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
-                                    (uint32_t)(stream_id >> 32)),
-                         (uint32_t)seed, (uint32_t)(seed >> 32));
+// Stochastic-rounding words of the 8 elements idx = 8*g .. 8*g+7 of a
+// quantised operand: the Philox block of counter (g, stream_id) under the key
+// schedule `key` (see philox4x32_10_not), complemented, so that the 16-bit
+// slice of element j (word j/2, low half first) holds rp = 65535 - u16.
+__device__ __forceinline__ uint4 sr_rp8(uint64_t g, uint64_t stream_id, const uint32_t* key) {
+    return philox4x32_10_not(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
+                                        (uint32_t)(stream_id >> 32)),
+                             key);
 }
 
-// Stochastic rounding realised as "add random bits below the kept precision,
-// then truncate".  On [1, 6) the E2M1 grid is 2^e x {1, 1.5}: the kept bits
-// are the exponent and mantissa bit 22, and the 16 bits below them hold
-// floor(frac * 2^16).  Adding rp = 65535 - u16 there carries into the kept
-// bits exactly when floor(frac * 2^16) > u16, i.e. the rule above.  Values
-// below 1 (grid 0, 0.5, 1: spacing 0.5) are first moved to [1, 2) by a
-// round-toward-zero add of 1.0 -- the truncation is below 2^-17, so
-// floor(frac * 2^16) is unchanged -- and moved back by an exact subtraction.
-// |v| is clamped to 8 first (anything >= 6 saturates to 6).  The result is
-// the chosen grid value (exact, sign kept), so RNE conversion returns its
-// code unchanged.
-__device__ __forceinline__ float sr_grid_value(float v, uint32_t rp) {
-    const uint32_t bits = __float_as_uint(v);
-    const float a = fminf(fabsf(v), 8.0f);
-    const bool lt1 = a < 1.0f;
-    const float a2 = lt1 ? __fadd_rz(a, 1.0f) : a;
+// dp2a selectors: rp * 64 from the low (SEL_LO) or high (SEL_HI) half-word.
+constexpr uint32_t SR_SEL_LO = 0x40u, SR_SEL_HI = 0x4000u;
+
+// Stochastic E2M1 rounding of one value v = x * r_b, realised as "add random
+// bits below the kept precision, then truncate".  With lo <= |v| < hi the
+// neighbouring grid values, the rule is: round up iff u16 < F = floor(frac *
+// 2^16), frac = (|v| - lo) / (hi - lo).
+//  * On [1, 16) the E2M1 grid (with 8, 12, 16 beyond the top, all of which
+//    saturate to 6) is 2^e x {1, 1.5}: the kept bits are the exponent and
+//    mantissa bit 22, and mantissa bits 21..6 hold F.  Adding rp = 65535 - u16
+//    at bit 6 carries into the kept bits exactly when F > u16.
+//  * Below 1 (grid 0, 0.5, 1: spacing 0.5) |v| is first moved to [1, 2) by a
+//    round-toward-zero add of c = 1.0 (the truncation is below 2^-17, so F is
+//    unchanged) and moved back by an exact subtraction of c.  For |v| >= 1,
+//    c = 0 and both adds are exact no-ops.
+//  * |v| < 16 always holds (|x| <= amax_b and s_b is at least 2/3 of
+//    amax_b * S_enc / 6 whenever it is non-zero), so the add never reaches
+//    the exponent field's top.
+// dp2a forms rp * 64 + bits(|v| + c) from the selected half-word of the
+// complemented Philox word in one instruction.  The result is the chosen
+// grid value, sign kept (the RNE conversion then returns its code unchanged).
+__device__ __forceinline__ float sr_grid_value(float v, uint32_t rp_word, uint32_t sel) {
+    const float a = fabsf(v);
+    float c;
+    asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(c) : "f"(a));
+    const float a2 = __fadd_rz(a, c);
     uint32_t qb;
-    asm("mad.lo.u32 %0, %1, 64, %2;" : "=r"(qb) : "r"(rp), "r"(__float_as_uint(a2)));
-    float q = __uint_as_float(qb & 0xFFC00000u);
-    q = __fsub_rn(q, lt1 ? 1.0f : 0.0f);
-    return __uint_as_float(__float_as_uint(q) | (bits & 0x80000000u));
+    asm("dp2a.lo.u32.u32 %0, %1, %2, %3;" : "=r"(qb) : "r"(rp_word), "r"(sel), "r"(__float_as_uint(a2)));
+    const float q = __fsub_rn(__uint_as_float(qb & 0xFFC00000u), c);
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(v) & 0x80000000u));
 }
 
-// Eight values -> eight SR codes (element 0 in the lowest nibble), r = the
-// Philox block of these 8 elements (slice j: word j/2, low half first).
-__device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 r) {
-    const uint32_t w[4] = {~r.x, ~r.y, ~r.z, ~r.w};      // both halves become 65535 - u16
+// Eight values -> eight SR codes (element 0 in the lowest nibble), rp = the
+// complemented Philox block of these 8 elements.
+__device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 rp) {
+    const uint32_t w[4] = {rp.x, rp.y, rp.z, rp.w};
     float g[8];
 #pragma unroll
-    for (int j = 0; j < 8; ++j) {
-        const uint32_t rp = (j & 1) ? (w[j >> 1] >> 16) : (w[j >> 1] & 0xFFFFu);
-        g[j] = sr_grid_value(v[j], rp);
-    }
+    for (int j = 0; j < 8; ++j) g[j] = sr_grid_value(v[j], w[j >> 1], (j & 1) ? SR_SEL_HI : SR_SEL_LO);
     return e2m1x8_rne(g);
 }
 
@@ -174,7 +171,7 @@ __device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 r) {
 // exact scaling by 1/4.  The sign flip is folded into the first butterfly
 // stage as fused multiply-adds by +-1: fma(s_b, b, s_a * a) rounds
 // s_a a + s_b b once, exactly like the separate negate-then-add.
-__device__ __forceinline__ void rht16(float* v, uint32_t mask) {
+__device__ __forceinline__ void rht16_first3(float* v, uint32_t mask) {
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
         const float sa = ((mask >> i) & 1u) ? -1.0f : 1.0f;
@@ -184,7 +181,7 @@ __device__ __forceinline__ void rht16(float* v, uint32_t mask) {
         v[i + 1] = __fmaf_rn(-sb, b, a);
     }
 #pragma unroll
-    for (int h = 2; h < 16; h <<= 1) {
+    for (int h = 2; h < 8; h <<= 1) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
             if (i & h) continue;
@@ -193,8 +190,34 @@ __device__ __forceinline__ void rht16(float* v, uint32_t mask) {
             v[i + h] = __fsub_rn(a, b);
         }
     }
+}
+
+// Magnitudes of the last-stage pairs: s_i = fp32(|a_i| + |b_i|) for the
+// stage-h=8 inputs a_i = v[i], b_i = v[i + 8].  For reals max(|a + b|,
+// |a - b|) = |a| + |b|; fp32 rounding is monotone and symmetric in sign, so
+// max(|fp32(a + b)|, |fp32(a - b)|) = fp32(|a| + |b|) exactly, and the
+// exact-or-monotone scaling by 1/4 keeps the maximum.  Hence
+// max_j |y_j| = fp32(max_i s_i * 1/4) bit for bit (and +Inf / NaN whenever
+// some y_j is).
+__device__ __forceinline__ void rht16_pair_mags(const float* v, float* s) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) s[i] = __fadd_rn(fabsf(v[i]), fabsf(v[i + 8]));
+}
+
+__device__ __forceinline__ void rht16_last(float* v) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+        const float a = v[i], b = v[i + 8];
+        v[i] = __fadd_rn(a, b);
+        v[i + 8] = __fsub_rn(a, b);
+    }
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+}
+
+__device__ __forceinline__ void rht16(float* v, uint32_t mask) {
+    rht16_first3(v, mask);
+    rht16_last(v);
 }
 
 // ------------------------------------------------------- scale layout -----

@@ -82,7 +82,7 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
     if (mask == 0) {
         if (x.ld == scols || srows == 1) {
             const int64_t len = srows * scols;
-            k_amax_plain<<<grid_for(cdiv(len, 32), kQuantThreads, 8), kQuantThreads, 0, st>>>(
+            k_amax_plain<<<grid_for(cdiv(len, 64), kQuantThreads, 4), kQuantThreads, 0, st>>>(
                 p, 1, len, x.ld, out);
         } else {
             const int g = (int)std::min<int64_t>(srows, (int64_t)device_sm_count() * 8);
@@ -92,7 +92,7 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
             p, x.rows, x.cols, x.ld, mask, out);
     } else {
-        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 4) * (x.cols / 16), kQuantThreads, 8), kQuantThreads,
+        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 2) * (x.cols / 16), kQuantThreads, 4), kQuantThreads,
                           0, st>>>(p, x.cols, x.rows, x.ld, mask, out);
     }
     return launch_status();
@@ -108,7 +108,7 @@ void launch_q1d(const QuantArgs& a, bool transposed, cudaStream_t st) {
         k_quant1d_rows<RHT, SR><<<grid_for(rows_pad * ngroups, kQuantThreads, 8), kQuantThreads, 0,
                                   st>>>(a);
     } else {
-        k_quant1d_cols<RHT, SR><<<grid_for((rows_pad / 2) * ngroups, kQuantThreads, 8),
+        k_quant1d_cols<RHT, SR><<<grid_for((rows_pad / 2) * ngroups, kQuantThreads, 1 << 20),
                                   kQuantThreads, 0, st>>>(a);
     }
 }
@@ -169,7 +169,17 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.gs_out = out->global_scale;
     a.gs_out2 = out_t ? out_t->global_scale : nullptr;
     a.rht_mask = mask;
-    a.seed = seed;
+    // Philox round keys of the seed; the round-9 pair is complemented (see
+    // philox4x32_10_not).
+    {
+        uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+        for (int r = 0; r < 10; ++r) {
+            a.sr_key[2 * r] = r == 9 ? ~k0 : k0;
+            a.sr_key[2 * r + 1] = r == 9 ? ~k1 : k1;
+            k0 += 0x9E3779B9u;
+            k1 += 0xBB67AE85u;
+        }
+    }
     a.stream_id = stream_id;
     const bool sr = round == NVFP4_SR;
 

@@ -43,6 +43,29 @@ __device__ __forceinline__ uint32_t ldg_u32(const void* p) {
     return v;
 }
 
+// A grid-stride walk over the items (major, minor) of a [nmajor x nminor]
+// index space, minor fastest, without a division per step.
+struct ItemWalk {
+    int64_t major, dmajor;
+    uint32_t minor, dminor, nminor;
+    __device__ __forceinline__ ItemWalk(uint32_t nminor_) : nminor(nminor_) {
+        const int64_t it0 = (int64_t)blockIdx.x * blockDim.x + threadIdx.x;
+        const int64_t stride = (int64_t)gridDim.x * blockDim.x;
+        major = it0 / nminor;
+        minor = (uint32_t)(it0 - major * nminor);
+        dmajor = stride / nminor;
+        dminor = (uint32_t)(stride - dmajor * nminor);
+    }
+    __device__ __forceinline__ void next() {
+        minor += dminor;
+        major += dmajor;
+        if (minor >= nminor) {
+            minor -= nminor;
+            ++major;
+        }
+    }
+};
+
 __device__ __forceinline__ void unpack8(uint4 w, float* v) {
     v[0] = bf16_lo(w.x); v[1] = bf16_hi(w.x);
     v[2] = bf16_lo(w.y); v[3] = bf16_hi(w.y);
@@ -50,13 +73,20 @@ __device__ __forceinline__ void unpack8(uint4 w, float* v) {
     v[6] = bf16_lo(w.w); v[7] = bf16_hi(w.w);
 }
 
-// max |v| over 16 finite values, as float bits (fmax of magnitudes; the
-// inputs of a quantiser are finite because a non-finite amax stops it).
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+    float d;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+    return d;
+}
+
+// max |v| over 16 finite values, as float bits (three-input maxima of the
+// magnitudes; the inputs of a quantiser are finite because a non-finite amax
+// stops it).
 __device__ __forceinline__ uint32_t absmax_bits16(const float* v) {
-    float m = 0.0f;
+    float m = fmax3(fabsf(v[0]), fabsf(v[1]), fabsf(v[2]));
 #pragma unroll
-    for (int j = 0; j < 16; ++j) m = fmaxf(m, fabsf(v[j]));
-    return __float_as_uint(m);
+    for (int j = 3; j < 15; j += 2) m = fmax3(m, fabsf(v[j]), fabsf(v[j + 1]));
+    return __float_as_uint(fmaxf(m, fabsf(v[15])));
 }
 
 // max |v| over 16 values as float bits, NaN-propagating (integer max of the
@@ -82,6 +112,24 @@ __device__ __forceinline__ void block_max_to_global(uint32_t m, float* out) {
         m = __reduce_max_sync(0xFFFFFFFFu, m);
         if (lane == 0 && m) atomicMax(reinterpret_cast<uint32_t*>(out), m);
     }
+}
+
+// max |RHT16(v)| as float bits, NaN-propagating.  Finite blocks take the
+// integer maximum of the non-negative pair magnitudes (see rht16_pair_mags);
+// a non-finite magnitude (where a +-Inf pair can also make a NaN output)
+// falls back to the full last stage.  v is clobbered.
+__device__ __forceinline__ uint32_t rht16_absmax_bits_nan(float* v, uint32_t mask) {
+    rht16_first3(v, mask);
+    float s[8];
+    rht16_pair_mags(v, s);
+    uint32_t m = 0;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = max(m, __float_as_uint(s[i]));
+    if (m >= 0x7F800000u) {
+        rht16_last(v);
+        return absmax_bits16_nan(v);
+    }
+    return __float_as_uint(__fmul_rn(__uint_as_float(m), 0.25f));
 }
 
 // Resolve the global encode scale for a quantiser CTA.  src holds either the
@@ -115,21 +163,24 @@ __global__ void k_publish_senc(const float* src, int src_is_senc, float* gs_out,
 
 // ============================================================== amax ======
 // max |x| (as bf16 magnitude bits) of a 16-byte aligned span, split over
-// `nt` threads starting at `tid`.
+// `nt` threads starting at `tid`: 8 independent 16-byte loads in flight per
+// thread, folded with half-word SIMD maxima of the magnitude bit patterns
+// (order-free and NaN-propagating: a NaN pattern exceeds every finite one).
 __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t len, int64_t tid,
                                                 int64_t nt) {
     constexpr uint32_t M = 0x7FFF7FFFu;
+    constexpr int U = 8;
     uint32_t m2 = 0, m1 = 0;
     const int64_t nch = len >> 3;
     const uint4* v = reinterpret_cast<const uint4*>(base);
     int64_t i = tid;
-    for (; i + 3 * nt < nch; i += 4 * nt) {
-        const uint4 a = ldg_stream(v + i), b = ldg_stream(v + i + nt);
-        const uint4 c = ldg_stream(v + i + 2 * nt), d = ldg_stream(v + i + 3 * nt);
-        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M)));
-        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(b.x & M, b.y & M), __vmaxu2(b.z & M, b.w & M)));
-        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(c.x & M, c.y & M), __vmaxu2(c.z & M, c.w & M)));
-        m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(d.x & M, d.y & M), __vmaxu2(d.z & M, d.w & M)));
+    for (; i + (U - 1) * nt < nch; i += U * nt) {
+        uint4 c[U];
+#pragma unroll
+        for (int u = 0; u < U; ++u) c[u] = ldg_stream(v + i + u * nt);
+#pragma unroll
+        for (int u = 0; u < U; ++u)
+            m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(c[u].x & M, c[u].y & M), __vmaxu2(c[u].z & M, c[u].w & M)));
     }
     for (; i < nch; i += nt) {
         const uint4 a = ldg_stream(v + i);
@@ -142,9 +193,9 @@ __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t le
 // max |x| of a bf16 array of nrows rows of len elements (leading dimension
 // ld).  One row (contiguous data): the whole grid strides over it; several
 // rows: CTAs stride over rows, threads over a row.
-__global__ void __launch_bounds__(kQuantThreads) k_amax_plain(const uint16_t* __restrict__ p,
-                                                              int64_t nrows, int64_t len,
-                                                              int64_t ld, float* out) {
+__global__ void __launch_bounds__(kQuantThreads, 4) k_amax_plain(const uint16_t* __restrict__ p,
+                                                                 int64_t nrows, int64_t len,
+                                                                 int64_t ld, float* out) {
     uint32_t m = 0;
     if (nrows == 1) {
         m = span_absmax(p, len, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
@@ -171,50 +222,39 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
         float v[16];
         unpack8(ldg_stream(src), v);
         unpack8(ldg_stream(src + 1), v + 8);
-        rht16(v, mask);
-        m = max(m, absmax_bits16_nan(v));
+        m = max(m, rht16_absmax_bits_nan(v, mask));
     }
     block_max_to_global(m, out);
 }
 
 // max |RHT16(x)| over 16-chunks down the stored columns (transposed view:
 // the logical k runs along the stored rows).  One thread: 16 stored rows x
-// 4 stored columns (8-byte loads; a warp covers 256 contiguous bytes of a row).
-__global__ void __launch_bounds__(kQuantThreads) k_amax_rht_cols(const uint16_t* __restrict__ p,
-                                                                 int64_t srows, int64_t scols,
-                                                                 int64_t ld, uint32_t mask,
-                                                                 float* out) {
+// 2 stored columns (4-byte loads; a warp covers 128 contiguous bytes of a
+// row), transformed one column at a time.
+__global__ void __launch_bounds__(kQuantThreads, 4) k_amax_rht_cols(const uint16_t* __restrict__ p,
+                                                                    int64_t srows, int64_t scols,
+                                                                    int64_t ld, uint32_t mask,
+                                                                    float* out) {
     uint32_t m = 0;
-    const int64_t ncb = (scols + 3) >> 2, nkb = srows >> 4;
-    const int64_t total = ncb * nkb;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t kb = it / ncb, cb = it - kb * ncb;
-        const int64_t c0 = cb * 4;
-        const uint16_t* base = p + kb * 16 * ld + c0;
-        float v[4][16];
-        if (c0 + 4 <= scols) {
-            uint2 w[16];
+    const int64_t ncp = (scols + 1) >> 1, nkb = srows >> 4;
+    for (ItemWalk it((uint32_t)ncp); it.major < nkb; it.next()) {
+        const int64_t c0 = (int64_t)it.minor * 2;
+        const uint16_t* base = p + it.major * 16 * ld + c0;
+        uint32_t w[16];
+        if (c0 + 2 <= scols) {
 #pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = *reinterpret_cast<const uint2*>(base + t * ld);
-#pragma unroll
-            for (int t = 0; t < 16; ++t) {
-                v[0][t] = bf16_lo(w[t].x); v[1][t] = bf16_hi(w[t].x);
-                v[2][t] = bf16_lo(w[t].y); v[3][t] = bf16_hi(w[t].y);
-            }
+            for (int t = 0; t < 16; ++t) w[t] = ldg_u32(base + t * ld);
         } else {
 #pragma unroll
-            for (int t = 0; t < 16; ++t)
-#pragma unroll
-                for (int c = 0; c < 4; ++c)
-                    v[c][t] = (c0 + c < scols) ? __uint_as_float((uint32_t)base[t * ld + c] << 16)
-                                               : 0.0f;
+            for (int t = 0; t < 16; ++t) w[t] = (uint32_t)base[t * ld];
         }
+        float v[16];
 #pragma unroll
-        for (int c = 0; c < 4; ++c) {
-            rht16(v[c], mask);
-            m = max(m, absmax_bits16_nan(v[c]));
-        }
+        for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
+        m = max(m, rht16_absmax_bits_nan(v, mask));
+#pragma unroll
+        for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
+        m = max(m, rht16_absmax_bits_nan(v, mask));
     }
     block_max_to_global(m, out);
 }
@@ -240,7 +280,8 @@ struct QuantArgs {
     uint8_t* codes;             // [rows x k/2]
     uint8_t* scales;            // swizzled
     uint32_t rht_mask;
-    uint64_t seed, stream_id;
+    uint64_t stream_id;
+    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10_not)
     // 2D transposed emit (optional)
     uint8_t* codes_t;           // [k x rows/2]
     uint8_t* scales_t;
@@ -248,31 +289,53 @@ struct QuantArgs {
     int write_primary;
 };
 
-// amax of 16 bf16 values held as 8 packed words: half-word SIMD max of the
-// magnitudes, returned as a float bit pattern.
+// |a| max |b| per bf16 half (the sign bits of the result are junk).
+__device__ __forceinline__ uint32_t bf16x2_absmax(uint32_t a, uint32_t b) {
+    uint32_t d;
+    asm("max.xorsign.abs.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+// amax of 16 finite bf16 values held as 8 packed words, returned as a float
+// bit pattern.
 __device__ __forceinline__ uint32_t absmax_bits16_packed(uint4 a, uint4 b) {
-    constexpr uint32_t M = 0x7FFF7FFFu;
-    uint32_t m = __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M));
-    m = __vmaxu2(m, __vmaxu2(__vmaxu2(b.x & M, b.y & M), __vmaxu2(b.z & M, b.w & M)));
-    return max(m << 16, m & 0xFFFF0000u);
+    const uint32_t m = bf16x2_absmax(bf16x2_absmax(bf16x2_absmax(a.x, a.y), bf16x2_absmax(a.z, a.w)),
+                                     bf16x2_absmax(bf16x2_absmax(b.x, b.y), bf16x2_absmax(b.z, b.w)));
+    return max((m & 0x7FFFu) << 16, m & 0x7FFF0000u);
+}
+
+// Per-CTA table of the encode factor r_b for every E4M3 code 0..127 (the
+// block scale is never negative, and 0x7F is never produced).
+__device__ __forceinline__ void init_rtab(float* rtab, float s_enc) {
+    for (int c = threadIdx.x; c < 128; c += blockDim.x) rtab[c] = encode_factor(s_enc, (uint32_t)c);
+    __syncthreads();
 }
 
 // Encode one 16-element block.  amax_bits: the block's max |value| as float
 // bits when already known (raw bf16 input), or ~0u to compute it here.
 template <bool RHT, bool SR>
-__device__ __forceinline__ void encode_block16(float* v, float s_enc, uint64_t idx0,
+__device__ __forceinline__ void encode_block16(float* v, float s_enc, const float* rtab, uint64_t idx0,
                                                const QuantArgs& a, uint32_t* sb_out,
                                                uint32_t* code_lo, uint32_t* code_hi,
                                                uint32_t amax_bits = ~0u) {
-    if (RHT) rht16(v, a.rht_mask);
-    if (RHT || amax_bits == ~0u) amax_bits = absmax_bits16(v);
-    float r_b;
-    *sb_out = block_scale(__uint_as_float(amax_bits), s_enc, &r_b);
+    if (RHT) {
+        rht16_first3(v, a.rht_mask);
+        float s[8];
+        rht16_pair_mags(v, s);
+        const float m = fmaxf(fmax3(s[0], s[1], s[2]), fmax3(fmax3(s[3], s[4], s[5]), s[6], s[7]));
+        amax_bits = __float_as_uint(__fmul_rn(m, 0.25f));
+        rht16_last(v);
+    } else if (amax_bits == ~0u) {
+        amax_bits = absmax_bits16(v);
+    }
+    const uint32_t sb = block_scale_code(__uint_as_float(amax_bits), s_enc);
+    const float r_b = rtab[sb];
+    *sb_out = sb;
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], r_b);
     if (SR) {
-        *code_lo = e2m1x8_sr(v, sr_bits8(idx0 >> 3, a.seed, a.stream_id));
-        *code_hi = e2m1x8_sr(v + 8, sr_bits8((idx0 >> 3) + 1, a.seed, a.stream_id));
+        *code_lo = e2m1x8_sr(v, sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+        *code_hi = e2m1x8_sr(v + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
     } else {
         *code_lo = e2m1x8_rne(v);
         *code_hi = e2m1x8_rne(v + 8);
@@ -281,24 +344,24 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, uint64_t i
 
 // Non-transposed view: thread item = (row, group of 4 blocks).
 template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_rows(QuantArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, RHT && SR ? 2 : 3) k_quant1d_rows(const QuantArgs a) {
+    __shared__ float rtab[128];
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
+    init_rtab(rtab, s_enc);
     const int64_t nkb = a.k >> 4;
     const uint32_t ngroups = (uint32_t)((nkb + 3) >> 2);
     const int64_t rows_pad = (a.rows + 127) & ~int64_t(127);
-    const int64_t total = rows_pad * ngroups;
     const bool vec16 = (a.k & 31) == 0;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = it / ngroups;
-        const int64_t g = it - r * ngroups;
+    for (ItemWalk w(ngroups); w.major < rows_pad; w.next()) {
+        const int64_t r = w.major;
+        const uint32_t g = w.minor;
         uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
         if (r >= a.rows) {
             *sdst = 0u;
             continue;
         }
-        const int nblk = (int)min64(4, nkb - g * 4);
+        const int nblk = (int)min64(4, nkb - (int64_t)g * 4);
         const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64);
         uint4 raw[8];
 #pragma unroll
@@ -316,7 +379,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_rows(QuantArgs a) 
                 unpack8(raw[2 * b], v);
                 unpack8(raw[2 * b + 1], v + 8);
                 uint32_t sb;
-                encode_block16<RHT, SR>(v, s_enc, (uint64_t)(r * a.k + g * 64 + b * 16), a, &sb,
+                encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)(r * a.k + g * 64 + b * 16), a, &sb,
                                         &cw[2 * b], &cw[2 * b + 1],
                                         RHT ? ~0u : absmax_bits16_packed(raw[2 * b], raw[2 * b + 1]));
                 sw |= sb << (8 * b);
@@ -335,81 +398,80 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_rows(QuantArgs a) 
     }
 }
 
-// Transposed view (stored [k x rows]): thread item = (pair of logical rows,
-// group of 4 blocks along the logical k = the stored rows).
+// 16 stored rows x 2 stored columns starting at src (one 16-element block of
+// two logical rows of the transposed view), one 32-bit word per stored row.
+__device__ __forceinline__ void load_col_pair(const uint16_t* src, int64_t ld, bool has2, uint32_t* w) {
+    if (has2) {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) w[t] = ldg_u32(src + t * ld);
+    } else {
+#pragma unroll
+        for (int t = 0; t < 16; ++t) w[t] = (uint32_t)src[t * ld];
+    }
+}
+
+// Transposed view (stored [k x rows]): thread item = (group of 4 blocks along
+// the logical k = the stored rows, pair of logical rows), pairs fastest so a
+// warp reads 128 contiguous bytes of each stored row.  The next block's 16
+// words are loaded while the current block is encoded; each block's codes are
+// stored as soon as they are made.
 template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(QuantArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(const QuantArgs a) {
+    __shared__ float rtab[128];
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
+    init_rtab(rtab, s_enc);
     const int64_t nkb = a.k >> 4;
     const int64_t ngroups = (nkb + 3) >> 2;
     const int64_t rows_pad = (a.rows + 127) & ~int64_t(127);
-    const int64_t npairs = rows_pad >> 1;
-    const int64_t total = npairs * ngroups;
-    const bool vec16 = (a.k & 31) == 0;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t g = it / npairs;
-        const int64_t r0 = (it - g * npairs) * 2;
+    const uint32_t npairs = (uint32_t)(rows_pad >> 1);
+    for (ItemWalk it(npairs); it.major < ngroups; it.next()) {
+        const int64_t g = it.major;
+        const int64_t r0 = (int64_t)it.minor * 2;
+        uint32_t* s0 = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0, g * 4, ngroups));
+        uint32_t* s1 = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups));
         if (r0 >= a.rows) {
-            *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0, g * 4, ngroups)) = 0u;
-            *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups)) = 0u;
+            *s0 = 0u;
+            *s1 = 0u;
             continue;
         }
         const bool has2 = r0 + 1 < a.rows;
         const int nblk = (int)min64(4, nkb - g * 4);
-        uint32_t sw0 = 0, sw1 = 0, c0w[8], c1w[8];
+        const uint16_t* src = a.x + g * 64 * a.ld + r0;
+        uint8_t* c0 = a.codes + r0 * (a.k >> 1) + g * 32;
+        uint8_t* c1 = c0 + (a.k >> 1);
+        uint32_t sw0 = 0, sw1 = 0;
+        uint32_t w[16];
+        load_col_pair(src, a.ld, has2, w);
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
-            c0w[2 * b] = c0w[2 * b + 1] = c1w[2 * b] = c1w[2 * b + 1] = 0u;
             if (b < nblk) {
-                const uint16_t* src = a.x + (g * 64 + b * 16) * a.ld + r0;
-                uint32_t w[16];
-                if (has2) {
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) w[t] = ldg_u32(src + t * a.ld);
-                } else {
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) w[t] = (uint32_t)src[t * a.ld];
-                }
-                float v0[16], v1[16];
-#pragma unroll
-                for (int t = 0; t < 16; ++t) {
-                    v0[t] = bf16_lo(w[t]);
-                    v1[t] = bf16_hi(w[t]);
-                }
+                uint32_t wn[16];
+                if (b + 1 < nblk) load_col_pair(src + (b + 1) * 16 * a.ld, a.ld, has2, wn);
                 const int64_t kc = g * 64 + b * 16;
-                uint32_t sb;
-                encode_block16<RHT, SR>(v0, s_enc, (uint64_t)(r0 * a.k + kc), a, &sb, &c0w[2 * b],
-                                        &c0w[2 * b + 1]);
+                float v[16];
+                uint32_t sb, lo, hi;
+#pragma unroll
+                for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
+                encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)(r0 * a.k + kc), a, &sb, &lo, &hi);
+                reinterpret_cast<uint2*>(c0)[b] = make_uint2(lo, hi);
                 sw0 |= sb << (8 * b);
                 if (has2) {
-                    encode_block16<RHT, SR>(v1, s_enc, (uint64_t)((r0 + 1) * a.k + kc), a, &sb,
-                                            &c1w[2 * b], &c1w[2 * b + 1]);
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
+                    encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)((r0 + 1) * a.k + kc), a, &sb, &lo,
+                                            &hi);
+                    reinterpret_cast<uint2*>(c1)[b] = make_uint2(lo, hi);
                     sw1 |= sb << (8 * b);
+                }
+                if (b + 1 < nblk) {
+#pragma unroll
+                    for (int t = 0; t < 16; ++t) w[t] = wn[t];
                 }
             }
         }
-#pragma unroll
-        for (int rr = 0; rr < 2; ++rr) {
-            if (rr == 1 && !has2) {
-                *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups)) = 0u;
-                continue;
-            }
-            const uint32_t* cw = rr ? c1w : c0w;
-            uint8_t* cdst = a.codes + (r0 + rr) * (a.k >> 1) + g * 32;
-            if (nblk == 4 && vec16) {
-                reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    if (b < nblk)
-                        reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-            }
-            *reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + rr, g * 4, ngroups)) =
-                rr ? sw1 : sw0;
-        }
+        *s0 = sw0;
+        *s1 = sw1;
     }
 }
 
@@ -420,9 +482,47 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(QuantArgs a) 
 // (covering the 128-padded row count).
 constexpr int k2DThreads = 128;
 
+// In-register transpose of an 8x8 matrix of nibbles: on entry x[i] holds
+// row i (nibble n = column n, low nibble first); on exit x[n] holds column n
+// (nibble i = row i).  Three independent swaps of row and column index bits:
+// bit 2 (16-bit halves) and bit 1 (bytes) by byte permutes, bit 0 (nibbles)
+// by masks.
+__device__ __forceinline__ void transpose8x8_nibbles(uint32_t* x) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const uint32_t a = x[i], b = x[i + 4];
+        x[i] = __byte_perm(a, b, 0x5410);
+        x[i + 4] = __byte_perm(a, b, 0x7632);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += (i & 1) ? 3 : 1) {      // 0, 1, 4, 5
+        const uint32_t a = x[i], b = x[i + 2];
+        x[i] = __byte_perm(a, b, 0x6240);
+        x[i + 2] = __byte_perm(a, b, 0x7351);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; i += 2) {
+        const uint32_t a = x[i], b = x[i + 1];
+        x[i] = (a & 0x0F0F0F0Fu) | ((b << 4) & 0xF0F0F0F0u);
+        x[i + 1] = ((a >> 4) & 0x0F0F0F0Fu) | (b & 0xF0F0F0F0u);
+    }
+}
+
+// Code tile of the transposed emit: 64 rows x 16 words (128 nibbles), stored
+// swizzled so that both the producer's 16-byte row writes (8 consecutive rows
+// per quarter-warp) and the transposer's word reads (8 row blocks x 4 word
+// columns per warp) are free of bank conflicts.  Logical (row R, 16-byte
+// chunk q, word u) lives at physical row R ^ bit3(R) and chunk
+// q ^ ((R >> 1) ^ (R >> 4)) & 3.
+__device__ __forceinline__ int tile_word(int R, int w) {
+    const int rp = R ^ ((R >> 3) & 1);
+    const int qp = (w >> 2) ^ (((R >> 1) ^ (R >> 4)) & 3);
+    return rp * 16 + qp * 4 + (w & 3);
+}
+
 template <bool RHT, bool SR, bool EMIT_T>
-__global__ void __launch_bounds__(k2DThreads) k_quant2d(QuantArgs a) {
-    __shared__ uint8_t tile_codes[64][64];     // [row][byte]: 128 nibbles per row
+__global__ void __launch_bounds__(k2DThreads) k_quant2d(const QuantArgs a) {
+    __shared__ __align__(16) uint32_t tile_codes[64 * 16];
     __shared__ uint8_t tile_sb[4][8];          // [row block][k block]
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
@@ -462,9 +562,8 @@ __global__ void __launch_bounds__(k2DThreads) k_quant2d(QuantArgs a) {
     uint32_t sw = 0, cw[8];
 #pragma unroll
     for (int b = 0; b < 4; ++b) {
-        float r_b;
-        const uint32_t sb = (b < nblk) ? block_scale(__uint_as_float(lmax[b]), s_enc, &r_b) : 0u;
-        if (b >= nblk) r_b = 0.0f;
+        const uint32_t sb = (b < nblk) ? block_scale_code(__uint_as_float(lmax[b]), s_enc) : 0u;
+        const float r_b = (b < nblk) ? encode_factor(s_enc, sb) : 0.0f;
         sw |= sb << (8 * b);
 #pragma unroll
         for (int j = 0; j < 16; ++j) v[b][j] = __fmul_rn(v[b][j], r_b);
@@ -473,22 +572,25 @@ __global__ void __launch_bounds__(k2DThreads) k_quant2d(QuantArgs a) {
             if (row_ok && b < nblk) {
                 const int64_t c0 = g * 64 + b * 16;
                 if (a.idx_transposed) {
-                    // index in the transposed logical layout: (r, c) -> c * rows + r
+                    // index in the transposed logical layout: (r, c) -> c * rows + r;
+                    // rows is a multiple of 16, so every element of the strip
+                    // takes the same slice (r & 7) of its own Philox block.
+                    const uint32_t sel = (r & 1) ? SR_SEL_HI : SR_SEL_LO;
+                    const uint32_t wsel = (uint32_t)(r & 7) >> 1;
+                    float gv[16];
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
-                        const uint4 rb = sr_bits8(idx >> 3, a.seed, a.stream_id);
-                        const uint32_t sel = (uint32_t)(idx & 7u) >> 1;
-                        const uint32_t w = sel == 0 ? rb.x : sel == 1 ? rb.y : sel == 2 ? rb.z : rb.w;
-                        const uint32_t u = (idx & 1u) ? (w >> 16) : (w & 0xFFFFu);
-                        const uint32_t q = e2m1_sr(v[b][j], u);
-                        if (j < 8) lo |= q << (4 * j);
-                        else hi |= q << (4 * (j - 8));
+                        const uint4 rb = sr_rp8(idx >> 3, a.stream_id, a.sr_key);
+                        const uint32_t w = wsel == 0 ? rb.x : wsel == 1 ? rb.y : wsel == 2 ? rb.z : rb.w;
+                        gv[j] = sr_grid_value(v[b][j], w, sel);
                     }
+                    lo = e2m1x8_rne(gv);
+                    hi = e2m1x8_rne(gv + 8);
                 } else {
                     const uint64_t idx0 = (uint64_t)(r * a.k + c0);
-                    lo = e2m1x8_sr(v[b], sr_bits8(idx0 >> 3, a.seed, a.stream_id));
-                    hi = e2m1x8_sr(v[b] + 8, sr_bits8((idx0 >> 3) + 1, a.seed, a.stream_id));
+                    lo = e2m1x8_sr(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+                    hi = e2m1x8_sr(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
                 }
             }
             cw[2 * b] = lo;
@@ -518,54 +620,52 @@ __global__ void __launch_bounds__(k2DThreads) k_quant2d(QuantArgs a) {
     if (!EMIT_T) return;
     // transposed operand: rows = k, k = a.rows (a multiple of 16 here)
     {
-        uint4* trow = reinterpret_cast<uint4*>(&tile_codes[warp * 16 + (lane & 15)][32 * (lane >> 4)]);
+        const int R = warp * 16 + (lane & 15);
         const bool live = row_ok && grp_ok;
-        trow[0] = live ? make_uint4(cw[0], cw[1], cw[2], cw[3]) : make_uint4(0, 0, 0, 0);
-        trow[1] = live ? make_uint4(cw[4], cw[5], cw[6], cw[7]) : make_uint4(0, 0, 0, 0);
+        const int h = lane >> 4;
+        *reinterpret_cast<uint4*>(&tile_codes[tile_word(R, 8 * h)]) =
+            live ? make_uint4(cw[0], cw[1], cw[2], cw[3]) : make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(&tile_codes[tile_word(R, 8 * h + 4)]) =
+            live ? make_uint4(cw[4], cw[5], cw[6], cw[7]) : make_uint4(0, 0, 0, 0);
         if ((lane & 15) == 0) {
 #pragma unroll
-            for (int b = 0; b < 4; ++b) tile_sb[warp][(lane >> 4) * 4 + b] = (sw >> (8 * b)) & 0xFFu;
+            for (int b = 0; b < 4; ++b) tile_sb[warp][h * 4 + b] = (sw >> (8 * b)) & 0xFFu;
         }
     }
     __syncthreads();
-    const int64_t ct = (int64_t)blockIdx.x * 128 + threadIdx.x;   // row of the transposed operand
-    const int64_t kt = a.rows;                                     // its k
+    const int64_t kt = a.rows;                                     // k of the transposed operand
     const int64_t ngroups_t = ((kt >> 4) + 3) >> 2;
-    const int64_t ct_pad = (a.k + 127) & ~int64_t(127);
-    if (ct >= ct_pad) return;
     const int64_t gt = row0 >> 6;                                  // 4 blocks of 16 rows
     if (gt >= ngroups_t) return;                                   // beyond the padded columns
-    uint32_t* sdst_t = reinterpret_cast<uint32_t*>(a.scales_t + scale_offset(ct, gt * 4, ngroups_t));
-    if (ct >= a.k) {
-        *sdst_t = 0u;
-        return;
-    }
-    const int c_local = threadIdx.x;                               // 0..127
-    const int kb_local = c_local >> 4;
-    *sdst_t = (uint32_t)tile_sb[0][kb_local] | ((uint32_t)tile_sb[1][kb_local] << 8) |
-              ((uint32_t)tile_sb[2][kb_local] << 16) | ((uint32_t)tile_sb[3][kb_local] << 24);
-    if (row0 >= a.rows) return;
-    uint32_t out[8];
-#pragma unroll
-    for (int wv = 0; wv < 8; ++wv) {
-        uint32_t word = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) {
-            const uint8_t byte = tile_codes[wv * 8 + j][c_local >> 1];
-            const uint32_t nib = (c_local & 1) ? (byte >> 4) : (byte & 0xFu);
-            word |= nib << (4 * j);
+    {
+        // scales: thread = one row (stored column) of the transposed operand
+        const int64_t ct = (int64_t)blockIdx.x * 128 + threadIdx.x;
+        const int64_t ct_pad = (a.k + 127) & ~int64_t(127);
+        if (ct < ct_pad) {
+            uint32_t* sdst_t =
+                reinterpret_cast<uint32_t*>(a.scales_t + scale_offset(ct, gt * 4, ngroups_t));
+            const int kb_local = threadIdx.x >> 4;
+            *sdst_t = ct >= a.k ? 0u
+                                : (uint32_t)tile_sb[0][kb_local] | ((uint32_t)tile_sb[1][kb_local] << 8) |
+                                      ((uint32_t)tile_sb[2][kb_local] << 16) |
+                                      ((uint32_t)tile_sb[3][kb_local] << 24);
         }
-        out[wv] = word;
     }
-    const int64_t rows_here = min64(64, a.rows - row0);     // multiple of 16
-    uint8_t* cdst = a.codes_t + ct * (kt >> 1) + (row0 >> 1);
-    if (rows_here == 64 && (kt & 31) == 0) {
-        reinterpret_cast<uint4*>(cdst)[0] = make_uint4(out[0], out[1], out[2], out[3]);
-        reinterpret_cast<uint4*>(cdst)[1] = make_uint4(out[4], out[5], out[6], out[7]);
-    } else {
-        for (int q = 0; q < rows_here / 16; ++q)
-            reinterpret_cast<uint2*>(cdst)[q] = make_uint2(out[2 * q], out[2 * q + 1]);
-    }
+    if (row0 >= a.rows) return;
+    // codes: thread = 8 stored rows (rb) x 8 stored columns (cb) of the tile,
+    // transposed in registers; a warp writes 4 columns x 32 contiguous bytes.
+    const int rb = threadIdx.x & 7, cb = threadIdx.x >> 3;
+    const int64_t rows_here = min64(64, a.rows - row0);            // multiple of 16
+    if (rb * 8 >= rows_here) return;
+    uint32_t x[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) x[i] = tile_codes[tile_word(rb * 8 + i, cb)];
+    transpose8x8_nibbles(x);
+    const int64_t c0 = (int64_t)blockIdx.x * 128 + cb * 8;
+    uint8_t* cdst = a.codes_t + c0 * (kt >> 1) + (row0 >> 1) + rb * 4;
+#pragma unroll
+    for (int n = 0; n < 8; ++n)
+        if (c0 + n < a.k) *reinterpret_cast<uint32_t*>(cdst + n * (kt >> 1)) = x[n];
 }
 
 // ======================================================== dequantise ======
