@@ -84,6 +84,7 @@ struct Args {
     int k_steps;               // ceil(K / 64): MMAs along k
     int sf_col_tiles;          // ceil(K / 64): 512-byte scale tiles per 128-row group
     int b_row_tiles;           // ceil(N / 128)
+    int n_fastest;             // tile walk: 1 = N blocks fastest (B stays in L2), 0 = M fastest
 };
 
 // Instruction descriptor of kind::mxf4nvf4: dense, A and B E2M1 (format 1),
@@ -219,7 +220,8 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         uint32_t fills[STAGES] = {};
         bool ok = true;
         for (int tile = blockIdx.x; tile < num_tiles && ok; tile += gridDim.x) {
-            const int m_blk = tile % args.m_tiles, n_blk = tile / args.m_tiles;
+            const int m_blk = args.n_fastest ? tile / args.n_tiles : tile % args.m_tiles;
+            const int n_blk = args.n_fastest ? tile % args.n_tiles : tile / args.m_tiles;
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag)) {
                     ok = false;
@@ -340,11 +342,13 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         const int quarter = warp & 3;
         const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
         const uint32_t stg = smem_addr(epi_stage) + (uint32_t)(warp - 2) * EPI_WARP_BYTES;
+        const uint64_t out_policy = l2_policy_evict_first();   // D is written once
         int local = 0;
         for (int tile = blockIdx.x; tile < num_tiles; tile += gridDim.x, ++local) {
             if (!mbar_wait_bounded(acc_full, (uint32_t)local & 1u, abort_flag)) break;
             tc_fence_after();
-            const int m_blk = tile % args.m_tiles, n_blk = tile / args.m_tiles;
+            const int m_blk = args.n_fastest ? tile / args.n_tiles : tile % args.m_tiles;
+            const int n_blk = args.n_fastest ? tile % args.n_tiles : tile / args.m_tiles;
             const int64_t row = (int64_t)m_blk * BM + quarter * 32 + lane;
             const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16);
             if (TMA_EPI && local > 0) {
@@ -373,7 +377,7 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
                     const int y = m_blk * BM + quarter * 32;
                     for (int b = 0; b < BN / 64; ++b) {
                         const int x = n_blk * BN + b * 64;
-                        if (x < args.N && y < args.M) tma_store_2d(&tma_d, epi_stage + (warp - 2) * EPI_WARP_BYTES + b * 4096, x, y);
+                        if (x < args.N && y < args.M) tma_store_2d_hint(&tma_d, epi_stage + (warp - 2) * EPI_WARP_BYTES + b * 4096, x, y, out_policy);
                     }
                     bulk_commit_group();
                 }

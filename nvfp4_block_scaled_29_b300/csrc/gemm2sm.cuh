@@ -24,8 +24,9 @@
 //               K=64, 4 per stage; tcgen05.commit multicasts the stage
 //               release to both CTAs' empty barriers and the tile's end to
 //               both CTAs' accumulator barriers.
-//  * warps 2-5: epilogue of the CTA's own 128 accumulator rows; they release
-//               the accumulator on the LEADER's barrier.
+//  * warps 2-5, 10-13: epilogue of the CTA's own 128 accumulator rows, two
+//               warps per TMEM lane quarter (accumulator columns 0-127 and
+//               128-255); they release the accumulator on the LEADER's barrier.
 // TMEM (each CTA, allocated collectively): [0, 256) accumulator, [256, 496)
 // scale slots of the 5-stage ring.  Every wait is bounded as in gemm.cuh.
 #pragma once
@@ -49,12 +50,13 @@ constexpr int SFA_BYTES = (BK / 64) * 512;              // 2 KB
 constexpr int SFB_BYTES = 2 * (BK / 64) * 512;          // 4 KB: both 128-row halves
 constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
 constexpr int STAGES = 5;
-// epilogue staging: per epilogue warp two 32-row x 64-column BF16 blocks
-// (4 KB each, 128-byte swizzle), double-buffered against the TMA stores
+// epilogue staging: per epilogue warp one 32-row x 64-column BF16 block
+// (4 KB, 128-byte swizzle)
+constexpr int EPI_WARPS = 8;
 constexpr int EPI_BLOCK = 32 * 64 * 2;
-constexpr int EPI_WARP_BYTES = 2 * EPI_BLOCK;
-constexpr int EPI_BYTES = 4 * EPI_WARP_BYTES;
-constexpr int THREADS = gemm::THREADS;
+constexpr int EPI_BYTES = EPI_WARPS * EPI_BLOCK;
+// warps: 0 TMA producer, 1 MMA issuer, 2-5 and 10-13 epilogue, 6-9 scale factors
+constexpr int THREADS = 14 * 32;
 constexpr int TMEM_COLS = gemm::TMEM_COLS;
 constexpr int TMEM_SF_BASE = gemm::TMEM_SF_BASE;
 constexpr int SF_COLS = gemm::SF_COLS_PER_STAGE;
@@ -68,6 +70,16 @@ static_assert(TMEM_SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
 // kind::mxf4nvf4 instruction descriptor for M = 256 (a CTA pair), N = 256.
 __host__ __device__ constexpr uint32_t make_idesc() {
     return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+}
+
+// Unit u -> (M unit, N block).  The walk keeps the smaller operand resident
+// in L2: M fastest when A is the smaller one (every A tile is revisited for
+// each N block while B streams), N fastest otherwise.
+__device__ __forceinline__ int unit_m(int u, int m_units, const Args& a) {
+    return a.n_fastest ? u / a.n_tiles : u % m_units;
+}
+__device__ __forceinline__ int unit_n(int u, int m_units, const Args& a) {
+    return a.n_fastest ? u % a.n_tiles : u / m_units;
 }
 
 template <bool TMA_EPI>
@@ -113,7 +125,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             mbar_init(&empty_bar[s], 1);
         }
         mbar_init(acc_full, 1);
-        mbar_init(acc_empty, 8);                   // 4 epilogue warps x 2 CTAs
+        mbar_init(acc_empty, 2 * EPI_WARPS);       // 8 epilogue warps x 2 CTAs
         mbar_init(drain_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
@@ -143,7 +155,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         uint32_t fills[STAGES] = {};
         bool ok = true;
         for (int u = unit0; u < num_units && ok; u += unit_step) {
-            const int m_blk = (u % m_units) * 2 + rank, n_blk = u / m_units;
+            const int m_blk = unit_m(u, m_units, args) * 2 + rank, n_blk = unit_n(u, m_units, args);
             for (int kb = 0; kb < args.k_blocks; ++kb) {
                 if (!mbar_wait_bounded(&empty_bar[stage], phase ^ 1u, abort_flag)) {
                     ok = false;
@@ -183,7 +195,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
             for (int s = 0; s < STAGES; ++s)
                 if (fills[s]) mbar_wait_bounded(&empty_bar[s], (fills[s] - 1) & 1u, abort_flag);
         }
-    } else if (warp >= 6) {
+    } else if (warp >= 6 && warp < 10) {
         // --------------------------------------------- scale-factor warps --
         const uint32_t lane_base = (uint32_t)((warp & 3) * 32) << 16;
         int stage = 0;
@@ -279,80 +291,78 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         __syncwarp();
     } else {
         // --------------------------------------------------- epilogue ----
-        // The CTA's 128 x 256 accumulator half is drained into registers as
-        // BF16 in two 128-column halves (64 packed words per thread) and is
-        // released after the second half's TMEM loads; the output streams out
-        // through two 4 KB staging blocks per warp.
+        // Each epilogue warp drains 32 accumulator rows (its TMEM lane
+        // quarter) x 128 columns (its half), 16 columns per TMEM load with the
+        // next load in flight, and releases the accumulator as soon as its
+        // last column has been read.  Columns 0-63 of the half stream out
+        // through the warp's 4 KB staging block before the release, columns
+        // 64-127 are held in registers and follow it.
         const int quarter = warp & 3;
+        const int col0 = warp >= 10 ? BN / 2 : 0;
+        const int ew = warp < 6 ? warp - 2 : warp - 6;
         const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
-        const uint32_t stg = smem_addr(epi_stage) + (uint32_t)(warp - 2) * EPI_WARP_BYTES;
+        const uint32_t stg = smem_addr(epi_stage) + (uint32_t)ew * EPI_BLOCK;
+        const uint64_t out_policy = l2_policy_evict_first();   // D is written once
         int local = 0;
         for (int u = unit0; u < num_units; u += unit_step, ++local) {
             if (!mbar_wait_bounded(acc_full, (uint32_t)local & 1u, abort_flag)) break;
             tc_fence_after();
-            const int m_blk = (u % m_units) * 2 + rank, n_blk = u / m_units;
+            const int m_blk = unit_m(u, m_units, args) * 2 + rank, n_blk = unit_n(u, m_units, args);
             const int64_t row = (int64_t)m_blk * HALF + quarter * 32 + lane;
-            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16);
+            const uint32_t t_row = tmem_base + ((uint32_t)(quarter * 32) << 16) + (uint32_t)col0;
             if (TMA_EPI) {
                 const int y = m_blk * HALF + quarter * 32;
+                uint32_t packed[32];
+                uint32_t acc[2][16];
+                tmem_ld_32x32b_x16(t_row, acc[0]);
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    // 128 accumulator columns -> 64 packed BF16 pairs
-                    uint32_t packed[BN / 4];
-                    uint32_t acc[32];
+                for (int c = 0; c < BN / 32; ++c) {
+                    tmem_ld_wait16(acc[c & 1]);
+                    if (c + 1 < BN / 32) tmem_ld_32x32b_x16(t_row + (c + 1) * 16, acc[(c + 1) & 1]);
 #pragma unroll
-                    for (int c = 0; c < BN / 64; ++c) {
-                        tmem_ld_32x32b_x32(t_row + (h * (BN / 64) + c) * 32, acc);
-                        tmem_ld_wait();
-#pragma unroll
-                        for (int j = 0; j < 16; ++j) {
-                            __nv_bfloat162 hv = __floats2bfloat162_rn(
-                                __fmul_rn(__uint_as_float(acc[2 * j]), alpha),
-                                __fmul_rn(__uint_as_float(acc[2 * j + 1]), alpha));
-                            packed[c * 16 + j] = *reinterpret_cast<uint32_t*>(&hv);
+                    for (int j = 0; j < 8; ++j) {
+                        __nv_bfloat162 hv = __floats2bfloat162_rn(
+                            __fmul_rn(__uint_as_float(acc[c & 1][2 * j]), alpha),
+                            __fmul_rn(__uint_as_float(acc[c & 1][2 * j + 1]), alpha));
+                        packed[(c & 3) * 8 + j] = *reinterpret_cast<uint32_t*>(&hv);
+                    }
+                    if (c == 3 || c == BN / 32 - 1) {
+                        if (c == BN / 32 - 1) {             // accumulator fully read
+                            tc_fence_before();
+                            __syncwarp();
+                            if (leader) mbar_arrive_cluster(acc_empty_leader);
                         }
-                    }
-                    if (h == 1) {                               // accumulator fully read
-                        tc_fence_before();
+                        if (leader) bulk_wait_read_all();   // the block's last store has read it
                         __syncwarp();
-                        if (leader) mbar_arrive_cluster(acc_empty_leader);
-                    }
-#pragma unroll
-                    for (int bb = 0; bb < 2; ++bb) {
-                        const int b = h * 2 + bb;
-                        const uint32_t buf = stg + (uint32_t)(b & 1) * EPI_BLOCK;
-                        if (leader) bulk_wait_read_le1();      // the buffer's last store has read it
-                        __syncwarp();
-                        const uint32_t rowp = buf + (uint32_t)lane * 128;
+                        const uint32_t rowp = stg + (uint32_t)lane * 128;
 #pragma unroll
                         for (int q = 0; q < 8; ++q) {
                             const uint32_t unit = (uint32_t)q ^ (uint32_t)(lane & 7);
-                            sts128(rowp + unit * 16, packed[bb * 32 + q * 4], packed[bb * 32 + q * 4 + 1],
-                                   packed[bb * 32 + q * 4 + 2], packed[bb * 32 + q * 4 + 3]);
+                            sts128(rowp + unit * 16, packed[q * 4], packed[q * 4 + 1], packed[q * 4 + 2],
+                                   packed[q * 4 + 3]);
                         }
                         fence_proxy_async_smem();
                         __syncwarp();
                         if (leader) {
-                            const int x = n_blk * BN + b * 64;
+                            const int x = n_blk * BN + col0 + (c == 3 ? 0 : 64);
                             if (x < args.N && y < args.M)
-                                tma_store_2d(&tma_d, epi_stage + (warp - 2) * EPI_WARP_BYTES + (b & 1) * EPI_BLOCK,
-                                             x, y);
+                                tma_store_2d_hint(&tma_d, epi_stage + ew * EPI_BLOCK, x, y, out_policy);
                             bulk_commit_group();
                         }
                     }
                 }
             } else {
                 uint32_t acc[32];
-                for (int c = 0; c < BN / 32; ++c) {
+                for (int c = 0; c < BN / 64; ++c) {
                     tmem_ld_32x32b_x32(t_row + c * 32, acc);
                     tmem_ld_wait();
-                    if (c == BN / 32 - 1) {
+                    if (c == BN / 64 - 1) {
                         tc_fence_before();
                         __syncwarp();
                         if (leader) mbar_arrive_cluster(acc_empty_leader);
                     }
-                    const int64_t col0 = (int64_t)n_blk * BN + c * 32;
-                    if (col0 < args.N) gemm::store_chunk(args, row, col0, acc, alpha);
+                    const int64_t cc = (int64_t)n_blk * BN + col0 + c * 32;
+                    if (cc < args.N) gemm::store_chunk(args, row, cc, acc, alpha);
                 }
             }
         }

@@ -484,6 +484,7 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
     g.K = (int)K;
     g.m_tiles = (int)cdiv(M, gemm::BM);
     g.n_tiles = (int)cdiv(N, gemm::BN);
+    g.n_fastest = M > N ? 1 : 0;               // keep the smaller operand resident in L2
     g.k_blocks = (int)cdiv(K, gemm::BK);
     g.k_steps = (int)cdiv(K, 64);
     g.sf_col_tiles = (int)cdiv(K, 64);
