@@ -46,8 +46,11 @@ WORKLOAD = ("linear-layer training step, 12B-hybrid FFN up-projection: X[8192x51
             "W[20480x5120] dY[8192x20480]; fwd (1x16 RNE X, 16x16 W + W^T), dgrad (1x16 SR dY), "
             "wgrad (RHT-16 along tokens, SR dY^T, RNE X^T); bf16 outputs")
 
-# algorithmic bytes per element (reads + writes) of each quantiser call
-B_AMAX, B_Q1D, B_Q2D_T = 2.0, 2.5625, 3.125
+# algorithmic bytes per element (reads + writes) of each quantiser call: an
+# amax reads 2 B; a 1x16 quantise reads 2 B and writes 0.5 B of codes and
+# 1/16 B of scales; the 16x16 quantise with W^T and the dual-axis quantise
+# read once and write two operands
+B_AMAX, B_Q1D, B_Q2D_T, B_QDUAL = 2.0, 2.5625, 3.125, 3.125
 
 
 def load_peaks():
@@ -57,12 +60,6 @@ def load_peaks():
             d = json.load(f)
         return float(d["hbm_gbs"]), float(d["bf16_tflops"]), "measured"
     return 6400.0, 1800.0, "fallback"
-
-
-def quant_bytes_per_step():
-    x, w, dy = TOKENS * HIDDEN, FFN * HIDDEN, TOKENS * FFN
-    return (x * B_AMAX + x * B_Q1D + w * B_AMAX + w * B_Q2D_T + dy * B_AMAX + dy * B_Q1D +
-            dy * B_AMAX + dy * B_Q1D + x * B_AMAX + x * B_Q1D)
 
 
 # ------------------------------------------------------------------ clocks --
@@ -79,7 +76,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         except OSError:
             self.proc = None
@@ -121,7 +118,7 @@ class ClockSampler:
 class Step:
     """Device buffers and the launch sequence of one linear-layer step."""
 
-    def __init__(self, nv, torch, host):
+    def __init__(self, nv, torch, host, path: str = "dual"):
         self.nv, self.torch = nv, torch
         dev = "cuda"
         self.stream = torch.cuda.current_stream()
@@ -138,9 +135,9 @@ class Step:
         self.dw = torch.empty((FFN, HIDDEN), dtype=torch.bfloat16, device=dev)
         self.mask = nv.nvfp4_rht_mask_from_seed(RHT_SEED)
         self.flush_buf = torch.empty((256 << 20,), dtype=torch.uint8, device=dev)
-        self.n_ev = 26
-        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(self.n_ev)]
-        self.launches_per_step = 13
+        self.seq = self.phases(path)
+        self.ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(self.seq))]
+        self.launches_per_step = len(self.seq)
 
     def h2d(self, host):
         self.x.view(torch_int16(self.torch)).copy_(host["x"], non_blocking=True)
@@ -160,38 +157,58 @@ class Step:
         self.flush_buf.fill_(1)
         self.torch.cuda._sleep(3_000_000)
 
-    def run(self, timed: bool):
-        nv, a, ev = self.nv, self.amax, self.ev
+    def phases(self, path: str):
+        """The launch sequence of one step: (name, call, algorithmic bytes,
+        is_gemm).  "dual": X and dY are each read once for both of their
+        operands (dual-axis amax and quantise); "separate": every operand by
+        its own amax and quantiser call."""
+        nv, a = self.nv, self.amax
         rne, sr = nv.NVFP4_RNE, nv.NVFP4_SR
-        i = 0
+        x, w, dy = TOKENS * HIDDEN, FFN * HIDDEN, TOKENS * FFN
+        fwd_w = [("amax_w", lambda: nv.nvfp4_amax(self.w, 0, a[1:2]), w * B_AMAX, False),
+                 ("q2d_w", lambda: nv.nvfp4_quantize_2d(self.w, a[1:2], rne, 0, 0, self.qw, self.qwt),
+                  w * B_Q2D_T, False)]
+        gemm_fwd = ("gemm_fwd", lambda: nv.nvfp4_gemm(self.qx, self.qw, self.y), 0, True)
+        gemm_dgrad = ("gemm_dgrad", lambda: nv.nvfp4_gemm(self.qdy, self.qwt, self.dx), 0, True)
+        gemm_wgrad = ("gemm_wgrad", lambda: nv.nvfp4_gemm(self.qdyt, self.qxt, self.dw), 0, True)
+        if path == "dual":
+            return [
+                ("amax_dual_x", lambda: nv.nvfp4_amax_dual(self.x, self.mask, a[0:1], a[4:5]), x * B_AMAX, False),
+                ("quant_dual_x", lambda: nv.nvfp4_quantize_dual(self.x, a[0:1], rne, 0, 0, self.qx, self.mask,
+                                                                a[4:5], rne, 0, 0, self.qxt), x * B_QDUAL, False),
+                *fwd_w, gemm_fwd,
+                ("amax_dual_dy", lambda: nv.nvfp4_amax_dual(self.dy, self.mask, a[2:3], a[3:4]), dy * B_AMAX, False),
+                ("quant_dual_dy", lambda: nv.nvfp4_quantize_dual(self.dy, a[2:3], sr, SR_SEED, 1, self.qdy, self.mask,
+                                                                 a[3:4], sr, SR_SEED, 2, self.qdyt), dy * B_QDUAL, False),
+                gemm_dgrad, gemm_wgrad]
+        return [
+            ("amax_x", lambda: nv.nvfp4_amax(self.x, 0, a[0:1]), x * B_AMAX, False),
+            ("q1d_x", lambda: nv.nvfp4_quantize_1d(self.x, a[0:1], rne, 0, 0, self.qx), x * B_Q1D, False),
+            *fwd_w, gemm_fwd,
+            ("amax_dy", lambda: nv.nvfp4_amax(self.dy, 0, a[2:3]), dy * B_AMAX, False),
+            ("q1d_dy_sr", lambda: nv.nvfp4_quantize_1d(self.dy, a[2:3], sr, SR_SEED, 1, self.qdy), dy * B_Q1D, False),
+            gemm_dgrad,
+            # wgrad: k = tokens, both operands read transposed, RHT-16 along k
+            ("amax_rht_dyt", lambda: nv.nvfp4_amax(self.dy, self.mask, a[3:4], transposed=True), dy * B_AMAX, False),
+            ("rhtq_dyt_sr", lambda: nv.nvfp4_rht_quantize(self.dy, self.mask, a[3:4], sr, SR_SEED, 2, self.qdyt,
+                                                          transposed=True), dy * B_Q1D, False),
+            ("amax_rht_xt", lambda: nv.nvfp4_amax(self.x, self.mask, a[4:5], transposed=True), x * B_AMAX, False),
+            ("rhtq_xt", lambda: nv.nvfp4_rht_quantize(self.x, self.mask, a[4:5], rne, 0, 0, self.qxt,
+                                                      transposed=True), x * B_Q1D, False),
+            gemm_wgrad]
 
-        def mark():
-            nonlocal i
+    def run(self, timed: bool):
+        ev = self.ev
+        for j, (_, call, _, _) in enumerate(self.seq):
             if timed:
-                ev[i].record()
-            i += 1
-
-        # forward
-        mark(); nv.nvfp4_amax(self.x, 0, a[0:1]); mark()
-        mark(); nv.nvfp4_quantize_1d(self.x, a[0:1], rne, 0, 0, self.qx); mark()
-        mark(); nv.nvfp4_amax(self.w, 0, a[1:2]); mark()
-        mark(); nv.nvfp4_quantize_2d(self.w, a[1:2], rne, 0, 0, self.qw, self.qwt); mark()
-        mark(); nv.nvfp4_gemm(self.qx, self.qw, self.y); mark()
-        # dgrad
-        mark(); nv.nvfp4_amax(self.dy, 0, a[2:3]); mark()
-        mark(); nv.nvfp4_quantize_1d(self.dy, a[2:3], sr, SR_SEED, 1, self.qdy); mark()
-        mark(); nv.nvfp4_gemm(self.qdy, self.qwt, self.dx); mark()
-        # wgrad: k = tokens, both operands read transposed, RHT-16 along k
-        mark(); nv.nvfp4_amax(self.dy, self.mask, a[3:4], transposed=True); mark()
-        mark(); nv.nvfp4_rht_quantize(self.dy, self.mask, a[3:4], sr, SR_SEED, 2, self.qdyt, transposed=True); mark()
-        mark(); nv.nvfp4_amax(self.x, self.mask, a[4:5], transposed=True); mark()
-        mark(); nv.nvfp4_rht_quantize(self.x, self.mask, a[4:5], rne, 0, 0, self.qxt, transposed=True); mark()
-        mark(); nv.nvfp4_gemm(self.qdyt, self.qxt, self.dw); mark()
-        assert i == self.n_ev
+                ev[2 * j].record()
+            call()
+            if timed:
+                ev[2 * j + 1].record()
 
     def phase_times(self):
-        """ms of each launch (13) of the last timed step."""
-        return [self.ev[2 * j].elapsed_time(self.ev[2 * j + 1]) for j in range(self.n_ev // 2)]
+        """ms of each launch of the last timed step."""
+        return [self.ev[2 * j].elapsed_time(self.ev[2 * j + 1]) for j in range(len(self.seq))]
 
 
 # single calls of the step, for kernel-level profiling (bench.py --profile-case)
@@ -206,10 +223,12 @@ PROFILE_CASES = {
     "rhtq_dyt_sr": lambda s: s.nv.nvfp4_rht_quantize(s.dy, s.mask, s.amax[3:4], s.nv.NVFP4_SR,
                                                       SR_SEED, 2, s.qdyt, transposed=True),
     "amax_rht_dyt": lambda s: s.nv.nvfp4_amax(s.dy, s.mask, s.amax[3:4], transposed=True),
+    "amax_dual_dy": lambda s: s.nv.nvfp4_amax_dual(s.dy, s.mask, s.amax[2:3], s.amax[3:4]),
+    "quant_dual_dy": lambda s: s.nv.nvfp4_quantize_dual(s.dy, s.amax[2:3], s.nv.NVFP4_SR, SR_SEED, 1, s.qdy, s.mask,
+                                                        s.amax[3:4], s.nv.NVFP4_SR, SR_SEED, 2, s.qdyt),
+    "quant_dual_x": lambda s: s.nv.nvfp4_quantize_dual(s.x, s.amax[0:1], s.nv.NVFP4_RNE, 0, 0, s.qx, s.mask,
+                                                       s.amax[4:5], s.nv.NVFP4_RNE, 0, 0, s.qxt),
 }
-
-GEMM_IDX = (4, 7, 12)
-QUANT_IDX = tuple(j for j in range(13) if j not in GEMM_IDX)
 
 
 def torch_int16(torch):
@@ -306,6 +325,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", default="dual", choices=["dual", "separate"],
+                    help="dual: X and dY read once each for both operands; separate: one call per operand")
     ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
                     help="after one full untimed step, launch only this call --steps times "
                          "(a target for ncu -k; prints nothing)")
@@ -331,7 +352,9 @@ def main():
     host["y"] = torch.empty((TOKENS, FFN), dtype=torch.int16).pin_memory()
     host["dx"] = torch.empty((TOKENS, HIDDEN), dtype=torch.int16).pin_memory()
     host["dw"] = torch.empty((FFN, HIDDEN), dtype=torch.int16).pin_memory()
-    step = Step(nv, torch, host)
+    step = Step(nv, torch, host, args.path)
+    gemm_idx = [j for j, p in enumerate(step.seq) if p[3]]
+    quant_idx = [j for j, p in enumerate(step.seq) if not p[3]]
     torch.cuda.synchronize()
     if args.profile_case:
         step.run(timed=False)
@@ -366,8 +389,8 @@ def main():
             torch.cuda.synchronize()
             ph = step.phase_times()
             step_ms.append(step.ev[0].elapsed_time(step.ev[-1]))
-            gemm_ms.extend(ph[j] for j in GEMM_IDX)
-            quant_ms.append(sum(ph[j] for j in QUANT_IDX))
+            gemm_ms.extend(ph[j] for j in gemm_idx)
+            quant_ms.append(sum(ph[j] for j in quant_idx))
         barrier()
     total_ms = sum(step_ms)
     if world > 1:
@@ -405,7 +428,7 @@ def main():
     ms_per_step = total_ms / args.steps
     gemm_avg_ms = statistics.mean(gemm_ms)
     gemm_tflops = GEMM_FLOPS / (gemm_avg_ms * 1e-3) / 1e12
-    qbytes = quant_bytes_per_step()
+    qbytes = sum(step.seq[j][2] for j in quant_idx)
     quant_gbs = qbytes / (statistics.mean(quant_ms) * 1e-3) / 1e9
     traffic = load_traffic()
     out = {
@@ -418,6 +441,7 @@ def main():
         "dtype": "fp4-e2m1 x e4m3-scaled, fp32 accumulate (bf16 in/out)",
         "data": "synthetic (seeded N(0,1)+outliers, N(0,0.02^2), 1e-3*t3)",
         "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
+                   "path": args.path,
                    "l2": "flushed before each step (256 MiB device write, untimed)",
                    "parallelism": f"replicas x{world}"},
         "gemm_tflops": gemm_tflops,
@@ -425,15 +449,15 @@ def main():
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": gemm_tflops / fp4_peak, "traffic": traffic.get("gemm_fwd"),
                      "traffic_note": "forward-GEMM launch (8192x20480x5120); achieved is the mean of the 3 GEMMs",
-                     "kernel": "k_gemm_nvfp4",
+                     "kernel": "k_gemm_nvfp4_2sm",
                      "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s x 6 (nominal dense FP4:BF16)"},
         "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm_peak, "unit": "GB/s",
-                              "frac": quant_gbs / hbm_peak, "traffic": traffic.get("quant_sr_dy"),
-                              "traffic_note": "1x16 SR quantise of dY (one launch)",
+                              "frac": quant_gbs / hbm_peak,
+                              "traffic": traffic.get("quant_dual_dy" if args.path == "dual" else "quant_sr_dy"),
+                              "traffic_note": ("dual-axis SR quantise of dY (one launch)" if args.path == "dual"
+                                               else "1x16 SR quantise of dY (one launch)"),
                               "peak_source": f"{peak_src} HBM copy"},
-        "phase_ms": dict(zip(["amax_x", "q1d_x", "amax_w", "q2d_w", "gemm_fwd", "amax_dy", "q1d_dy_sr",
-                              "gemm_dgrad", "amax_rht_dyt", "rhtq_dyt_sr", "amax_rht_xt", "rhtq_xt",
-                              "gemm_wgrad"], [round(v, 4) for v in step.phase_times()])),
+        "phase_ms": dict(zip([p[0] for p in step.seq], [round(v, 4) for v in step.phase_times()])),
         "e2e": {"value": world * STEP_FLOPS / (e2e_avg * 1e-3) / 1e12, "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d_bytes, "d2h_bytes_per_step": d2h_bytes,
                 "ms_per_step": e2e_avg},

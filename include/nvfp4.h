@@ -148,6 +148,36 @@ nvfp4_status nvfp4_rht_quantize(nvfp4_bf16_view x, uint32_t rht_mask, const floa
                                 nvfp4_round round, uint64_t seed, uint64_t stream_id,
                                 nvfp4_q* out, cudaStream_t stream);
 
+/* Dual-axis amax: one read of a stored tensor S for both GEMM views of it
+ * ([NVB] bullet 3 applies the Hadamard transform to the weight-gradient
+ * inputs only; [SAI] per-tensor scale).  x must be a non-transposed view of
+ * S [rows x cols] with rows % 16 == 0.  Writes
+ *   *amax_dev   = max |S|                       (== nvfp4_amax(x, 0)),
+ *   *amax_t_dev = max |RHT16 along rows of S|   (== nvfp4_amax of the
+ *                 transposed view of S, k = rows, with rht_mask; the plain
+ *                 max |S| when rht_mask == 0),
+ * bit for bit.  The two outputs must be distinct floats.                    */
+nvfp4_status nvfp4_amax_dual(nvfp4_bf16_view x, uint32_t rht_mask, float* amax_dev,
+                             float* amax_t_dev, cudaStream_t stream);
+
+/* Dual-axis 1x16 quantisation: one read of a stored tensor S [rows x cols]
+ * emits both operands a training step takes from it ([NVB] bullets 1-3, 5):
+ *   out   = logical S   [rows x cols], 1x16 blocks along cols, no RHT,
+ *           rounding `round` with (seed, stream_id)          (fprop / dgrad);
+ *   out_t = logical S^T [cols x rows], 1x16 blocks along rows (the tokens),
+ *           RHT-16 with rht_mask_t (none when 0), rounding `round_t` with
+ *           (seed_t, stream_id_t)                             (wgrad).
+ * Each is bit for bit what nvfp4_quantize_1d(x, ...) and
+ * nvfp4_rht_quantize / nvfp4_quantize_1d of the transposed view of S make.
+ * x must be non-transposed with rows % 16 == 0 and cols % 16 == 0.
+ * amax_dev / amax_t_dev: the amaxes of the two operands (nvfp4_amax_dual),
+ * both required (no self-amax form).                                        */
+nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4_round round,
+                                 uint64_t seed, uint64_t stream_id, nvfp4_q* out,
+                                 uint32_t rht_mask_t, const float* amax_t_dev, nvfp4_round round_t,
+                                 uint64_t seed_t, uint64_t stream_id_t, nvfp4_q* out_t,
+                                 cudaStream_t stream);
+
 /* Dequantisation ([SAI] MXFP4 example: value = scale x code; with the global
  * scale divided out).  Writes q as fp32 (out_is_bf16 == 0) or bf16 (RNE) into
  * out[r * ld + c]; ld >= q->k, out 16-byte aligned, ld*elem a multiple of 16. */

@@ -9,8 +9,8 @@ status the C ABI returns.
 The functions carry the C names of ``include/nvfp4.h``:
 
   nvfp4_amax, nvfp4_quantize_1d, nvfp4_quantize_2d, nvfp4_rht_quantize,
-  nvfp4_dequantize, nvfp4_gemm, nvfp4_rht_mask_from_seed, nvfp4_get_status,
-  nvfp4_scale_bytes
+  nvfp4_amax_dual, nvfp4_quantize_dual, nvfp4_dequantize, nvfp4_gemm,
+  nvfp4_rht_mask_from_seed, nvfp4_get_status, nvfp4_scale_bytes
 
 Sources of the method: NVIDIA blog "NVFP4 Trains with Precision of 16-Bit and
 Speed and Efficiency of 4-Bit" (recipe bullets 1-5, Figure 1) and the
@@ -73,6 +73,11 @@ def _load():
     L.nvfp4_rht_quantize.argtypes = [Bf16View, ctypes.c_uint32, vp, ctypes.c_int, u64, u64,
                                      ctypes.POINTER(QStruct), vp]
     L.nvfp4_rht_quantize.restype = st
+    L.nvfp4_amax_dual.argtypes = [Bf16View, ctypes.c_uint32, vp, vp, vp]
+    L.nvfp4_amax_dual.restype = st
+    L.nvfp4_quantize_dual.argtypes = [Bf16View, vp, ctypes.c_int, u64, u64, ctypes.POINTER(QStruct),
+                                      ctypes.c_uint32, vp, ctypes.c_int, u64, u64, ctypes.POINTER(QStruct), vp]
+    L.nvfp4_quantize_dual.restype = st
     L.nvfp4_dequantize.argtypes = [ctypes.POINTER(QStruct), vp, ctypes.c_int, ctypes.c_int64, vp]
     L.nvfp4_dequantize.restype = st
     L.nvfp4_gemm.argtypes = [ctypes.POINTER(QStruct), ctypes.POINTER(QStruct), vp, ctypes.c_int,
@@ -181,6 +186,32 @@ def nvfp4_rht_quantize(x, rht_mask: int, amax: torch.Tensor | None, rnd: int, se
     return _check(lib.nvfp4_rht_quantize(_as_view(x, transposed), rht_mask, _ptr(amax), rnd, seed,
                                          stream_id, ctypes.byref(q), _stream(stream)),
                   "nvfp4_rht_quantize", check)
+
+
+def nvfp4_amax_dual(x, rht_mask: int = 0, amax: torch.Tensor | None = None,
+                    amax_t: torch.Tensor | None = None, *, stream=None, check=True):
+    """Both amaxes of a stored tensor S in one read: (max |S|, max |RHT16 of
+    S^T along its k = S's rows|)."""
+    v = _as_view(x, False)
+    if amax is None:
+        amax = torch.empty((1,), dtype=torch.float32, device="cuda")
+    if amax_t is None:
+        amax_t = torch.empty((1,), dtype=torch.float32, device="cuda")
+    _check(lib.nvfp4_amax_dual(v, rht_mask, amax.data_ptr(), amax_t.data_ptr(), _stream(stream)),
+           "nvfp4_amax_dual", check)
+    return amax, amax_t
+
+
+def nvfp4_quantize_dual(x, amax: torch.Tensor, rnd: int, seed: int, stream_id: int, out: QTensor,
+                        rht_mask_t: int, amax_t: torch.Tensor, rnd_t: int, seed_t: int,
+                        stream_id_t: int, out_t: QTensor, *, stream=None, check=True) -> int:
+    """Row-wise operand S (out) and column-wise operand S^T with optional
+    RHT (out_t) from one read of S."""
+    q, qt = out.c(), out_t.c()
+    return _check(lib.nvfp4_quantize_dual(_as_view(x, False), _ptr(amax), rnd, seed, stream_id,
+                                          ctypes.byref(q), rht_mask_t, _ptr(amax_t), rnd_t, seed_t,
+                                          stream_id_t, ctypes.byref(qt), _stream(stream)),
+                  "nvfp4_quantize_dual", check)
 
 
 def nvfp4_dequantize(q: QTensor, out: torch.Tensor, *, stream=None, check=True) -> int:

@@ -15,6 +15,7 @@
 #include "codec.cuh"
 #include "gemm.cuh"
 #include "gemm2sm.cuh"
+#include "dual.cuh"
 #include "quantize.cuh"
 #include "status.cuh"
 
@@ -99,6 +100,18 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
 }
 
 // -------------------------------------------------------------- quantise ---
+// Philox round keys of the seed; the round-9 pair is complemented (see
+// philox4x32_10_not).
+void set_sr_keys(QuantArgs* a, uint64_t seed) {
+    uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    for (int r = 0; r < 10; ++r) {
+        a->sr_key[2 * r] = r == 9 ? ~k0 : k0;
+        a->sr_key[2 * r + 1] = r == 9 ? ~k1 : k1;
+        k0 += 0x9E3779B9u;
+        k1 += 0xBB67AE85u;
+    }
+}
+
 template <bool RHT, bool SR>
 void launch_q1d(const QuantArgs& a, bool transposed, cudaStream_t st) {
     const int64_t nkb = a.k / 16;
@@ -169,17 +182,7 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.gs_out = out->global_scale;
     a.gs_out2 = out_t ? out_t->global_scale : nullptr;
     a.rht_mask = mask;
-    // Philox round keys of the seed; the round-9 pair is complemented (see
-    // philox4x32_10_not).
-    {
-        uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
-        for (int r = 0; r < 10; ++r) {
-            a.sr_key[2 * r] = r == 9 ? ~k0 : k0;
-            a.sr_key[2 * r + 1] = r == 9 ? ~k1 : k1;
-            k0 += 0x9E3779B9u;
-            k1 += 0xBB67AE85u;
-        }
-    }
+    set_sr_keys(&a, seed);
     a.stream_id = stream_id;
     const bool sr = round == NVFP4_SR;
 
@@ -230,6 +233,39 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     if (sr) launch_q2d<false, true>(a, true, st);
     else launch_q2d<false, false>(a, true, st);
     return launch_status();
+}
+
+// ------------------------------------------------------------------ dual ---
+template <bool SR1, bool SR2, bool RHT2>
+nvfp4_status launch_dual_t(const DualArgs& d, dim3 grid, cudaStream_t st) {
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+    if (!ready[dev].load()) {
+        if (cudaFuncSetAttribute(k_quant_dual<SR1, SR2, RHT2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kDualSmem) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ready[dev].store(1);
+    }
+    k_quant_dual<SR1, SR2, RHT2><<<grid, kQuantThreads, kDualSmem, st>>>(d);
+    return launch_status();
+}
+
+nvfp4_status launch_dual(const DualArgs& d, bool sr1, bool sr2, bool rht2, cudaStream_t st) {
+    const int64_t rows_pad = cdiv(d.row.rows, 128) * 128;
+    const dim3 grid((unsigned)cdiv(d.row.k, kDualCols), (unsigned)(rows_pad / kDualRows));
+    const int sel = (sr1 ? 4 : 0) | (sr2 ? 2 : 0) | (rht2 ? 1 : 0);
+    switch (sel) {
+        case 0: return launch_dual_t<false, false, false>(d, grid, st);
+        case 1: return launch_dual_t<false, false, true>(d, grid, st);
+        case 2: return launch_dual_t<false, true, false>(d, grid, st);
+        case 3: return launch_dual_t<false, true, true>(d, grid, st);
+        case 4: return launch_dual_t<true, false, false>(d, grid, st);
+        case 5: return launch_dual_t<true, false, true>(d, grid, st);
+        case 6: return launch_dual_t<true, true, false>(d, grid, st);
+        default: return launch_dual_t<true, true, true>(d, grid, st);
+    }
 }
 
 // ----------------------------------------------------------- tensor maps ---
@@ -417,6 +453,77 @@ nvfp4_status nvfp4_rht_quantize(nvfp4_bf16_view x, uint32_t rht_mask, const floa
     if (out->block2d != 0 && out->block2d != 1) return NVFP4_ERR_INVALID_ARG;
     return quantize_impl(x, rht_mask, amax_dev, round, seed, stream_id, out, nullptr,
                          out->block2d == 1, stream);
+}
+
+nvfp4_status nvfp4_amax_dual(nvfp4_bf16_view x, uint32_t rht_mask, float* amax_dev,
+                             float* amax_t_dev, cudaStream_t stream) {
+    nvfp4_status s = check_view(x, false);
+    if (s != NVFP4_OK) return s;
+    if (x.transposed != 0 || rht_mask > 0xFFFFu || amax_dev == nullptr || amax_t_dev == nullptr ||
+        amax_dev == amax_t_dev)
+        return NVFP4_ERR_INVALID_ARG;
+    if (x.rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (!aligned(amax_dev, 4) || !aligned(amax_t_dev, 4)) return NVFP4_ERR_MISALIGNED;
+    if (cudaMemsetAsync(amax_dev, 0, sizeof(float), stream) != cudaSuccess ||
+        cudaMemsetAsync(amax_t_dev, 0, sizeof(float), stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (x.rows == 0 || x.cols == 0) return NVFP4_OK;
+    k_amax_dual<<<grid_for(cdiv(x.cols, 2) * (x.rows / 16), kQuantThreads, 3), kQuantThreads, 0, stream>>>(
+        static_cast<const uint16_t*>(x.ptr), x.rows, x.cols, x.ld, rht_mask, amax_dev, amax_t_dev);
+    return launch_status();
+}
+
+nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4_round round,
+                                 uint64_t seed, uint64_t stream_id, nvfp4_q* out,
+                                 uint32_t rht_mask_t, const float* amax_t_dev, nvfp4_round round_t,
+                                 uint64_t seed_t, uint64_t stream_id_t, nvfp4_q* out_t,
+                                 cudaStream_t stream) {
+    nvfp4_status s = check_view(x, true);
+    if (s != NVFP4_OK) return s;
+    if (x.transposed != 0 || rht_mask_t > 0xFFFFu) return NVFP4_ERR_INVALID_ARG;
+    if ((round != NVFP4_RNE && round != NVFP4_SR) || (round_t != NVFP4_RNE && round_t != NVFP4_SR))
+        return NVFP4_ERR_INVALID_ARG;
+    if (x.rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if ((s = check_q(out, x.rows, x.cols)) != NVFP4_OK) return s;
+    if ((s = check_q(out_t, x.cols, x.rows)) != NVFP4_OK) return s;
+    if (amax_dev == nullptr || amax_t_dev == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(amax_dev, 4) || !aligned(amax_t_dev, 4)) return NVFP4_ERR_MISALIGNED;
+    if (amax_dev == out->global_scale || amax_dev == out_t->global_scale ||
+        amax_t_dev == out->global_scale || amax_t_dev == out_t->global_scale ||
+        out->global_scale == out_t->global_scale)
+        return NVFP4_ERR_INVALID_ARG;
+    if (x.rows == 0 || x.cols == 0) {
+        k_publish_senc<<<1, 1, 0, stream>>>(amax_dev, 0, out->global_scale, nullptr);
+        k_publish_senc<<<1, 1, 0, stream>>>(amax_t_dev, 0, out_t->global_scale, nullptr);
+        return launch_status();
+    }
+    DualArgs d{};
+    QuantArgs& a1 = d.row;
+    a1.x = static_cast<const uint16_t*>(x.ptr);
+    a1.ld = x.ld;
+    a1.rows = x.rows;
+    a1.k = x.cols;
+    a1.scale_src = amax_dev;
+    a1.gs_out = out->global_scale;
+    a1.codes = out->codes;
+    a1.scales = out->scales;
+    a1.stream_id = stream_id;
+    a1.write_primary = 1;
+    set_sr_keys(&a1, seed);
+    QuantArgs& a2 = d.col;
+    a2.x = a1.x;
+    a2.ld = x.ld;
+    a2.rows = x.cols;
+    a2.k = x.rows;
+    a2.scale_src = amax_t_dev;
+    a2.gs_out = out_t->global_scale;
+    a2.codes = out_t->codes;
+    a2.scales = out_t->scales;
+    a2.rht_mask = rht_mask_t;
+    a2.stream_id = stream_id_t;
+    a2.write_primary = 1;
+    set_sr_keys(&a2, seed_t);
+    return launch_dual(d, round == NVFP4_SR, round_t == NVFP4_SR, rht_mask_t != 0, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int64_t ld,

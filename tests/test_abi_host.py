@@ -30,6 +30,7 @@ def _declared_functions():
 def test_header_declares_the_path_calls():
     names = _declared_functions()
     for required in ["nvfp4_amax", "nvfp4_quantize_1d", "nvfp4_quantize_2d", "nvfp4_rht_quantize",
+                     "nvfp4_amax_dual", "nvfp4_quantize_dual",
                      "nvfp4_dequantize", "nvfp4_gemm"]:
         assert required in names
 
@@ -102,3 +103,30 @@ def test_validation_rejects_bad_calls(nv):
     assert L.nvfp4_dequantize(ctypes.byref(q), ctypes.c_void_p(0x4004), 0, 64, None) == nv.NVFP4_ERR_MISALIGNED
     # amax: null output
     assert L.nvfp4_amax(good, 0, None, None) == nv.NVFP4_ERR_INVALID_ARG
+
+
+def test_dual_validation_rejects_bad_calls(nv):
+    L = nv.lib
+    good = _view(nv, 0x10000, 32, 64, 64)
+    q, qt = _q(nv, 32, 64), _q(nv, 64, 32, 0x5000, 0x6000, 0x7000)
+    A, AT = ctypes.c_void_p(0x8000), ctypes.c_void_p(0x8004)
+    # amax_dual: transposed view, rows % 16, aliased or null outputs
+    assert L.nvfp4_amax_dual(_view(nv, 0x10000, 32, 64, 32, 1), 0, A, AT, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_amax_dual(_view(nv, 0x10000, 24, 64, 64), 0, A, AT, None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert L.nvfp4_amax_dual(good, 0, A, A, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_amax_dual(good, 0, None, AT, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_amax_dual(good, 0x10000, A, AT, None) == nv.NVFP4_ERR_INVALID_ARG
+    # quantize_dual: shapes of the two outputs, required amaxes, aliasing
+    args = lambda q_, qt_, a_, at_, mask=0, rnd=0: (good, a_, rnd, 0, 0, ctypes.byref(q_), mask, at_, 0, 0, 0,
+                                                    ctypes.byref(qt_), None)
+    assert L.nvfp4_quantize_dual(*args(q, _q(nv, 32, 64, 0x5000, 0x6000, 0x7000), A, AT)) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_dual(*args(q, qt, None, AT)) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_dual(*args(q, qt, A, None)) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_dual(*args(q, qt, ctypes.c_void_p(0x3000), AT)) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_dual(*args(q, _q(nv, 64, 32, 0x5000, 0x6000, 0x3000), A, AT)) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_dual(*args(q, qt, A, AT, mask=0x10000)) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_dual(*args(q, qt, A, AT, rnd=5)) == nv.NVFP4_ERR_INVALID_ARG
+    odd = _view(nv, 0x10000, 24, 64, 64)
+    assert L.nvfp4_quantize_dual(odd, A, 0, 0, 0, ctypes.byref(_q(nv, 24, 64)), 0, AT, 0, 0, 0,
+                                 ctypes.byref(_q(nv, 64, 24, 0x5000, 0x6000, 0x7000)), None) == \
+        nv.NVFP4_ERR_UNSUPPORTED_SHAPE

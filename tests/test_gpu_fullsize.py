@@ -160,3 +160,28 @@ def test_dgrad_gemm(step):
 def test_wgrad_gemm(step):
     s = step
     _gemm_points(s["qdyt"], s["qxt"], FFN, HID, TOK, s["dw"], 9, "dW = dY^T X")
+
+
+def test_dual_axis_path_matches(step, nv):
+    """The dual-axis calls on the full-size X and dY write exactly the bytes
+    of the separate calls above (which are checked against the oracle)."""
+    s = step
+    dx_, ddy = dev_bf16(s["x"]), dev_bf16(s["dy"])
+    Q = nv.QTensor
+    a = torch.zeros((4,), dtype=torch.float32, device="cuda")
+    qx, qxt, qdy, qdyt = Q(TOK, HID), Q(HID, TOK), Q(TOK, FFN), Q(FFN, TOK)
+    nv.nvfp4_amax_dual(dx_, s["mask"], a[0:1], a[1:2])
+    nv.nvfp4_quantize_dual(dx_, a[0:1], nv.NVFP4_RNE, 0, 0, qx, s["mask"], a[1:2], nv.NVFP4_RNE, 0, 0, qxt)
+    nv.nvfp4_amax_dual(ddy, s["mask"], a[2:3], a[3:4])
+    nv.nvfp4_quantize_dual(ddy, a[2:3], nv.NVFP4_SR, SR_SEED, 1, qdy, s["mask"], a[3:4], nv.NVFP4_SR, SR_SEED, 2,
+                           qdyt)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK
+    am = a.cpu().numpy()
+    assert am[0] == s["amax"][0] and am[1] == s["amax"][4]
+    assert am[2] == s["amax"][2] and am[3] == s["amax"][3]
+    for got, key in ((qx, "qx"), (qxt, "qxt"), (qdy, "qdy"), (qdyt, "qdyt")):
+        codes, scales, gs = s[key]
+        assert np.array_equal(got.codes.cpu().numpy(), codes), key
+        assert np.array_equal(got.scales.cpu().numpy(), scales), key
+        assert float(got.global_scale.cpu()[0]) == gs, key
