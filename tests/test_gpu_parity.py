@@ -214,7 +214,10 @@ def _upload_operand(nv, codes, scales_plain, s_enc, rows, k):
 
 
 @pytest.mark.parametrize("M,N,K", [(128, 256, 256), (256, 512, 512), (200, 300, 96), (1, 1, 32),
-                                   (130, 260, 320), (384, 256, 1024), (128, 128, 4160)])
+                                   (130, 260, 320), (384, 256, 1024), (128, 128, 4160),
+                                   # several CTA-pair units, M- and N-fastest tile walks
+                                   (512, 512, 512), (500, 300, 96), (1024, 768, 1280), (2048, 256, 512),
+                                   (512, 4096, 256)])
 @pytest.mark.parametrize("bf16", [False, True])
 def test_gemm_random_operands(nv, M, N, K, bf16):
     ca, sa = synth.random_operand(M, K, M + 7 * K)
@@ -249,11 +252,12 @@ def test_gemm_integer_exact(nv):
     np.testing.assert_array_equal(d.cpu().numpy(), ref.astype(np.float32))
 
 
-def test_gemm_scale_rows_are_distinct(nv):
+@pytest.mark.parametrize("M", [256, 512, 1024])
+def test_gemm_scale_rows_are_distinct(nv, M):
     """Each row of A and of B gets its own scale (power of two by row): a
     wrong scale layout in shared or tensor memory shows up as a wrong row or
-    column of D."""
-    M, N, K = 256, 256, 256
+    column of D (M = 512, 1024: several CTA pairs)."""
+    N, K = 256, 256
     rng = np.random.default_rng(6)
     ca = np.full((M, K // 2), 0x22, np.uint8)                 # all elements 1.0
     cb = np.full((N, K // 2), 0x22, np.uint8)
