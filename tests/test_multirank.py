@@ -39,9 +39,7 @@ def _worker(rank, world, port, out_dir):
     shard = np.ascontiguousarray(x[rank * rows:(rank + 1) * rows])
     local = torch.tensor([oracle.amax(shard)], dtype=torch.float32)
     dist.all_reduce(local, op=dist.ReduceOp.MAX)
-    q = oracle.quantize(shard, amax_v=float(local.item()), sr=True, seed=5, stream_id=9)
-    # element indices of the SR stream are those of the whole tensor: the
-    # shard's rows are offset by rank*rows, so recompute with the global view
+    # the shard's rows, quantised within the whole tensor's index space
     q_global_rows = oracle.quantize(x, amax_v=float(local.item()), sr=False,
                                     rows_range=(rank * rows, (rank + 1) * rows))
     q_rne = oracle.quantize(shard, amax_v=float(local.item()), sr=False)
@@ -53,7 +51,6 @@ def _worker(rank, world, port, out_dir):
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     np.save(os.path.join(out_dir, f"tmax{rank}.npy"), t.numpy())
     np.save(os.path.join(out_dir, f"amax{rank}.npy"), local.numpy())
-    del q
     dist.destroy_process_group()
 
 
