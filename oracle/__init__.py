@@ -116,6 +116,28 @@ def lib():
                                         ctypes.c_float, ctypes.c_int64, ctypes.c_int64,
                                         ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
                                         _c_f64p, _c_f64p]
+            L.orc_e8m0_value.restype = ctypes.c_double
+            L.orc_e8m0_value.argtypes = [ctypes.c_uint8]
+            L.orc_mx_scale_code.restype = ctypes.c_uint8
+            L.orc_mx_scale_code.argtypes = [ctypes.c_float]
+            L.orc_mx_quantize.restype = ctypes.c_int
+            L.orc_mx_quantize.argtypes = [_c_u16p, ctypes.c_int64, ctypes.c_int64, ctypes.c_int64,
+                                          ctypes.c_int, ctypes.c_uint32, ctypes.c_int64, ctypes.c_int64,
+                                          _c_u8p, _c_u8p]
+            L.orc_mx_scale_bytes.restype = ctypes.c_size_t
+            L.orc_mx_scale_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+            L.orc_mx_swizzle_scales.restype = None
+            L.orc_mx_swizzle_scales.argtypes = [_c_u8p, ctypes.c_int64, ctypes.c_int64, _c_u8p]
+            L.orc_mx_unswizzle_scales.restype = None
+            L.orc_mx_unswizzle_scales.argtypes = [_c_u8p, ctypes.c_int64, ctypes.c_int64, _c_u8p]
+            L.orc_mx_dequantize.restype = None
+            L.orc_mx_dequantize.argtypes = [_c_u8p, _c_u8p, ctypes.c_int64, ctypes.c_int64,
+                                            ctypes.c_int64, ctypes.c_int64, ctypes.POINTER(ctypes.c_float),
+                                            ctypes.c_int64]
+            L.orc_mx_gemm_points.restype = None
+            L.orc_mx_gemm_points.argtypes = [_c_u8p, _c_u8p, _c_u8p, _c_u8p, ctypes.c_int64, ctypes.c_int64,
+                                             ctypes.c_int64, ctypes.c_int64, _c_i64p, _c_i64p, _c_f64p,
+                                             _c_f64p]
             _lib = L
     return _lib
 
@@ -346,3 +368,103 @@ def gemm_full(qa, sa_swz, s_a, qb, sb_swz, s_b, m: int, n: int, k: int,
     with ThreadPoolExecutor(len(chunks)) as ex:
         list(ex.map(run, chunks))
     return y, ab
+
+
+# ------------------------------------------------------------------ MXFP4 --
+# The comparison format of [NVB] bullets 1-2 and [SAI] "MVFP4 and MXFP4":
+# 32-element blocks with one power-of-two (E8M0) scale each, no tensor scale.
+def e8m0_value(code: int) -> float:
+    return float(lib().orc_e8m0_value(code))
+
+
+def mx_scale_code(amax_b: float) -> int:
+    """E8M0 code of a block: X = floor(log2 amax_b) - 2, clamped to
+    [-127, 127]; code X + 127."""
+    return int(lib().orc_mx_scale_code(amax_b))
+
+
+def mx_scale_bytes(rows: int, k: int) -> int:
+    return int(lib().orc_mx_scale_bytes(rows, k))
+
+
+def mx_swizzle_scales(plain: np.ndarray, rows: int, k: int) -> np.ndarray:
+    plain = np.ascontiguousarray(plain, dtype=np.uint8)
+    out = np.zeros(mx_scale_bytes(rows, k), dtype=np.uint8)
+    lib().orc_mx_swizzle_scales(_p(plain, ctypes.c_uint8), rows, k, _p(out, ctypes.c_uint8))
+    return out
+
+
+def mx_unswizzle_scales(swz: np.ndarray, rows: int, k: int) -> np.ndarray:
+    swz = np.ascontiguousarray(swz, dtype=np.uint8)
+    out = np.zeros((rows, k // 32), dtype=np.uint8)
+    lib().orc_mx_unswizzle_scales(_p(swz, ctypes.c_uint8), rows, k, _p(out, ctypes.c_uint8))
+    return out
+
+
+class MxQuantized:
+    """An MXFP4 operand: codes [rows x k/2], plain E8M0 scales [rows x k/32]
+    and the swizzled scale buffer."""
+
+    def __init__(self, codes, scales_plain, rows, k):
+        self.codes, self.scales_plain, self.rows, self.k = codes, scales_plain, rows, k
+        self.scales = mx_swizzle_scales(scales_plain, rows, k)
+
+
+def mx_quantize(x: np.ndarray, *, transposed: bool = False, rht_mask: int = 0,
+                threads: int | None = None) -> MxQuantized:
+    """1x32 MXFP4 quantisation (RNE) of the logical operand of bf16 array x,
+    optionally after RHT16 of every 16-chunk along k."""
+    rows, k, ld = _view_dims(x, transposed)
+    if k % 32:
+        raise ValueError("k must be a multiple of 32")
+    codes = np.zeros((rows, k // 2), dtype=np.uint8)
+    scales = np.zeros((rows, k // 32), dtype=np.uint8)
+    chunks = _row_chunks(rows, threads or default_threads(), 1)
+
+    def run(ch):
+        return lib().orc_mx_quantize(_p(x, ctypes.c_uint16), rows, k, ld, int(transposed), rht_mask,
+                                     ch[0], ch[1], _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
+
+    with ThreadPoolExecutor(len(chunks)) as ex:
+        rcs = list(ex.map(run, chunks))
+    if any(rcs):
+        raise ValueError("non-finite block amax")
+    return MxQuantized(codes, scales, rows, k)
+
+
+def mx_dequantize(q: MxQuantized) -> np.ndarray:
+    out = np.zeros((q.rows, q.k), dtype=np.float32)
+    lib().orc_mx_dequantize(_p(q.codes, ctypes.c_uint8), _p(q.scales, ctypes.c_uint8), q.rows, q.k,
+                            0, q.rows, out.ctypes.data_as(ctypes.POINTER(ctypes.c_float)), q.k)
+    return out
+
+
+def mx_gemm_points(qa, sa_swz, qb, sb_swz, m: int, n: int, k: int, ms, ns, threads: int | None = None):
+    """FP64 reference y[i] = sum_k a[ms[i],k] b[ns[i],k] of MXFP4 operands
+    and the matching sum of |a b|."""
+    ms = np.ascontiguousarray(ms, dtype=np.int64)
+    ns = np.ascontiguousarray(ns, dtype=np.int64)
+    y = np.zeros(len(ms), dtype=np.float64)
+    ab = np.zeros(len(ms), dtype=np.float64)
+    qa, qb = np.ascontiguousarray(qa, dtype=np.uint8), np.ascontiguousarray(qb, dtype=np.uint8)
+    sa_swz, sb_swz = np.ascontiguousarray(sa_swz, dtype=np.uint8), np.ascontiguousarray(sb_swz, dtype=np.uint8)
+    nthr = max(1, min(threads or default_threads(), len(ms)))
+    bounds = np.linspace(0, len(ms), nthr + 1).astype(np.int64)
+
+    def run(i):
+        lo, hi = int(bounds[i]), int(bounds[i + 1])
+        if hi > lo:
+            lib().orc_mx_gemm_points(_p(qa, ctypes.c_uint8), _p(sa_swz, ctypes.c_uint8), _p(qb, ctypes.c_uint8),
+                                     _p(sb_swz, ctypes.c_uint8), m, n, k, hi - lo, _p(ms[lo:hi], ctypes.c_int64),
+                                     _p(ns[lo:hi], ctypes.c_int64), _p(y[lo:hi], ctypes.c_double),
+                                     _p(ab[lo:hi], ctypes.c_double))
+
+    with ThreadPoolExecutor(nthr) as ex:
+        list(ex.map(run, range(nthr)))
+    return y, ab
+
+
+def mx_gemm_full(qa, sa_swz, qb, sb_swz, m: int, n: int, k: int, threads: int | None = None):
+    mm, nn = np.meshgrid(np.arange(m), np.arange(n), indexing="ij")
+    y, ab = mx_gemm_points(qa, sa_swz, qb, sb_swz, m, n, k, mm.ravel(), nn.ravel(), threads)
+    return y.reshape(m, n), ab.reshape(m, n)

@@ -435,3 +435,102 @@ void orc_gemm_full(const uint8_t* qa, const uint8_t* sa_swz, float s_a,
             dot_point(qa, sa_swz, qb, sb_swz, k, m, n, inv_scale, &y[m * n_rows + n],
                       &abs_sum[m * n_rows + n]);
 }
+
+/* ------------------------------------------------------------------------ */
+/* MXFP4: 32-element blocks, power-of-two (E8M0) scales, no tensor scale.    */
+/* ------------------------------------------------------------------------ */
+double orc_e8m0_value(uint8_t code) {
+    if (code == 0xFF) return NAN;
+    return ldexp(1.0, (int)code - 127);
+}
+
+uint8_t orc_mx_scale_code(float amax_b) {
+    int X;
+    if (amax_b == 0.0f) {
+        X = -127;
+    } else {
+        int e;
+        frexp((double)amax_b, &e);        /* amax_b = m 2^e, m in [0.5, 1) */
+        X = (e - 1) - 2;                  /* floor(log2 amax_b) - emax(E2M1) */
+        if (X < -127) X = -127;
+        if (X > 127) X = 127;
+    }
+    return (uint8_t)(X + 127);
+}
+
+int orc_mx_quantize(const uint16_t* x, int64_t rows, int64_t k, int64_t ld, int transposed,
+                    uint32_t rht_mask, int64_t row_begin, int64_t row_end,
+                    uint8_t* codes, uint8_t* scales_plain) {
+    int64_t nb = k / 32;
+    for (int64_t r = row_begin; r < row_end; ++r) {
+        for (int64_t b = 0; b < nb; ++b) {
+            float v[32];
+            load_block16(x, ld, transposed, rht_mask, r, 2 * b, v);
+            load_block16(x, ld, transposed, rht_mask, r, 2 * b + 1, v + 16);
+            float amax_b = 0.0f;
+            for (int j = 0; j < 32; ++j) {
+                if (!isfinite(v[j])) return -1;
+                if (fabsf(v[j]) > amax_b) amax_b = fabsf(v[j]);
+            }
+            uint8_t sc = orc_mx_scale_code(amax_b);
+            scales_plain[r * nb + b] = sc;
+            double inv = ldexp(1.0, -((int)sc - 127));   /* 2^-X */
+            for (int j = 0; j < 32; ++j) {
+                float e = (float)((double)v[j] * inv);    /* exact product, one rounding */
+                put_code(codes, k, r, b * 32 + j, orc_e2m1_rne(e));
+            }
+        }
+    }
+    (void)rows;
+    return 0;
+}
+
+size_t orc_mx_scale_bytes(int64_t rows, int64_t k) {
+    return (size_t)(ceil_div(rows, 128) * ceil_div(k / 32, 4) * 512);
+}
+
+void orc_mx_swizzle_scales(const uint8_t* plain, int64_t rows, int64_t k, uint8_t* swz) {
+    int64_t nb = k / 32, col_tiles = ceil_div(nb, 4);
+    memset(swz, 0, orc_mx_scale_bytes(rows, k));
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < nb; ++c)
+            swz[swz_offset(r, c, col_tiles)] = plain[r * nb + c];
+}
+
+void orc_mx_unswizzle_scales(const uint8_t* swz, int64_t rows, int64_t k, uint8_t* plain) {
+    int64_t nb = k / 32, col_tiles = ceil_div(nb, 4);
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < nb; ++c)
+            plain[r * nb + c] = swz[swz_offset(r, c, col_tiles)];
+}
+
+void orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales_swz, int64_t rows, int64_t k,
+                       int64_t row_begin, int64_t row_end, float* out, int64_t ld) {
+    int64_t col_tiles = ceil_div(k / 32, 4);
+    (void)rows;
+    for (int64_t r = row_begin; r < row_end; ++r)
+        for (int64_t c = 0; c < k; ++c)
+            out[r * ld + c] = (float)(orc_e2m1_value(get_code(codes, k, r, c)) *
+                                      orc_e8m0_value(scales_swz[swz_offset(r, c / 32, col_tiles)]));
+}
+
+void orc_mx_gemm_points(const uint8_t* qa, const uint8_t* sa_swz, const uint8_t* qb,
+                        const uint8_t* sb_swz, int64_t m_rows, int64_t n_rows, int64_t k,
+                        int64_t npts, const int64_t* ms, const int64_t* ns,
+                        double* y, double* abs_sum) {
+    int64_t col_tiles = ceil_div(k / 32, 4);
+    (void)m_rows; (void)n_rows;
+    for (int64_t i = 0; i < npts; ++i) {
+        double acc = 0.0, acc_abs = 0.0;
+        for (int64_t c = 0; c < k; ++c) {
+            double a = orc_e2m1_value(get_code(qa, k, ms[i], c)) *
+                       orc_e8m0_value(sa_swz[swz_offset(ms[i], c / 32, col_tiles)]);
+            double b = orc_e2m1_value(get_code(qb, k, ns[i], c)) *
+                       orc_e8m0_value(sb_swz[swz_offset(ns[i], c / 32, col_tiles)]);
+            acc += a * b;
+            acc_abs += fabs(a * b);
+        }
+        y[i] = acc;
+        abs_sum[i] = acc_abs;
+    }
+}

@@ -115,6 +115,36 @@ void orc_gemm_full(const uint8_t* qa, const uint8_t* sa_swz, float s_a,
                    int64_t m_rows, int64_t n_rows, int64_t k,
                    int64_t m_begin, int64_t m_end, double* y, double* abs_sum);
 
+/* ---- MXFP4: the comparison format ---------------------------------------
+ * [NVB] bullets 1-2 and [SAI] "MVFP4 and MXFP4" / "Core architectural
+ * changes of the MVFP4 format": one shared power-of-two scale (E8M0) per 32
+ * elements, no per-tensor scale.  The reading of the scale rule (the pages
+ * give none): block exponent X = floor(log2(amax_b)) - 2, where 2 is the
+ * E2M1 maximum's exponent (6 = 1.5 * 2^2), clamped to [-127, 127]; amax_b
+ * == 0 gives X = -127.  Elements: v = x * 2^-X, E2M1 RNE with saturation.
+ * Scales are E8M0 codes X + 127; the swizzled layout is the NVFP4 one with
+ * 32-element blocks (512-byte tiles of 128 rows x 4 blocks = 128 k).      */
+double  orc_e8m0_value(uint8_t code);               /* 2^(code - 127); code 255 is NaN */
+uint8_t orc_mx_scale_code(float amax_b);            /* finite amax_b >= 0 */
+/* Quantise logical rows [row_begin, row_end) in 1x32 blocks along k
+ * (k % 32 == 0), RNE; rht_mask != 0 applies RHT16 to every 16-chunk along k
+ * first.  codes [rows x k/2]; scales_plain [rows x k/32] E8M0 codes.
+ * Returns 0, or -1 if a block's amax is not finite.                        */
+int orc_mx_quantize(const uint16_t* x, int64_t rows, int64_t k, int64_t ld, int transposed,
+                    uint32_t rht_mask, int64_t row_begin, int64_t row_end,
+                    uint8_t* codes, uint8_t* scales_plain);
+size_t orc_mx_scale_bytes(int64_t rows, int64_t k);
+void   orc_mx_swizzle_scales(const uint8_t* plain, int64_t rows, int64_t k, uint8_t* swz);
+void   orc_mx_unswizzle_scales(const uint8_t* swz, int64_t rows, int64_t k, uint8_t* plain);
+/* x_hat = q * 2^X (exact) for rows [row_begin, row_end); fp32 [rows x ld]   */
+void   orc_mx_dequantize(const uint8_t* codes, const uint8_t* scales_swz, int64_t rows, int64_t k,
+                         int64_t row_begin, int64_t row_end, float* out, int64_t ld);
+/* FP64 GEMM reference: y = sum_k a b, abs = sum_k |a b|, a = e2m1 * 2^Xa.   */
+void   orc_mx_gemm_points(const uint8_t* qa, const uint8_t* sa_swz, const uint8_t* qb,
+                          const uint8_t* sb_swz, int64_t m_rows, int64_t n_rows, int64_t k,
+                          int64_t npts, const int64_t* ms, const int64_t* ns,
+                          double* y, double* abs_sum);
+
 #ifdef __cplusplus
 }
 #endif

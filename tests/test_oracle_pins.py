@@ -498,3 +498,95 @@ def test_gemm_end_to_end_approximates_bf16_matmul():
     y, _ = oracle.gemm_full(qx.codes, qx.scales, qx.s_enc, qw.codes, qw.scales, qw.s_enc, 128, 256, 256)
     ref = synth.bf16_bits_to_f32(x).astype(np.float64) @ synth.bf16_bits_to_f32(w).astype(np.float64).T
     assert np.linalg.norm(y - ref) / np.linalg.norm(ref) < 0.2
+
+
+# ------------------------------------------------------------------ MXFP4 --
+def test_mx_scale_examples_from_pages(golden_dir):
+    for amax_b, scale in read_golden(os.path.join(golden_dir, "mx_scale_examples.txt")):
+        assert oracle.e8m0_value(oracle.mx_scale_code(float(amax_b))) == float(scale)
+
+
+def test_mx_scale_rule_closed_form():
+    """The block max lands in [4, 8) after scaling by 2^-X, away from the
+    clamps; zero gives the smallest scale."""
+    rng = np.random.default_rng(3)
+    vals = np.concatenate([np.exp2(rng.uniform(-120, 120, 2000)), [1.0, 4.0, 6.0, 7.99, 8.0, 2.0 ** -125]])
+    for a in vals.astype(np.float32):
+        s = oracle.e8m0_value(oracle.mx_scale_code(float(a)))
+        assert 4.0 <= float(a) / s < 8.0, a
+        assert math.log2(s) == math.floor(math.log2(float(a))) - 2
+    assert oracle.mx_scale_code(0.0) == 0
+    assert oracle.mx_scale_code(2.0 ** -126) == 0                # X = -128 clamps to -127
+    assert oracle.mx_scale_code(1e-45) == 0
+    assert oracle.e8m0_value(255) != oracle.e8m0_value(255)      # NaN code
+
+
+def _grid():
+    return np.array([oracle.e2m1_value(c) for c in range(16)])
+
+
+def test_mx_quantize_is_nearest_grid_point_by_brute_force():
+    """Every element dequantises to the E2M1 grid point nearest to x / 2^X
+    (ties to the even code, saturating at 6), times 2^X."""
+    x = synth.normal_bf16((8, 256), 5, 1.0, 0.01, 30.0)
+    q = oracle.mx_quantize(x)
+    xf = synth.bf16_bits_to_f32(x).astype(np.float64)
+    deq = oracle.mx_dequantize(q).astype(np.float64)
+    grid = _grid()
+    for r in range(8):
+        for b in range(256 // 32):
+            blk = xf[r, 32 * b:32 * b + 32]
+            s = 2.0 ** (math.floor(math.log2(np.abs(blk).max())) - 2)
+            for j, v in enumerate(blk / s):
+                d = np.abs(grid - np.clip(v, -6, 6))
+                best = np.flatnonzero(d == d.min())
+                best = [c for c in best if (grid[c] < 0) == (v < 0) or grid[c] == 0] or list(best)
+                code = min(best, key=lambda c: (c & 1, c))          # ties: even code
+                assert deq[r, 32 * b + j] == grid[code] * s, (r, b, j, v)
+
+
+def test_mx_exact_on_grid_values():
+    """A block whose values are grid points times 2^X is represented exactly."""
+    rng = np.random.default_rng(7)
+    grid = _grid()
+    vals = grid[rng.integers(0, 16, (4, 64))] * 2.0 ** 5
+    vals[:, 0] = 6 * 2.0 ** 5                                 # block max -> scale 2^5
+    vals[:, 32] = -4 * 2.0 ** 5
+    x = np.vectorize(lambda f: oracle.f32_to_bf16_rne(float(f)))(vals.astype(np.float32)).astype(np.uint16)
+    q = oracle.mx_quantize(x)
+    assert np.array_equal(oracle.mx_dequantize(q), vals.astype(np.float32))
+
+
+def test_mx_swizzle_roundtrip():
+    rng = np.random.default_rng(8)
+    for rows, k in [(1, 32), (130, 96), (256, 512)]:
+        plain = rng.integers(1, 255, (rows, k // 32)).astype(np.uint8)
+        swz = oracle.mx_swizzle_scales(plain, rows, k)
+        assert swz.size == oracle.mx_scale_bytes(rows, k)
+        assert np.array_equal(oracle.mx_unswizzle_scales(swz, rows, k), plain)
+        assert np.count_nonzero(swz) == plain.size                # padding is zero
+
+
+def test_mx_gemm_integer_special_case_exact():
+    rng = np.random.default_rng(9)
+    M, N, K = 16, 24, 128
+    pick = np.array([0, 2, 10], np.uint8)                       # codes of 0, +1, -1
+    av, bv = rng.integers(0, 3, (M, K)), rng.integers(0, 3, (N, K))
+    pack = lambda v: (pick[v[:, 0::2]] | (pick[v[:, 1::2]] << 4)).astype(np.uint8)
+    one = np.full((M, K // 32), 127, np.uint8)                  # 2^0
+    sa = oracle.mx_swizzle_scales(one, M, K)
+    sb = oracle.mx_swizzle_scales(np.full((N, K // 32), 127, np.uint8), N, K)
+    y, _ = oracle.mx_gemm_full(pack(av), sa, pack(bv), sb, M, N, K)
+    sv = np.array([0, 1, -1])
+    assert np.array_equal(y, (sv[av] @ sv[bv].T).astype(np.float64))
+
+
+def test_mx_gemm_matches_numpy_on_dequantised_operands():
+    a = synth.normal_bf16((32, 256), 10, 1.0, 0.01, 30.0)
+    b = synth.normal_bf16((48, 256), 11, 0.02, 0.0, 1.0)
+    qa, qb = oracle.mx_quantize(a), oracle.mx_quantize(b)
+    y, ab = oracle.mx_gemm_full(qa.codes, qa.scales, qb.codes, qb.scales, 32, 48, 256)
+    da, db = oracle.mx_dequantize(qa).astype(np.float64), oracle.mx_dequantize(qb).astype(np.float64)
+    ref = da @ db.T
+    assert np.allclose(y, ref, rtol=0, atol=1e-12 * np.abs(da) @ np.abs(db).T + 1e-300)
+    assert np.allclose(ab, np.abs(da) @ np.abs(db).T, rtol=1e-12)
