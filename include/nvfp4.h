@@ -193,6 +193,32 @@ nvfp4_status nvfp4_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int6
 nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf16,
                         int64_t ldd, cudaStream_t stream);
 
+/* ---- MXFP4, the comparison format ([NVB] bullets 1-2: 32-element blocks
+ * with power-of-two E8M0 scales; [SAI] "MVFP4 and MXFP4", "Core
+ * architectural changes of the MVFP4 format").  An MXFP4 operand uses
+ * nvfp4_q with: codes as for NVFP4; scales = one E8M0 byte (2^(byte-127))
+ * per (row, 32-column block) in the same 512-byte-tile layout with 32-element
+ * blocks (nvfp4_mx_scale_bytes); global_scale unused (may be NULL); block2d 0.
+ * Scale rule (the pages give none): X = floor(log2(block max)) - 2, clamped
+ * to [-127, 127]; elements x * 2^-X rounded to E2M1 (RNE, saturating).     */
+size_t nvfp4_mx_scale_bytes(int64_t rows, int64_t k);
+
+/* 1x32 MXFP4 quantisation of a non-transposed view, k % 32 == 0, RNE;
+ * rht_mask != 0 first applies RHT-16 to every 16-chunk along k.  A block
+ * holding a NaN or Inf gets scale 0xFF and the call reports
+ * NVFP4_ERR_NONFINITE through nvfp4_get_status.                              */
+nvfp4_status nvfp4_mx_quantize(nvfp4_bf16_view x, uint32_t rht_mask, nvfp4_q* out, cudaStream_t stream);
+
+/* x_hat = q * 2^X (exact), fp32 or bf16 (RNE), like nvfp4_dequantize.      */
+nvfp4_status nvfp4_mx_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int64_t ld,
+                                 cudaStream_t stream);
+
+/* MXFP4 GEMM on the tensor cores (tcgen05.mma kind::mxf4, scale_vec::2X):
+ * D[m, n] = sum_k A[m,k] B[n,k] with FP32 accumulation (no tensor scales).
+ * Same shapes, layouts and rules as nvfp4_gemm (K % 32 == 0).               */
+nvfp4_status nvfp4_mx_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf16, int64_t ldd,
+                           cudaStream_t stream);
+
 /* Host helper: the 16-bit RHT sign mask of a seed = low 16 bits of word 0 of
  * Philox4x32-10(counter = 0, key = seed).                                   */
 uint32_t nvfp4_rht_mask_from_seed(uint64_t seed);

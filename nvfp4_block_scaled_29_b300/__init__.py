@@ -10,6 +10,7 @@ The functions carry the C names of ``include/nvfp4.h``:
 
   nvfp4_amax, nvfp4_quantize_1d, nvfp4_quantize_2d, nvfp4_rht_quantize,
   nvfp4_amax_dual, nvfp4_quantize_dual, nvfp4_dequantize, nvfp4_gemm,
+  nvfp4_mx_quantize, nvfp4_mx_dequantize, nvfp4_mx_gemm, nvfp4_mx_scale_bytes,
   nvfp4_rht_mask_from_seed, nvfp4_get_status, nvfp4_scale_bytes
 
 Sources of the method: NVIDIA blog "NVFP4 Trains with Precision of 16-Bit and
@@ -78,6 +79,15 @@ def _load():
     L.nvfp4_quantize_dual.argtypes = [Bf16View, vp, ctypes.c_int, u64, u64, ctypes.POINTER(QStruct),
                                       ctypes.c_uint32, vp, ctypes.c_int, u64, u64, ctypes.POINTER(QStruct), vp]
     L.nvfp4_quantize_dual.restype = st
+    L.nvfp4_mx_scale_bytes.argtypes = [ctypes.c_int64, ctypes.c_int64]
+    L.nvfp4_mx_scale_bytes.restype = ctypes.c_size_t
+    L.nvfp4_mx_quantize.argtypes = [Bf16View, ctypes.c_uint32, ctypes.POINTER(QStruct), vp]
+    L.nvfp4_mx_quantize.restype = st
+    L.nvfp4_mx_dequantize.argtypes = [ctypes.POINTER(QStruct), vp, ctypes.c_int, ctypes.c_int64, vp]
+    L.nvfp4_mx_dequantize.restype = st
+    L.nvfp4_mx_gemm.argtypes = [ctypes.POINTER(QStruct), ctypes.POINTER(QStruct), vp, ctypes.c_int,
+                                ctypes.c_int64, vp]
+    L.nvfp4_mx_gemm.restype = st
     L.nvfp4_dequantize.argtypes = [ctypes.POINTER(QStruct), vp, ctypes.c_int, ctypes.c_int64, vp]
     L.nvfp4_dequantize.restype = st
     L.nvfp4_gemm.argtypes = [ctypes.POINTER(QStruct), ctypes.POINTER(QStruct), vp, ctypes.c_int,
@@ -146,6 +156,19 @@ class QTensor:
     def c(self) -> QStruct:
         return QStruct(self.codes.data_ptr(), self.scales.data_ptr(), self.global_scale.data_ptr(),
                        self.rows, self.k, int(self.block2d))
+
+
+class MxQTensor:
+    """An MXFP4 operand in device memory: codes [rows, k/2] uint8 and swizzled
+    E8M0 scales (nvfp4_mx_scale_bytes) uint8; no tensor scale."""
+
+    def __init__(self, rows: int, k: int, device="cuda"):
+        self.rows, self.k = rows, k
+        self.codes = torch.empty((rows, k // 2), dtype=torch.uint8, device=device)
+        self.scales = torch.empty((max(1, nvfp4_mx_scale_bytes(rows, k)),), dtype=torch.uint8, device=device)
+
+    def c(self) -> QStruct:
+        return QStruct(self.codes.data_ptr(), self.scales.data_ptr(), None, self.rows, self.k, 0)
 
 
 def _as_view(x, transposed):
@@ -229,6 +252,33 @@ def nvfp4_gemm(a: QTensor, b: QTensor, d: torch.Tensor, *, stream=None, check=Tr
     return _check(lib.nvfp4_gemm(ctypes.byref(qa), ctypes.byref(qb), d.data_ptr(),
                                  int(d.dtype == torch.bfloat16), d.stride(0), _stream(stream)),
                   "nvfp4_gemm", check)
+
+
+def nvfp4_mx_scale_bytes(rows: int, k: int) -> int:
+    return int(lib.nvfp4_mx_scale_bytes(rows, k))
+
+
+def nvfp4_mx_quantize(x, rht_mask: int, out: MxQTensor, *, stream=None, check=True) -> int:
+    q = out.c()
+    return _check(lib.nvfp4_mx_quantize(_as_view(x, False), rht_mask, ctypes.byref(q), _stream(stream)),
+                  "nvfp4_mx_quantize", check)
+
+
+def nvfp4_mx_dequantize(q: MxQTensor, out: torch.Tensor, *, stream=None, check=True) -> int:
+    if out.dtype not in (torch.float32, torch.bfloat16) or out.dim() != 2 or out.stride(1) != 1:
+        raise ValueError("out must be a 2-D float32 or bfloat16 tensor with unit column stride")
+    qs = q.c()
+    return _check(lib.nvfp4_mx_dequantize(ctypes.byref(qs), out.data_ptr(), int(out.dtype == torch.bfloat16),
+                                          out.stride(0), _stream(stream)), "nvfp4_mx_dequantize", check)
+
+
+def nvfp4_mx_gemm(a: MxQTensor, b: MxQTensor, d: torch.Tensor, *, stream=None, check=True) -> int:
+    if d.dtype not in (torch.float32, torch.bfloat16) or d.dim() != 2 or d.stride(1) != 1:
+        raise ValueError("d must be a 2-D float32 or bfloat16 tensor with unit column stride")
+    qa, qb = a.c(), b.c()
+    return _check(lib.nvfp4_mx_gemm(ctypes.byref(qa), ctypes.byref(qb), d.data_ptr(),
+                                    int(d.dtype == torch.bfloat16), d.stride(0), _stream(stream)),
+                  "nvfp4_mx_gemm", check)
 
 
 def nvfp4_rht_mask_from_seed(seed: int) -> int:

@@ -46,9 +46,18 @@ using gemm::BN;
 constexpr int HALF = 128;                               // rows of A and of B per CTA
 constexpr int A_BYTES = HALF * BK / 2;                  // 16 KB
 constexpr int B_BYTES = HALF * BK / 2;                  // 16 KB
-constexpr int SFA_BYTES = (BK / 64) * 512;              // 2 KB
-constexpr int SFB_BYTES = 2 * (BK / 64) * 512;          // 4 KB: both 128-row halves
-constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+// Scale-factor format of a stage: NVFP4 (E4M3, one scale per 16 elements,
+// a 512-byte scale tile per 64 k) or MXFP4 (E8M0, one per 32, a tile per
+// 128 k).  Each stage holds A's tiles and both 128-row halves of B's.
+template <bool MX>
+struct Fmt {
+    static constexpr int SF_TILES = BK / (MX ? 128 : 64);     // scale tiles per stage and 128 rows
+    static constexpr int SFA_BYTES = SF_TILES * 512;
+    static constexpr int SFB_BYTES = 2 * SF_TILES * 512;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES + SFA_BYTES + SFB_BYTES;
+    static constexpr int SF_COLS = 3 * SF_TILES * 4;             // TMEM columns of a stage's scales
+    static_assert(STAGE_BYTES % 1024 == 0, "stage buffers must stay 1024-byte aligned");
+};
 constexpr int STAGES = 5;
 // epilogue staging: per epilogue warp one 32-row x 64-column BF16 block
 // (4 KB, 128-byte swizzle)
@@ -59,17 +68,19 @@ constexpr int EPI_BYTES = EPI_WARPS * EPI_BLOCK;
 constexpr int THREADS = 14 * 32;
 constexpr int TMEM_COLS = gemm::TMEM_COLS;
 constexpr int TMEM_SF_BASE = gemm::TMEM_SF_BASE;
-constexpr int SF_COLS = gemm::SF_COLS_PER_STAGE;
-static_assert(STAGE_BYTES % 1024 == 0, "stage buffers must stay 1024-byte aligned");
-__host__ __device__ constexpr int smem_bytes_for(bool tma_epi) {
-    return STAGES * STAGE_BYTES + (tma_epi ? EPI_BYTES : 0) + gemm::BAR_BYTES + 1024;
+__host__ __device__ constexpr int smem_bytes_for(bool tma_epi, bool mx = false) {
+    return STAGES * (mx ? Fmt<true>::STAGE_BYTES : Fmt<false>::STAGE_BYTES) + (tma_epi ? EPI_BYTES : 0) +
+           gemm::BAR_BYTES + 1024;
 }
 static_assert(smem_bytes_for(true) <= gemm::SMEM_LIMIT, "shared memory budget");
-static_assert(TMEM_SF_BASE + STAGES * SF_COLS <= TMEM_COLS, "TMEM budget");
+static_assert(TMEM_SF_BASE + STAGES * Fmt<false>::SF_COLS <= TMEM_COLS, "TMEM budget");
 
-// kind::mxf4nvf4 instruction descriptor for M = 256 (a CTA pair), N = 256.
-__host__ __device__ constexpr uint32_t make_idesc() {
-    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24);
+// Instruction descriptor for M = 256 (a CTA pair), N = 256, E2M1 A and B,
+// K-major: kind::mxf4nvf4 with UE4M3 scales, or (mx) kind::mxf4 with UE8M0
+// scales (bit 23) and the scale-factor ids of A (bits 29-30) and B (bits 4-5).
+__host__ __device__ constexpr uint32_t make_idesc(bool mx = false, uint32_t sf_id = 0) {
+    return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(256 >> 4) << 24) |
+           (mx ? (1u << 23) | (sf_id << 29) | (sf_id << 4) : 0u);
 }
 
 // Unit u -> (M unit, N block).  The walk keeps the smaller operand resident
@@ -82,7 +93,7 @@ __device__ __forceinline__ int unit_n(int u, int m_units, const Args& a) {
     return a.n_fastest ? u % a.n_tiles : u / m_units;
 }
 
-template <bool TMA_EPI>
+template <bool TMA_EPI, bool MX>
 __global__ void __launch_bounds__(THREADS, 1)
 k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ CUtensorMap tma_b,
                  const __grid_constant__ CUtensorMap tma_d, const __grid_constant__ CUtensorMap tma_sfa,
@@ -94,12 +105,13 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         uint32_t dyn;
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
         const uint32_t pad = (uint32_t)(smem - smem_raw);
-        if (pad + (uint32_t)(smem_bytes_for(TMA_EPI) - 1024) > dyn) {
+        if (pad + (uint32_t)(smem_bytes_for(TMA_EPI, MX) - 1024) > dyn) {
             if (threadIdx.x == 0) record_device_error(NVFP4_DEV_TIMEOUT);
             return;
         }
     }
-    uint8_t* epi_stage = smem + STAGES * STAGE_BYTES;
+    using F = Fmt<MX>;
+    uint8_t* epi_stage = smem + STAGES * F::STAGE_BYTES;
     uint64_t* full_bar = reinterpret_cast<uint64_t*>(epi_stage + (TMA_EPI ? EPI_BYTES : 0));
     uint64_t* sf_full = full_bar + STAGES;         // the stage's scale tiles landed
     uint64_t* sf_bar = sf_full + STAGES;           // leader: scales of both CTAs in TMEM
@@ -162,16 +174,16 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                     break;
                 }
                 if (leader) {
-                    uint8_t* sa = smem + stage * STAGE_BYTES;
+                    uint8_t* sa = smem + stage * F::STAGE_BYTES;
                     uint8_t* sb = sa + A_BYTES;
                     uint8_t* ssfa = sb + B_BYTES;
-                    uint8_t* ssfb = ssfa + SFA_BYTES;
+                    uint8_t* ssfb = ssfa + F::SFA_BYTES;
                     // scale tiles first (3D tensor loads of A's 4 tiles and both of
                     // B's 128-row halves, zero-filled beyond the buffer) on their
                     // own barrier, so the scale warps overlap them with A and B
-                    mbar_arrive_expect_tx(&sf_full[stage], SFA_BYTES + SFB_BYTES);
-                    tma_load_3d(ssfa, &tma_sfa, &sf_full[stage], 0, kb * 4, m_blk);
-                    tma_load_3d(ssfb, &tma_sfb, &sf_full[stage], 0, kb * 4, n_blk * 2);
+                    mbar_arrive_expect_tx(&sf_full[stage], F::SFA_BYTES + F::SFB_BYTES);
+                    tma_load_3d(ssfa, &tma_sfa, &sf_full[stage], 0, kb * F::SF_TILES, m_blk);
+                    tma_load_3d(ssfb, &tma_sfb, &sf_full[stage], 0, kb * F::SF_TILES, n_blk * 2);
                     mbar_arrive_expect_tx(&full_bar[stage], A_BYTES + B_BYTES);
                     tma_load_2d(sa, &tma_a, &full_bar[stage], kb * (BK / 2), m_blk * HALF);
                     tma_load_2d(sb, &tma_b, &full_bar[stage], kb * (BK / 2), n_blk * BN + rank * HALF);
@@ -207,24 +219,32 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                     ok = false;
                     break;
                 }
-                const uint32_t ssfa = smem_addr(smem + stage * STAGE_BYTES + A_BYTES + B_BYTES);
-                const uint32_t ssfb = ssfa + SFA_BYTES;
-                uint32_t r[48];
+                const uint32_t ssfa = smem_addr(smem + stage * F::STAGE_BYTES + A_BYTES + B_BYTES);
+                const uint32_t ssfb = ssfa + F::SFA_BYTES;
+                // TMEM slot of the stage: A's tiles in columns [0, 4T), B's in
+                // [4T, 12T): tile kt, row group g of A at 4kt + g, of B half h at
+                // 4T + 8kt + 4h + g (T = scale tiles per stage)
+                constexpr int T = F::SF_TILES;
+                uint32_t r[F::SF_COLS];
 #pragma unroll
-                for (int ks = 0; ks < 4; ++ks) {
-                    const uint4 a = lds128(ssfa + ks * 512 + lane * 16);
-                    r[ks * 4 + 0] = a.x; r[ks * 4 + 1] = a.y; r[ks * 4 + 2] = a.z; r[ks * 4 + 3] = a.w;
+                for (int kt = 0; kt < T; ++kt) {
+                    const uint4 a = lds128(ssfa + kt * 512 + lane * 16);
+                    r[kt * 4 + 0] = a.x; r[kt * 4 + 1] = a.y; r[kt * 4 + 2] = a.z; r[kt * 4 + 3] = a.w;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        const uint4 b = lds128(ssfb + h * 2048 + ks * 512 + lane * 16);
-                        const int c = 16 + ks * 8 + h * 4;
+                        const uint4 b = lds128(ssfb + h * (T * 512) + kt * 512 + lane * 16);
+                        const int c = 4 * T + kt * 8 + h * 4;
                         r[c + 0] = b.x; r[c + 1] = b.y; r[c + 2] = b.z; r[c + 3] = b.w;
                     }
                 }
-                const uint32_t t = tmem_base + lane_base + TMEM_SF_BASE + stage * SF_COLS;
+                const uint32_t t = tmem_base + lane_base + TMEM_SF_BASE + stage * F::SF_COLS;
                 tmem_st_32x32b_x16(t, r);
-                tmem_st_32x32b_x16(t + 16, r + 16);
-                tmem_st_32x32b_x16(t + 32, r + 32);
+                if (MX) {
+                    tmem_st_32x32b_x8(t + 16, r + 16);
+                } else {
+                    tmem_st_32x32b_x16(t + 16, r + 16);
+                    tmem_st_32x32b_x16(t + 32, r + 32);
+                }
                 tmem_st_wait();
                 tc_fence_before();
                 // this CTA's A and B tiles of the stage must be in place too:
@@ -244,7 +264,8 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
     } else if (warp == 1) {
         // ------------------------------------ MMA issuer (leader CTA) ----
         if (rank == 0) {
-            constexpr uint32_t idesc = make_idesc();
+            constexpr int T = F::SF_TILES;
+            constexpr int KS_PER_TILE = (BK / 64) / T;     // MMAs sharing one scale word
             int stage = 0;
             uint32_t phase = 0;
             bool ok = true;
@@ -262,16 +283,25 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_addr(smem + stage * STAGE_BYTES);
+                    const uint32_t sa = smem_addr(smem + stage * F::STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    const uint32_t t_sf = tmem_base + TMEM_SF_BASE + stage * SF_COLS;
+                    const uint32_t t_sf = tmem_base + TMEM_SF_BASE + stage * F::SF_COLS;
                     const int nks = min(BK / 64, args.k_steps - kb * (BK / 64));
 #pragma unroll
                     for (int ks = 0; ks < BK / 64; ++ks) {
                         const uint64_t adesc = smem_desc(sa + ks * 32, 16, 1024, 2);
                         const uint64_t bdesc = smem_desc(sb + ks * 32, 16, 1024, 2);
-                        tc_mma_nvf4_pair_if(leader & (ks < nks ? 1u : 0u), tmem_base, adesc, bdesc, idesc,
-                                            t_sf + ks * 4, t_sf + 16 + ks * 8, (kb | ks) != 0 ? 1u : 0u);
+                        const int kt = ks / KS_PER_TILE;
+                        const uint32_t pr = leader & (ks < nks ? 1u : 0u), acc = (kb | ks) != 0 ? 1u : 0u;
+                        if (MX) {
+                            // byte pair (ks % 2) * 2 of the tile's scale words
+                            constexpr uint32_t id0 = make_idesc(true, 0), id1 = make_idesc(true, 2);
+                            tc_mma_mxf4_pair_if(pr, tmem_base, adesc, bdesc, (ks % KS_PER_TILE) ? id1 : id0,
+                                                t_sf + kt * 4, t_sf + 4 * T + kt * 8, acc);
+                        } else {
+                            tc_mma_nvf4_pair_if(pr, tmem_base, adesc, bdesc, make_idesc(), t_sf + kt * 4,
+                                                t_sf + 4 * T + kt * 8, acc);
+                        }
                     }
                     issued = true;
                     tc_commit_pair_mc_if(leader, &empty_bar[stage], (uint16_t)0x3);
@@ -300,7 +330,8 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         const int quarter = warp & 3;
         const int col0 = warp >= 10 ? BN / 2 : 0;
         const int ew = warp < 6 ? warp - 2 : warp - 6;
-        const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
+        // MXFP4 has no tensor scales: D is the plain sum of the scaled products
+        const float alpha = MX ? 1.0f : (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
         const uint32_t stg = smem_addr(epi_stage) + (uint32_t)ew * EPI_BLOCK;
         const uint64_t out_policy = l2_policy_evict_first();   // D is written once
         int local = 0;

@@ -16,6 +16,7 @@
 #include "gemm.cuh"
 #include "gemm2sm.cuh"
 #include "dual.cuh"
+#include "mx.cuh"
 #include "quantize.cuh"
 #include "status.cuh"
 
@@ -315,16 +316,18 @@ bool make_out_map(CUtensorMap* m, void* d, int64_t rows, int64_t cols, int64_t l
              CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-// The swizzled scale buffer of a [rows x k] operand as a 3D tensor of u32:
-// [row tiles][512-byte tiles along k][128 words]; box = 4 k tiles (one
-// 256-wide k block) x `box_row_tiles` row tiles.  Out-of-range boxes read 0.
-bool make_scale_map(CUtensorMap* m, const uint8_t* scales, int64_t rows, int64_t k, int box_row_tiles) {
+// The swizzled scale buffer of a [rows x k] operand with `block`-element
+// blocks (16: NVFP4, 32: MXFP4) as a 3D tensor of u32: [row tiles][512-byte
+// tiles along k][128 words]; box = the tiles of one 256-wide k block (4 or 2)
+// x `box_row_tiles` row tiles.  Out-of-range boxes read 0.
+bool make_scale_map(CUtensorMap* m, const uint8_t* scales, int64_t rows, int64_t k, int box_row_tiles,
+                    int block = 16) {
     EncodeTiledFn f = encode_fn();
     if (!f) return false;
-    const int64_t row_tiles = cdiv(rows, 128), col_tiles = cdiv(k / 16, 4);
+    const int64_t row_tiles = cdiv(rows, 128), col_tiles = cdiv(k / block, 4);
     const cuuint64_t dims[3] = {128u, (cuuint64_t)col_tiles, (cuuint64_t)row_tiles};
     const cuuint64_t strides[2] = {512u, (cuuint64_t)(col_tiles * 512)};
-    const cuuint32_t box[3] = {128u, 4u, (cuuint32_t)box_row_tiles};
+    const cuuint32_t box[3] = {128u, (cuuint32_t)(gemm::BK / (4 * block)), (cuuint32_t)box_row_tiles};
     const cuuint32_t estr[3] = {1u, 1u, 1u};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_UINT32, 3, const_cast<uint8_t*>(scales), dims, strides, box, estr,
              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -347,10 +350,14 @@ bool gemm_smem_ready() {
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load()) return true;
     if (!set_gemm_attrs<true>() || !set_gemm_attrs<false>() ||
-        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gemm2::smem_bytes_for(true)) != cudaSuccess ||
-        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             gemm2::smem_bytes_for(false)) != cudaSuccess)
+        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm2::smem_bytes_for(false)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm2::smem_bytes_for(true, true)) != cudaSuccess ||
+        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<false, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             gemm2::smem_bytes_for(false, true)) != cudaSuccess)
         return false;
     done[dev].store(1);
     return true;
@@ -370,13 +377,14 @@ nvfp4_status launch_gemm(const GemmMaps& mp, const gemm::Args& g, cudaStream_t s
     return NVFP4_OK;
 }
 
-// Launch the CTA-pair GEMM (clusters of 2 along M).
-template <bool TMA>
+// Launch the CTA-pair GEMM (clusters of 2 along M); MX selects the MXFP4
+// (E8M0, 32-element blocks) scale format.
+template <bool TMA, bool MX = false>
 nvfp4_status launch_gemm_pair(const GemmMaps& mp, const gemm::Args& g, cudaStream_t stream) {
     const int64_t units = (int64_t)(g.m_tiles / 2) * g.n_tiles;
     cudaLaunchConfig_t cfg = {};
     cfg.blockDim = dim3(gemm2::THREADS);
-    cfg.dynamicSmemBytes = (size_t)gemm2::smem_bytes_for(TMA);
+    cfg.dynamicSmemBytes = (size_t)gemm2::smem_bytes_for(TMA, MX);
     cfg.stream = stream;
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -391,13 +399,13 @@ nvfp4_status launch_gemm_pair(const GemmMaps& mp, const gemm::Args& g, cudaStrea
     int n = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
     if (n <= 0) {
         cfg.gridDim = dim3((unsigned)(device_sm_count() / 2 * 2));
-        if (cudaOccupancyMaxActiveClusters(&n, gemm2::k_gemm_nvfp4_2sm<TMA>, &cfg) != cudaSuccess || n <= 0)
+        if (cudaOccupancyMaxActiveClusters(&n, gemm2::k_gemm_nvfp4_2sm<TMA, MX>, &cfg) != cudaSuccess || n <= 0)
             return NVFP4_ERR_CUDA;
         if (dev >= 0 && dev < kMaxDevices) cache[dev].store(n);
     }
     const int clusters = (int)std::min<int64_t>(n, units);
     cfg.gridDim = dim3((unsigned)(clusters * 2));
-    if (cudaLaunchKernelEx(&cfg, gemm2::k_gemm_nvfp4_2sm<TMA>, mp.a, mp.b, mp.d, mp.sfa, mp.sfb, g) !=
+    if (cudaLaunchKernelEx(&cfg, gemm2::k_gemm_nvfp4_2sm<TMA, MX>, mp.a, mp.b, mp.d, mp.sfa, mp.sfb, g) !=
         cudaSuccess)
         return NVFP4_ERR_CUDA;
     return NVFP4_OK;
@@ -601,6 +609,97 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
         st = d_is_bf16 ? launch_gemm_pair<true>(mp, g, stream) : launch_gemm_pair<false>(mp, g, stream);
     else
         st = d_is_bf16 ? launch_gemm<true>(mp, g, stream) : launch_gemm<false>(mp, g, stream);
+    if (st != NVFP4_OK) return st;
+    return launch_status();
+}
+
+// ----------------------------------------------------------------- MXFP4 ---
+size_t nvfp4_mx_scale_bytes(int64_t rows, int64_t k) {
+    if (rows <= 0 || k <= 0) return 0;
+    return (size_t)(cdiv(rows, 128) * cdiv(k / 32, 4) * 512);
+}
+
+nvfp4_status nvfp4_mx_quantize(nvfp4_bf16_view x, uint32_t rht_mask, nvfp4_q* out, cudaStream_t stream) {
+    nvfp4_status s = check_view(x, true);
+    if (s != NVFP4_OK) return s;
+    if (x.transposed != 0 || rht_mask > 0xFFFFu || out == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (x.cols % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (out->rows != x.rows || out->k != x.cols) return NVFP4_ERR_INVALID_ARG;
+    if (x.rows == 0 || x.cols == 0) return NVFP4_OK;
+    if (out->codes == nullptr || out->scales == nullptr) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(out->codes, 16) || !aligned(out->scales, 16)) return NVFP4_ERR_MISALIGNED;
+    MxArgs a{};
+    a.x = static_cast<const uint16_t*>(x.ptr);
+    a.rows = x.rows;
+    a.k = x.cols;
+    a.ld = x.ld;
+    a.codes = out->codes;
+    a.scales = out->scales;
+    a.rht_mask = rht_mask;
+    const int64_t items = cdiv(x.rows, 128) * 128 * cdiv(x.cols / 32, 4) * 2;
+    const int g = grid_for(items, kQuantThreads, 8);
+    if (rht_mask) k_mx_quant_rows<true><<<g, kQuantThreads, 0, stream>>>(a);
+    else k_mx_quant_rows<false><<<g, kQuantThreads, 0, stream>>>(a);
+    return launch_status();
+}
+
+nvfp4_status nvfp4_mx_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int64_t ld, cudaStream_t stream) {
+    if (q == nullptr || (out_is_bf16 != 0 && out_is_bf16 != 1)) return NVFP4_ERR_INVALID_ARG;
+    if (q->rows < 0 || q->k < 0) return NVFP4_ERR_INVALID_ARG;
+    if (q->k % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (q->rows == 0 || q->k == 0) return NVFP4_OK;
+    if (q->codes == nullptr || q->scales == nullptr || out == nullptr || ld < q->k) return NVFP4_ERR_INVALID_ARG;
+    const int64_t esz = out_is_bf16 ? 2 : 4;
+    if (!aligned(q->codes, 16) || !aligned(out, 16) || (ld * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
+    const int g = grid_for(q->rows * (q->k / 16), kQuantThreads, 8);
+    if (out_is_bf16) k_mx_dequant<true><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->rows, q->k, out, ld);
+    else k_mx_dequant<false><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->rows, q->k, out, ld);
+    return launch_status();
+}
+
+nvfp4_status nvfp4_mx_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf16, int64_t ldd,
+                           cudaStream_t stream) {
+    if (a == nullptr || b == nullptr || (d_is_bf16 != 0 && d_is_bf16 != 1)) return NVFP4_ERR_INVALID_ARG;
+    if (a->rows < 0 || b->rows < 0 || a->k < 0 || a->k != b->k) return NVFP4_ERR_INVALID_ARG;
+    const int64_t M = a->rows, N = b->rows, K = a->k;
+    if (K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0 || N == 0) return NVFP4_OK;
+    for (const nvfp4_q* q : {a, b}) {
+        if (K > 0 && (q->codes == nullptr || q->scales == nullptr)) return NVFP4_ERR_INVALID_ARG;
+        if (!aligned(q->codes, 16) || !aligned(q->scales, 16)) return NVFP4_ERR_MISALIGNED;
+    }
+    const int64_t esz = d_is_bf16 ? 2 : 4;
+    if (d == nullptr || ldd < N) return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(d, 16) || (ldd * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
+    if (K == 0) {
+        return cudaMemset2DAsync(d, ldd * esz, 0, N * esz, M, stream) == cudaSuccess ? NVFP4_OK
+                                                                                      : NVFP4_ERR_CUDA;
+    }
+    GemmMaps mp;
+    std::memset(&mp, 0, sizeof(mp));
+    if (!make_code_map(&mp.a, a->codes, M, K, gemm::BM) || !make_code_map(&mp.b, b->codes, N, K, gemm::BN / 2) ||
+        !make_scale_map(&mp.sfa, a->scales, M, K, 1, 32) || !make_scale_map(&mp.sfb, b->scales, N, K, 2, 32))
+        return NVFP4_ERR_CUDA;
+    if (d_is_bf16 && !make_out_map(&mp.d, d, M, N, ldd)) return NVFP4_ERR_CUDA;
+    if (!gemm_smem_ready()) return NVFP4_ERR_CUDA;
+    gemm::Args g{};
+    g.d = d;
+    g.ldd = ldd;
+    g.d_bf16 = d_is_bf16;
+    g.M = (int)M;
+    g.N = (int)N;
+    g.K = (int)K;
+    // CTA pairs always: an odd last 128-row tile pairs with an empty one,
+    // whose loads read zeros and whose rows are never stored
+    g.m_tiles = (int)(cdiv(cdiv(M, gemm::BM), 2) * 2);
+    g.n_tiles = (int)cdiv(N, gemm::BN);
+    g.n_fastest = M > N ? 1 : 0;
+    g.k_blocks = (int)cdiv(K, gemm::BK);
+    g.k_steps = (int)cdiv(K, 64);
+    g.sf_col_tiles = (int)cdiv(K / 32, 4);
+    g.b_row_tiles = (int)cdiv(N, 128);
+    nvfp4_status st = d_is_bf16 ? launch_gemm_pair<true, true>(mp, g, stream) : launch_gemm_pair<false, true>(mp, g, stream);
     if (st != NVFP4_OK) return st;
     return launch_status();
 }

@@ -359,6 +359,33 @@ __device__ __forceinline__ void tc_mma_nvf4_pair_if(uint32_t pred, uint32_t d_tm
         : "memory");
 }
 
+// MXFP4 pair MMA: E2M1 operands, UE8M0 scales, one scale per 32 elements
+// (two per row per K = 64 MMA; the descriptor's scale-factor ids select the
+// byte pair inside each 32-bit TMEM scale word).
+__device__ __forceinline__ void tc_mma_mxf4_pair_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
+                                                    uint64_t b_desc, uint32_t idesc,
+                                                    uint32_t sfa_tmem, uint32_t sfb_tmem,
+                                                    uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.b32 p, %6, 0;\n\t"
+        "setp.ne.b32 q, %7, 0;\n\t"
+        "@q tcgen05.mma.cta_group::2.kind::mxf4.block_scale.scale_vec::2X"
+        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
+        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate),
+        "r"(pred)
+        : "memory");
+}
+
+// 32 lanes x 32 bit, 8 consecutive columns per thread (warp-collective).
+__device__ __forceinline__ void tmem_st_32x32b_x8(uint32_t taddr, const uint32_t* r) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8};" ::"r"(taddr),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7])
+        : "memory");
+}
+
 // 32 lanes x 32 bit, 16 consecutive columns per thread (warp-collective).
 __device__ __forceinline__ void tmem_st_32x32b_x16(uint32_t taddr, const uint32_t* r) {
     asm volatile(

@@ -130,3 +130,22 @@ def test_dual_validation_rejects_bad_calls(nv):
     assert L.nvfp4_quantize_dual(odd, A, 0, 0, 0, ctypes.byref(_q(nv, 24, 64)), 0, AT, 0, 0, 0,
                                  ctypes.byref(_q(nv, 64, 24, 0x5000, 0x6000, 0x7000)), None) == \
         nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+
+
+def test_mx_helpers_and_validation(nv):
+    for rows, k in [(1, 32), (128, 64), (129, 96), (8192, 5120)]:
+        assert nv.nvfp4_mx_scale_bytes(rows, k) == oracle.mx_scale_bytes(rows, k)
+    L = nv.lib
+    q = nv.QStruct(0x1000, 0x2000, None, 32, 64, 0)
+    good = _view(nv, 0x10000, 32, 64, 64)
+    assert L.nvfp4_mx_quantize(_view(nv, 0x10000, 32, 48, 48), 0, ctypes.byref(nv.QStruct(0x1000, 0x2000, None, 32, 48, 0)),
+                               None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+    assert L.nvfp4_mx_quantize(_view(nv, 0x10000, 32, 64, 32, 1), 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_mx_quantize(good, 0x10000, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_mx_quantize(good, 0, ctypes.byref(nv.QStruct(0x1008, 0x2000, None, 32, 64, 0)), None) == \
+        nv.NVFP4_ERR_MISALIGNED
+    a, b = nv.QStruct(0x1000, 0x2000, None, 128, 96, 0), nv.QStruct(0x3000, 0x4000, None, 256, 64, 0)
+    assert L.nvfp4_mx_gemm(ctypes.byref(a), ctypes.byref(b), 0x5000, 0, 256, None) == nv.NVFP4_ERR_INVALID_ARG
+    a2 = nv.QStruct(0x1000, 0x2000, None, 128, 48, 0)
+    b2 = nv.QStruct(0x3000, 0x4000, None, 256, 48, 0)
+    assert L.nvfp4_mx_gemm(ctypes.byref(a2), ctypes.byref(b2), 0x5000, 0, 256, None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
