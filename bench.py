@@ -325,6 +325,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-mx", action="store_true", help="skip the MXFP4 comparison timing")
     ap.add_argument("--path", default="dual", choices=["dual", "separate"],
                     help="dual: X and dY read once each for both operands; separate: one call per operand")
     ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
@@ -464,6 +465,9 @@ def main():
         "gpu_launches": step.launches_per_step * args.steps,
         "clocks": clk.summary(),
     }
+    if not args.no_mx:
+        out["mxfp4"] = time_mxfp4(nv, torch, step)
+        out["autograd"] = time_autograd(torch, step)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_step_sample(rows=96, pts=2048)
         out["cpu_baseline"].pop("seconds_per_step_extrapolated", None)
@@ -472,6 +476,67 @@ def main():
     if world > 1:
         dist.destroy_process_group()
     return 0
+
+
+def time_autograd(torch, step, reps: int = 10) -> dict:
+    """The same training step through the autograd NVFP4 linear layer
+    (forward + backward of NVFP4LinearFunction at the step's shapes), timed
+    with CUDA events after an L2 flush."""
+    import statistics as st
+    from nvfp4_block_scaled_29_b300.linear import NVFP4LinearFunction
+    x = step.x.detach().clone().requires_grad_(True)
+    w = step.w.detach().clone().requires_grad_(True)
+    dy = step.dy
+
+    def once():
+        y = NVFP4LinearFunction.apply(x, w, SR_SEED, step.mask)
+        y.backward(dy)
+
+    once()
+    ts = []
+    for _ in range(reps):
+        x.grad = None
+        w.grad = None
+        step.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); once(); e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    ms = st.median(ts)
+    return {"ms_per_step": round(ms, 4), "tflops": STEP_FLOPS / (ms * 1e-3) / 1e12}
+
+
+def time_mxfp4(nv, torch, step, reps: int = 10) -> dict:
+    """The MXFP4 comparison path at the step's shapes: 1x32 quantise of X and
+    dY (CUDA events, L2 flushed before each call) and the three GEMMs on
+    MXFP4 operands of the forward, dgrad and wgrad shapes (operands made once,
+    untimed)."""
+    import statistics as st
+    Q = nv.MxQTensor
+    ops = {"x": (step.x, Q(TOKENS, HIDDEN)), "w": (step.w, Q(FFN, HIDDEN)), "dy": (step.dy, Q(TOKENS, FFN)),
+           "wt": (step.w.t().contiguous(), Q(HIDDEN, FFN)), "dyt": (step.dy.t().contiguous(), Q(FFN, TOKENS)),
+           "xt": (step.x.t().contiguous(), Q(HIDDEN, TOKENS))}
+    for t, q in ops.values():
+        nv.nvfp4_mx_quantize(t, 0, q)
+
+    def timed(fn):
+        ts = []
+        for _ in range(reps):
+            step.flush_l2()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(); fn(); e1.record()
+            torch.cuda.synchronize()
+            ts.append(e0.elapsed_time(e1))
+        return st.median(ts)
+
+    q_ms = {n: timed(lambda n=n: nv.nvfp4_mx_quantize(ops[n][0], 0, ops[n][1])) for n in ("x", "dy")}
+    g_ms = [timed(lambda a=a, b=b, d=d: nv.nvfp4_mx_gemm(ops[a][1], ops[b][1], d))
+            for a, b, d in (("x", "w", step.y), ("dy", "wt", step.dx), ("dyt", "xt", step.dw))]
+    qbytes = {"x": TOKENS * HIDDEN, "dy": TOKENS * FFN}
+    return {"gemm_ms": [round(v, 4) for v in g_ms],
+            "gemm_tflops": GEMM_FLOPS / (st.mean(g_ms) * 1e-3) / 1e12,
+            "quantize_ms": {n: round(v, 4) for n, v in q_ms.items()},
+            "quantize_gbs": sum(qbytes[n] * (2 + 0.5 + 1 / 32) for n in q_ms) / (sum(q_ms.values()) * 1e-3) / 1e9}
 
 
 def load_traffic():
