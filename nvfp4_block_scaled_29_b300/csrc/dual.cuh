@@ -249,3 +249,97 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant_dual(const DualArgs 
 }
 
 }  // namespace nvfp4
+
+namespace nvfp4 {
+
+// ============================================ streamed (TMA-fed) amax ======
+// max |S| and (RHT_COLS) max |RHT16 down the columns of S| for a stored bf16
+// array S [srows x scols], streamed through shared memory: persistent CTAs
+// walk 64-row x 256-column tiles (32 KB, loaded by one 2D TMA copy; zeros
+// beyond the array) through a ring of kAmaxStages slots, so that up to
+// kAmaxStages - 1 tiles per CTA are in flight while one is reduced.
+// A tile is 128 column pairs x 4 blocks of 16 rows; each thread reduces two
+// (pair, block) items with conflict-free 4-byte reads (a warp reads 128
+// contiguous bytes of a tile row).
+constexpr int kAmaxTileRows = 64, kAmaxTileCols = 256;
+constexpr int kAmaxTileBytes = kAmaxTileRows * kAmaxTileCols * 2;
+constexpr int kAmaxStages = 3;
+constexpr int kAmaxSmem = kAmaxStages * kAmaxTileBytes + 64;
+
+template <bool RHT_COLS>
+__global__ void __launch_bounds__(kQuantThreads, 2) k_amax_stream(const __grid_constant__ CUtensorMap map,
+                                                                  int64_t srows, int64_t scols, uint32_t mask,
+                                                                  float* out_plain, float* out_t) {
+    extern __shared__ __align__(128) uint8_t amax_smem[];
+    uint64_t* full = reinterpret_cast<uint64_t*>(amax_smem + kAmaxStages * kAmaxTileBytes);
+    __shared__ int abort_flag;
+    const int64_t row_tiles = (srows + kAmaxTileRows - 1) / kAmaxTileRows;
+    const int64_t col_tiles = (scols + kAmaxTileCols - 1) / kAmaxTileCols;
+    const int64_t ntiles = row_tiles * col_tiles;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kAmaxStages; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&map);
+    }
+    __syncthreads();
+    auto issue = [&](int64_t t, int s) {
+        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+        mbar_arrive_expect_tx(&full[s], kAmaxTileBytes);
+        tma_load_2d(amax_smem + s * kAmaxTileBytes, &map, &full[s], (int32_t)(tc * kAmaxTileCols),
+                    (int32_t)(tr * kAmaxTileRows));
+    };
+    if (threadIdx.x == 0)
+        for (int s = 0; s < kAmaxStages; ++s) {
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)s * gridDim.x;
+            if (t < ntiles) issue(t, s);
+        }
+    constexpr uint32_t M = 0x7FFF7FFFu;
+    uint32_t m2 = 0, m = 0;
+    const int pr = threadIdx.x & 127;                 // column pair of the tile
+    const int kb0 = threadIdx.x >> 7;                 // blocks kb0 and kb0 + 2
+    int i = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        const int s = i % kAmaxStages;
+        const uint32_t ph = (uint32_t)(i / kAmaxStages) & 1u;
+        const bool ok = mbar_wait_bounded(&full[s], ph, &abort_flag);
+        __syncthreads();                              // every thread saw the same outcome
+        if (abort_flag || !ok) break;
+        const uint32_t* words = reinterpret_cast<const uint32_t*>(amax_smem + s * kAmaxTileBytes);
+#pragma unroll
+        for (int j = 0; j < 2; ++j) {
+            const int kb = kb0 + 2 * j;
+            uint32_t w[16];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) w[r] = words[(kb * 16 + r) * (kAmaxTileCols / 2) + pr];
+#pragma unroll
+            for (int r = 0; r < 16; ++r) m2 = __vmaxu2(m2, w[r] & M);
+            if (RHT_COLS) {
+                float v[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) v[r] = bf16_lo(w[r]);
+                m = max(m, rht16_absmax_bits_nan(v, mask));
+#pragma unroll
+                for (int r = 0; r < 16; ++r) v[r] = bf16_hi(w[r]);
+                m = max(m, rht16_absmax_bits_nan(v, mask));
+            }
+        }
+        __syncthreads();                              // slot s fully read
+        if (threadIdx.x == 0) {
+            const int64_t tn = t + (int64_t)kAmaxStages * gridDim.x;
+            if (tn < ntiles) issue(tn, s);
+        }
+    }
+    // drain: no copy may still be writing into this CTA's shared memory
+    if (threadIdx.x == 0 && abort_flag) {
+        for (int k = 0; k < kAmaxStages; ++k) {
+            const int ii = i + k;
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)ii * gridDim.x;
+            if (t < ntiles && ii < i + kAmaxStages) mbar_wait_bounded(&full[ii % kAmaxStages], (uint32_t)(ii / kAmaxStages) & 1u, nullptr);
+        }
+    }
+    const uint32_t plain = max(m2 & 0xFFFFu, m2 >> 16) << 16;
+    block_max2_to_global(plain, out_plain, RHT_COLS ? m : plain, out_t);
+}
+
+}  // namespace nvfp4

@@ -74,6 +74,65 @@ nvfp4_status check_q(const nvfp4_q* q, int64_t rows, int64_t k) {
     return NVFP4_OK;
 }
 
+// ----------------------------------------------------------- tensor maps ---
+typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
+                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
+                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
+                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+EncodeTiledFn encode_fn() {
+    static std::atomic<EncodeTiledFn> fn{nullptr};
+    EncodeTiledFn f = fn.load();
+    if (f) return f;
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess || p == nullptr)
+        return nullptr;
+    f = reinterpret_cast<EncodeTiledFn>(p);
+    fn.store(f);
+    return f;
+}
+
+// A stored bf16 array [rows x cols] (leading dimension ld) in the streamed
+// amax's tiles: box 256 columns x 64 rows, no swizzle, zeros beyond.
+bool make_bf16_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+    EncodeTiledFn f = encode_fn();
+    if (!f) return false;
+    const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+    const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
+    const cuuint32_t box[2] = {(cuuint32_t)kAmaxTileCols, (cuuint32_t)kAmaxTileRows};
+    const cuuint32_t estr[2] = {1u, 1u};
+    return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// Streamed amax of a stored array (plain, and with RHT down the columns when
+// mask != 0); out_t may equal out_plain when mask == 0.
+nvfp4_status launch_amax_stream(const void* ptr, int64_t srows, int64_t scols, int64_t ld, uint32_t mask,
+                                float* out_plain, float* out_t, cudaStream_t st) {
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+    if (!ready[dev].load()) {
+        if (cudaFuncSetAttribute(k_amax_stream<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAmaxSmem) !=
+                cudaSuccess ||
+            cudaFuncSetAttribute(k_amax_stream<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, kAmaxSmem) !=
+                cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ready[dev].store(1);
+    }
+    CUtensorMap map;
+    if (!make_bf16_tile_map(&map, ptr, srows, scols, ld)) return NVFP4_ERR_CUDA;
+    const int64_t tiles = cdiv(srows, kAmaxTileRows) * cdiv(scols, kAmaxTileCols);
+    const int g = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
+    if (mask) k_amax_stream<true><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, mask, out_plain, out_t);
+    else k_amax_stream<false><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, 0, out_plain, out_t);
+    return launch_status();
+}
+
 // ------------------------------------------------------------------ amax ---
 nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cudaStream_t st) {
     if (cudaMemsetAsync(out, 0, sizeof(float), st) != cudaSuccess) return NVFP4_ERR_CUDA;
@@ -82,14 +141,7 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
     const int64_t srows = x.transposed ? x.cols : x.rows;
     const int64_t scols = x.transposed ? x.rows : x.cols;
     if (mask == 0) {
-        if (x.ld == scols || srows == 1) {
-            const int64_t len = srows * scols;
-            k_amax_plain<<<grid_for(cdiv(len, 64), kQuantThreads, 4), kQuantThreads, 0, st>>>(
-                p, 1, len, x.ld, out);
-        } else {
-            const int g = (int)std::min<int64_t>(srows, (int64_t)device_sm_count() * 8);
-            k_amax_plain<<<g, kQuantThreads, 0, st>>>(p, srows, scols, x.ld, out);
-        }
+        return launch_amax_stream(p, srows, scols, x.ld, 0, out, out, st);
     } else if (!x.transposed) {
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
             p, x.rows, x.cols, x.ld, mask, out);
@@ -267,27 +319,6 @@ nvfp4_status launch_dual(const DualArgs& d, bool sr1, bool sr2, bool rht2, cudaS
         case 6: return launch_dual_t<true, true, false>(d, grid, st);
         default: return launch_dual_t<true, true, true>(d, grid, st);
     }
-}
-
-// ----------------------------------------------------------- tensor maps ---
-typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*,
-                                  const cuuint64_t*, const cuuint64_t*, const cuuint32_t*,
-                                  const cuuint32_t*, CUtensorMapInterleave, CUtensorMapSwizzle,
-                                  CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeTiledFn encode_fn() {
-    static std::atomic<EncodeTiledFn> fn{nullptr};
-    EncodeTiledFn f = fn.load();
-    if (f) return f;
-    void* p = nullptr;
-    cudaDriverEntryPointQueryResult q;
-    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) !=
-            cudaSuccess ||
-        q != cudaDriverEntryPointSuccess || p == nullptr)
-        return nullptr;
-    f = reinterpret_cast<EncodeTiledFn>(p);
-    fn.store(f);
-    return f;
 }
 
 // [rows x k/2] bytes of E2M1 codes, box = 128 bytes x box_rows, 128-byte swizzle.
@@ -476,9 +507,7 @@ nvfp4_status nvfp4_amax_dual(nvfp4_bf16_view x, uint32_t rht_mask, float* amax_d
         cudaMemsetAsync(amax_t_dev, 0, sizeof(float), stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     if (x.rows == 0 || x.cols == 0) return NVFP4_OK;
-    k_amax_dual<<<grid_for(cdiv(x.cols, 2) * (x.rows / 16), kQuantThreads, 3), kQuantThreads, 0, stream>>>(
-        static_cast<const uint16_t*>(x.ptr), x.rows, x.cols, x.ld, rht_mask, amax_dev, amax_t_dev);
-    return launch_status();
+    return launch_amax_stream(x.ptr, x.rows, x.cols, x.ld, rht_mask, amax_dev, amax_t_dev, stream);
 }
 
 nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4_round round,
