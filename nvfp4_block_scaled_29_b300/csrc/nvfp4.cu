@@ -141,7 +141,13 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
     const int64_t srows = x.transposed ? x.cols : x.rows;
     const int64_t scols = x.transposed ? x.rows : x.cols;
     if (mask == 0) {
-        return launch_amax_stream(p, srows, scols, x.ld, 0, out, out, st);
+        if (x.ld == scols || srows == 1) {
+            const int64_t len = srows * scols;
+            k_amax_plain<<<grid_for(cdiv(len, 128), kQuantThreads, 3), kQuantThreads, 0, st>>>(
+                p, 1, len, x.ld, out);
+        } else {
+            return launch_amax_stream(p, srows, scols, x.ld, 0, out, out, st);
+        }
     } else if (!x.transposed) {
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
             p, x.rows, x.cols, x.ld, mask, out);

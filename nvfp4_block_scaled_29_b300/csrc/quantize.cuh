@@ -29,6 +29,15 @@ namespace nvfp4 {
 
 constexpr int kQuantThreads = 256;
 
+// 16-byte streaming load that does not allocate in L1 (data read once).
+__device__ __forceinline__ uint4 ldg_stream_na(const void* p) {
+    uint4 v;
+    asm volatile("ld.global.nc.L1::no_allocate.v4.u32 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+                 : "l"(p));
+    return v;
+}
+
 __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     uint4 v;
     asm volatile("ld.global.nc.v4.u32 {%0, %1, %2, %3}, [%4];"
@@ -163,13 +172,14 @@ __global__ void k_publish_senc(const float* src, int src_is_senc, float* gs_out,
 
 // ============================================================== amax ======
 // max |x| (as bf16 magnitude bits) of a 16-byte aligned span, split over
-// `nt` threads starting at `tid`: 8 independent 16-byte loads in flight per
-// thread, folded with half-word SIMD maxima of the magnitude bit patterns
-// (order-free and NaN-propagating: a NaN pattern exceeds every finite one).
+// `nt` threads starting at `tid`: 16 independent 16-byte loads in flight per
+// thread (HBM needs a few hundred KB in flight per SM), folded with
+// half-word SIMD maxima of the magnitude bit patterns (order-free and
+// NaN-propagating: a NaN pattern exceeds every finite one).
 __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t len, int64_t tid,
                                                 int64_t nt) {
     constexpr uint32_t M = 0x7FFF7FFFu;
-    constexpr int U = 8;
+    constexpr int U = 16;
     uint32_t m2 = 0, m1 = 0;
     const int64_t nch = len >> 3;
     const uint4* v = reinterpret_cast<const uint4*>(base);
@@ -177,13 +187,13 @@ __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t le
     for (; i + (U - 1) * nt < nch; i += U * nt) {
         uint4 c[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) c[u] = ldg_stream(v + i + u * nt);
+        for (int u = 0; u < U; ++u) c[u] = ldg_stream_na(v + i + u * nt);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(c[u].x & M, c[u].y & M), __vmaxu2(c[u].z & M, c[u].w & M)));
     }
     for (; i < nch; i += nt) {
-        const uint4 a = ldg_stream(v + i);
+        const uint4 a = ldg_stream_na(v + i);
         m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M)));
     }
     for (int64_t j = (nch << 3) + tid; j < len; j += nt) m1 = max(m1, (uint32_t)(base[j] & 0x7FFFu));
@@ -193,7 +203,7 @@ __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t le
 // max |x| of a bf16 array of nrows rows of len elements (leading dimension
 // ld).  One row (contiguous data): the whole grid strides over it; several
 // rows: CTAs stride over rows, threads over a row.
-__global__ void __launch_bounds__(kQuantThreads, 4) k_amax_plain(const uint16_t* __restrict__ p,
+__global__ void __launch_bounds__(kQuantThreads, 3) k_amax_plain(const uint16_t* __restrict__ p,
                                                                  int64_t nrows, int64_t len,
                                                                  int64_t ld, float* out) {
     uint32_t m = 0;
