@@ -159,13 +159,12 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
 }
 
 // -------------------------------------------------------------- quantise ---
-// Philox round keys of the seed; the round-9 pair is complemented (see
-// philox4x32_10_not).
+// Philox round keys of the seed (see philox4x32_10).
 void set_sr_keys(QuantArgs* a, uint64_t seed) {
     uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
     for (int r = 0; r < 10; ++r) {
-        a->sr_key[2 * r] = r == 9 ? ~k0 : k0;
-        a->sr_key[2 * r + 1] = r == 9 ? ~k1 : k1;
+        a->sr_key[2 * r] = k0;
+        a->sr_key[2 * r + 1] = k1;
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }

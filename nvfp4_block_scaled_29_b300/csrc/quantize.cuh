@@ -291,7 +291,7 @@ struct QuantArgs {
     uint8_t* scales;            // swizzled
     uint32_t rht_mask;
     uint64_t stream_id;
-    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10_not)
+    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10)
     // 2D transposed emit (optional)
     uint8_t* codes_t;           // [k x rows/2]
     uint8_t* scales_t;
@@ -344,8 +344,7 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], r_b);
     if (SR) {
-        *code_lo = e2m1x8_sr(v, sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
-        *code_hi = e2m1x8_sr(v + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+        e2m1x16_sr(v, sr_words16(idx0 >> 4, a.stream_id, a.sr_key), code_lo, code_hi);
     } else {
         *code_lo = e2m1x8_rne(v);
         *code_hi = e2m1x8_rne(v + 8);
@@ -584,23 +583,21 @@ __global__ void __launch_bounds__(k2DThreads) k_quant2d(const QuantArgs a) {
                 if (a.idx_transposed) {
                     // index in the transposed logical layout: (r, c) -> c * rows + r;
                     // rows is a multiple of 16, so every element of the strip
-                    // takes the same slice (r & 7) of its own Philox block.
-                    const uint32_t sel = (r & 1) ? SR_SEL_HI : SR_SEL_LO;
-                    const uint32_t wsel = (uint32_t)(r & 7) >> 1;
-                    float gv[16];
+                    // takes the same word ((r % 16) / 4) and element position
+                    // (r % 4) of its own Philox block.
+                    const int wsel = (r >> 2) & 3, pos = r & 3;
 #pragma unroll
                     for (int j = 0; j < 16; ++j) {
                         const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
-                        const uint4 rb = sr_rp8(idx >> 3, a.stream_id, a.sr_key);
+                        const uint4 rb = sr_words16(idx >> 4, a.stream_id, a.sr_key);
                         const uint32_t w = wsel == 0 ? rb.x : wsel == 1 ? rb.y : wsel == 2 ? rb.z : rb.w;
-                        gv[j] = sr_grid_value(v[b][j], w, sel);
+                        const uint32_t q = e2m1_sr_at(v[b][j], w, pos);
+                        if (j < 8) lo |= q << (4 * j);
+                        else hi |= q << (4 * (j - 8));
                     }
-                    lo = e2m1x8_rne(gv);
-                    hi = e2m1x8_rne(gv + 8);
                 } else {
                     const uint64_t idx0 = (uint64_t)(r * a.k + c0);
-                    lo = e2m1x8_sr(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
-                    hi = e2m1x8_sr(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+                    e2m1x16_sr(v[b], sr_words16(idx0 >> 4, a.stream_id, a.sr_key), &lo, &hi);
                 }
             }
             cw[2 * b] = lo;

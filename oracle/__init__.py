@@ -79,6 +79,8 @@ def lib():
             L.orc_philox4x32_10.argtypes = [_c_u32p, _c_u32p, _c_u32p]
             L.orc_rht_mask_from_seed.restype = ctypes.c_uint32
             L.orc_rht_mask_from_seed.argtypes = [ctypes.c_uint64]
+            L.orc_sr_r16_of_word.restype = ctypes.c_uint32
+            L.orc_sr_r16_of_word.argtypes = [ctypes.c_uint32, ctypes.c_int]
             L.orc_sr_bits16.restype = ctypes.c_uint32
             L.orc_sr_bits16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
             L.orc_rht16.restype = None
@@ -160,8 +162,9 @@ def e2m1_rne(v: float) -> int:
     return lib().orc_e2m1_rne(v)
 
 
-def e2m1_sr(v: float, u16: int) -> int:
-    return lib().orc_e2m1_sr(v, u16)
+def e2m1_sr(v: float, r16: int) -> int:
+    """Stochastic E2M1 code of v: up iff floor(frac * 2^16) + r16 >= 2^16."""
+    return lib().orc_e2m1_sr(v, r16)
 
 
 def e4m3_value(code: int) -> float:
@@ -186,6 +189,11 @@ def philox4x32_10(ctr, key):
 
 def rht_mask_from_seed(seed: int) -> int:
     return lib().orc_rht_mask_from_seed(seed)
+
+
+def sr_r16_of_word(w: int, p: int) -> int:
+    """16-bit random integer of element p (0..3) of the 32-bit word w."""
+    return lib().orc_sr_r16_of_word(w, p)
 
 
 def sr_bits16(seed: int, stream_id: int, idx: int) -> int:

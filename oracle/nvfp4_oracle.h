@@ -49,10 +49,13 @@ uint16_t orc_f32_to_bf16_rne(float f);
 /* ---- Philox4x32-10 [PHX] ------------------------------------------------ */
 void     orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 uint32_t orc_rht_mask_from_seed(uint64_t seed);    /* low 16 bits of word 0 of Philox(ctr=0, key=seed) */
-/* 16-bit random slice for element index idx of a quantised operand */
+/* 16-bit random integer of element p (0..3) of a 32-bit random word */
+uint32_t orc_sr_r16_of_word(uint32_t w, int p);
+/* 16-bit random integer for element index idx of a quantised operand */
 uint32_t orc_sr_bits16(uint64_t seed, uint64_t stream_id, uint64_t idx);
-/* stochastic E2M1 rounding of v given its 16 random bits */
-uint8_t  orc_e2m1_sr(float v, uint32_t u16);
+/* stochastic E2M1 rounding of v given its 16-bit random integer:
+ * up iff floor(frac * 2^16) + r16 >= 2^16 */
+uint8_t  orc_e2m1_sr(float v, uint32_t r16);
 
 /* ---- random Hadamard transform, 16 points ------------------------------ */
 void orc_rht16(const float in[16], uint32_t mask, float out[16]);
