@@ -19,6 +19,7 @@
 namespace nvfp4 {
 
 __host__ __device__ __forceinline__ int64_t min64(int64_t a, int64_t b) { return a < b ? a : b; }
+__host__ __device__ __forceinline__ int64_t max64(int64_t a, int64_t b) { return a > b ? a : b; }
 
 // ---------------------------------------------------------------- bf16 ----
 __device__ __forceinline__ float bf16_lo(uint32_t w) { return __uint_as_float(w << 16); }
@@ -156,14 +157,19 @@ __device__ __forceinline__ uint32_t e2m1_sr_at(float v, uint32_t w, int p) {
 // exact scaling by 1/4.  The sign flip is folded into the first butterfly
 // stage as fused multiply-adds by +-1: fma(s_b, b, s_a * a) rounds
 // s_a a + s_b b once, exactly like the separate negate-then-add.
-__device__ __forceinline__ void rht16_first3(float* v, uint32_t mask) {
+// Sign multipliers of the diagonal: s[j] = -1 where bit j of the 16-bit mask
+// is set, else +1.  Passed by value as a kernel parameter, so that the
+// butterflies take them straight from the constant bank.
+struct RhtSigns {
+    float s[16];
+};
+
+__device__ __forceinline__ void rht16_first3(float* v, const RhtSigns& sg) {
 #pragma unroll
     for (int i = 0; i < 16; i += 2) {
-        const float sa = ((mask >> i) & 1u) ? -1.0f : 1.0f;
-        const float sb = ((mask >> (i + 1)) & 1u) ? -1.0f : 1.0f;
-        const float a = __fmul_rn(v[i], sa), b = v[i + 1];
-        v[i] = __fmaf_rn(sb, b, a);
-        v[i + 1] = __fmaf_rn(-sb, b, a);
+        const float a = __fmul_rn(v[i], sg.s[i]), b = v[i + 1];
+        v[i] = __fmaf_rn(sg.s[i + 1], b, a);
+        v[i + 1] = __fmaf_rn(-sg.s[i + 1], b, a);
     }
 #pragma unroll
     for (int h = 2; h < 8; h <<= 1) {
@@ -200,8 +206,8 @@ __device__ __forceinline__ void rht16_last(float* v) {
     for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
 }
 
-__device__ __forceinline__ void rht16(float* v, uint32_t mask) {
-    rht16_first3(v, mask);
+__device__ __forceinline__ void rht16(float* v, const RhtSigns& sg) {
+    rht16_first3(v, sg);
     rht16_last(v);
 }
 

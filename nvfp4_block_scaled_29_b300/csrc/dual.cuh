@@ -1,8 +1,6 @@
 // dual.cuh -- dual-axis kernels: one read of a stored bf16 tensor S [R x C]
 // serves both GEMM views of it.
 //
-//  * k_amax_dual: max |S| (the amax of either view) and max |RHT16(S^T)|
-//    (the amax of the column-wise operand, transformed along K = R).
 //  * k_quant_dual: the row-wise 1x16 operand S [R x C] (fprop / dgrad: blocks
 //    along C) and the column-wise 1x16 operand S^T [C x R] (wgrad: blocks
 //    along the tokens R, optionally after the 16-point random Hadamard
@@ -18,8 +16,10 @@
 // rounding of gradients); prism.simon-ai.net article 7890, "Techniques
 // against outliers and rounding error" (RHT along the reduction dimension).
 #pragma once
+#include <cuda.h>
 #include <cstdint>
 #include "codec.cuh"
+#include "ptx.cuh"
 #include "quantize.cuh"
 #include "status.cuh"
 
@@ -48,70 +48,44 @@ __device__ __forceinline__ void block_max2_to_global(uint32_t m0, float* out0, u
     }
 }
 
-// ============================================================ dual amax ====
-// Thread item: 16 stored rows (one K block of the column-wise view) x 2
-// stored columns, 4-byte loads (a warp covers 128 contiguous bytes of a row).
-// The raw words feed the plain maximum (half-word SIMD max of the magnitude
-// bits, NaN-propagating); the two columns are transformed one at a time.
-__global__ void __launch_bounds__(kQuantThreads, 3) k_amax_dual(const uint16_t* __restrict__ p,
-                                                                int64_t srows, int64_t scols, int64_t ld,
-                                                                uint32_t mask, float* out_plain,
-                                                                float* out_t) {
-    constexpr uint32_t M = 0x7FFF7FFFu;
-    uint32_t m = 0, m2 = 0;
-    const int64_t ncp = (scols + 1) >> 1, nkb = srows >> 4;
-    for (ItemWalk it((uint32_t)ncp); it.major < nkb; it.next()) {
-        const int64_t c0 = (int64_t)it.minor * 2;
-        const uint16_t* base = p + it.major * 16 * ld + c0;
-        uint32_t w[16];
-        if (c0 + 2 <= scols) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = ldg_u32(base + t * ld);
-        } else {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = (uint32_t)base[t * ld];
-        }
-#pragma unroll
-        for (int t = 0; t < 16; ++t) m2 = __vmaxu2(m2, w[t] & M);
-        float v[16];
-        if (mask) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
-            m = max(m, rht16_absmax_bits_nan(v, mask));
-#pragma unroll
-            for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
-            m = max(m, rht16_absmax_bits_nan(v, mask));
-        }
-    }
-    const uint32_t plain = max(m2 & 0xFFFFu, m2 >> 16) << 16;
-    block_max2_to_global(plain, out_plain, mask ? m : plain, out_t);
-}
-
 // ======================================================== dual quantise ====
-// CTA tile: 128 stored rows x 256 stored columns (64 KB of bf16), staged in
-// shared memory as 16-byte chunks, chunk q of row r at position
-// q ^ (((q >> 3) & 3) | ((r & 1) << 2)) of its row: the row stores (a warp
-// per row), the row-wise reads (8 rows x 4 column groups per warp, 16-byte
-// reads) and the column-pair reads (32 consecutive words of a row per warp)
-// are all free of bank conflicts.
-constexpr int kDualRows = 128, kDualCols = 256;
-constexpr int kDualChunks = kDualCols / 8;                       // 16-byte chunks per row
-constexpr int kDualSmem = kDualRows * kDualCols * 2;             // 64 KB
-
+// Persistent CTAs walk 64-row x 256-column tiles of S through a ring of
+// kDqStages shared-memory slots, so that up to kDqStages - 1 tiles per CTA
+// are in flight while one is encoded.  A tile arrives as four 64 x 64 boxes
+// (one TMA copy each, 128-byte swizzle: 16-byte chunk c of row r of a box
+// sits at chunk c ^ (r & 7)); rows and columns beyond S read as zeros.
+// Row tiles cover S's 128-padded row count, so that the padding rows' scale
+// words are written too.
+//  * row-wise items (tile row r, group g of 4 blocks = box g): 16-byte reads;
+//    the 8 lanes of a quarter warp read one chunk of 8 consecutive rows,
+//    which the swizzle spreads over all banks;
+//  * column-wise items (column pair, half h of the tile's rows = 2 blocks):
+//    4-byte reads, a warp reading the 128 bytes of one box row.
+// Both item kinds carry 64 elements, one of each per thread.
 struct DualArgs {
     QuantArgs row;      // logical S [R x C]: x, rows = R, k = C, ld; codes/scales of out
-    QuantArgs col;      // logical S^T [C x R]: rows = C, k = R; codes/scales of out_t; rht_mask
+    QuantArgs col;      // logical S^T [C x R]: rows = C, k = R; codes/scales of out_t; rht
 };
 
-__device__ __forceinline__ int dual_chunk(int r, int q) {
-    return r * kDualChunks + (q ^ (((q >> 3) & 3) | ((r & 1) << 2)));
+constexpr int kDqRows = 64, kDqCols = 256, kDqBoxCols = 64;
+constexpr int kDqBoxBytes = kDqRows * kDqBoxCols * 2;            // 8 KB
+constexpr int kDqTileBytes = (kDqCols / kDqBoxCols) * kDqBoxBytes;  // 32 KB
+constexpr int kDqStages = 3;
+constexpr int kDqSmem = kDqStages * kDqTileBytes + 1024 + 64;      // + 1024-byte alignment slack, barriers
+
+// Byte offset of 16-byte chunk c of row r of box b in a tile slot.
+__device__ __forceinline__ uint32_t dq_chunk(int b, int r, int c) {
+    return (uint32_t)(b * kDqBoxBytes + r * 128 + ((c ^ (r & 7)) << 4));
 }
 
 template <bool SR1, bool SR2, bool RHT2>
-__global__ void __launch_bounds__(kQuantThreads, 3) k_quant_dual(const DualArgs d) {
-    extern __shared__ __align__(16) uint8_t dual_smem[];
-    uint4* tile = reinterpret_cast<uint4*>(dual_smem);
+__global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_constant__ CUtensorMap map,
+                                                                 const __grid_constant__ DualArgs d) {
+    extern __shared__ uint8_t dq_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dq_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kDqStages * kDqTileBytes);
     __shared__ float rtab1[128], rtab2[128];
+    __shared__ int abort_flag;
     const QuantArgs& a1 = d.row;
     const QuantArgs& a2 = d.col;
     float s1, s2;
@@ -123,127 +97,162 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant_dual(const DualArgs 
         rtab2[c] = ok2 ? encode_factor(s2, (uint32_t)c) : 0.0f;
     }
     const int64_t R = a1.rows, C = a1.k;
-    const int64_t r0 = (int64_t)blockIdx.y * kDualRows, c0 = (int64_t)blockIdx.x * kDualCols;
-    // ---- stage the tile (zeros beyond the tensor)
-    {
-        const int q = threadIdx.x & 31;
-        const bool col_ok = c0 + q * 8 < C;
-#pragma unroll 4
-        for (int k = 0; k < kDualRows / 8; ++k) {
-            const int r = (threadIdx.x >> 5) + 8 * k;
-            uint4 v = make_uint4(0, 0, 0, 0);
-            if (col_ok && r0 + r < R) v = ldg_stream(a1.x + (r0 + r) * a1.ld + c0 + q * 8);
-            tile[dual_chunk(r, q)] = v;
-        }
+    const int64_t rows_pad = (R + 127) & ~int64_t(127);
+    const int64_t row_tiles = rows_pad / kDqRows;
+    const int64_t col_tiles = (C + kDqCols - 1) / kDqCols;
+    const int64_t ntiles = row_tiles * col_tiles;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kDqStages; ++s) mbar_init(&full[s], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&map);
     }
     __syncthreads();
-
-    // ---- row-wise operand: items (tile row, group of 4 blocks), 2 per thread
-    if (ok1) {
-        const int64_t nkb = C >> 4;
-        const int64_t ngroups = (nkb + 3) >> 2;
-        const int64_t rows_pad = (R + 127) & ~int64_t(127);
-#pragma unroll 1
-        for (int i = threadIdx.x; i < kDualRows * 4; i += blockDim.x) {
-            const int r = i >> 2, g = i & 3;
-            const int64_t rg = r0 + r;
-            const int64_t G = c0 / 64 + g;
-            if (rg >= rows_pad || G >= ngroups) continue;
-            uint32_t* sdst = reinterpret_cast<uint32_t*>(a1.scales + scale_offset(rg, G * 4, ngroups));
-            if (rg >= R) {
-                *sdst = 0u;
-                continue;
-            }
-            const int nblk = (int)min64(4, nkb - G * 4);
-            uint32_t sw = 0, cw[8];
+    auto issue = [&](int64_t t, int s) {
+        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+        mbar_arrive_expect_tx(&full[s], kDqTileBytes);
 #pragma unroll
-            for (int b = 0; b < 4; ++b) {
-                cw[2 * b] = cw[2 * b + 1] = 0u;
-                if (b < nblk) {
-                    const uint4 lo = tile[dual_chunk(r, 8 * g + 2 * b)];
-                    const uint4 hi = tile[dual_chunk(r, 8 * g + 2 * b + 1)];
-                    float v[16];
-                    unpack8(lo, v);
-                    unpack8(hi, v + 8);
-                    uint32_t sb;
-                    encode_block16<false, SR1>(v, s1, rtab1, (uint64_t)(rg * C + G * 64 + b * 16), a1, &sb,
-                                               &cw[2 * b], &cw[2 * b + 1], absmax_bits16_packed(lo, hi));
-                    sw |= sb << (8 * b);
-                }
-            }
-            uint8_t* cdst = a1.codes + rg * (C >> 1) + G * 32;
-            if (nblk == 4 && (C & 31) == 0) {
-                reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-            }
-            *sdst = sw;
+        for (int b = 0; b < kDqCols / kDqBoxCols; ++b)
+            tma_load_2d(ring + s * kDqTileBytes + b * kDqBoxBytes, &map, &full[s],
+                        (int32_t)(tc * kDqCols + b * kDqBoxCols), (int32_t)(tr * kDqRows));
+    };
+    if (threadIdx.x == 0)
+        for (int s = 0; s < kDqStages; ++s) {
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)s * gridDim.x;
+            if (t < ntiles) issue(t, s);
         }
-    }
 
-    // ---- column-wise operand: item (column pair, half of the tile's rows)
-    if (ok2) {
-        const uint32_t* words = reinterpret_cast<const uint32_t*>(tile);
-        const int pr = threadIdx.x & 127, h = threadIdx.x >> 7;
-        const int64_t cc = c0 + 2 * pr;                       // logical rows cc, cc + 1
-        const int64_t nkb = R >> 4;
-        const int64_t ngroups = (nkb + 3) >> 2;
-        const int64_t G = r0 / 64 + h;                        // group of 4 K blocks
-        const int64_t rows_pad = (C + 127) & ~int64_t(127);
-        if (G < ngroups && cc < rows_pad) {
-            uint32_t* s0 = reinterpret_cast<uint32_t*>(a2.scales + scale_offset(cc, G * 4, ngroups));
-            uint32_t* s1p = reinterpret_cast<uint32_t*>(a2.scales + scale_offset(cc + 1, G * 4, ngroups));
-            if (cc >= C) {                                    // C is even: both rows are padding
-                *s0 = 0u;
-                *s1p = 0u;
-            } else {
-                const int nblk = (int)min64(4, nkb - G * 4);
-                uint32_t sw0 = 0, sw1 = 0, c0w[8], c1w[8];
+    // per-thread item coordinates (fixed over tiles)
+    const int ri = threadIdx.x;
+    const int rr = (ri & 7) | ((ri >> 5) << 3);                  // row-wise: tile row 0..63
+    const int rg = (ri >> 3) & 3;                                // row-wise: 64-column group = box
+    const int pc = threadIdx.x & 127;                            // column-wise: column pair
+    const int ch = threadIdx.x >> 7;                             // column-wise: 32-row half
+    const int pb = pc >> 5, pchunk = (pc & 31) >> 2, pword = pc & 3;
+
+    const int64_t nkb = C >> 4, ngroups = (nkb + 3) >> 2;        // row-wise operand
+    const int64_t nkb_t = R >> 4, ngroups_t = (nkb_t + 3) >> 2;  // column-wise operand
+    const int64_t rows_pad_t = (C + 127) & ~int64_t(127);
+
+    int i = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+        const int s = i % kDqStages;
+        const uint32_t ph = (uint32_t)(i / kDqStages) & 1u;
+        const bool ok = mbar_wait_bounded(&full[s], ph, &abort_flag);
+        __syncthreads();                                         // every thread saw the same outcome
+        if (abort_flag || !ok) break;
+        const uint8_t* tile = ring + s * kDqTileBytes;
+        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+        const int64_t r0 = tr * kDqRows, c0 = tc * kDqCols;
+
+        // ---- row-wise operand
+        if (ok1) {
+            const int64_t row = r0 + rr;
+            const int64_t G = c0 / 64 + rg;
+            if (G < ngroups) {
+                uint32_t* sdst = reinterpret_cast<uint32_t*>(a1.scales + scale_offset(row, G * 4, ngroups));
+                if (row >= R) {
+                    *sdst = 0u;
+                } else {
+                    const int nblk = (int)min64(4, nkb - G * 4);
+                    uint32_t sw = 0, cw[8];
 #pragma unroll
-                for (int b = 0; b < 4; ++b) {
-                    c0w[2 * b] = c0w[2 * b + 1] = c1w[2 * b] = c1w[2 * b + 1] = 0u;
-                    if (b < nblk) {
-                        uint32_t w[16];
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) {
-                            const int r = h * 64 + b * 16 + t;
-                            w[t] = words[dual_chunk(r, pr >> 2) * 4 + (pr & 3)];
+                    for (int b = 0; b < 4; ++b) {
+                        cw[2 * b] = cw[2 * b + 1] = 0u;
+                        if (b < nblk) {
+                            const uint4 lo = *reinterpret_cast<const uint4*>(tile + dq_chunk(rg, rr, 2 * b));
+                            const uint4 hi = *reinterpret_cast<const uint4*>(tile + dq_chunk(rg, rr, 2 * b + 1));
+                            float v[16];
+                            unpack8(lo, v);
+                            unpack8(hi, v + 8);
+                            uint32_t sb;
+                            encode_block16<false, SR1>(v, s1, rtab1, (uint64_t)(row * C + G * 64 + b * 16), a1, &sb,
+                                                       &cw[2 * b], &cw[2 * b + 1], absmax_bits16_packed(lo, hi));
+                            sw |= sb << (8 * b);
                         }
-                        const int64_t kc = G * 64 + b * 16;
-                        float v[16];
-                        uint32_t sb;
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
-                        encode_block16<RHT2, SR2>(v, s2, rtab2, (uint64_t)(cc * R + kc), a2, &sb, &c0w[2 * b],
-                                                  &c0w[2 * b + 1]);
-                        sw0 |= sb << (8 * b);
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
-                        encode_block16<RHT2, SR2>(v, s2, rtab2, (uint64_t)((cc + 1) * R + kc), a2, &sb,
-                                                  &c1w[2 * b], &c1w[2 * b + 1]);
-                        sw1 |= sb << (8 * b);
                     }
-                }
-#pragma unroll
-                for (int rr = 0; rr < 2; ++rr) {
-                    const uint32_t* cw = rr ? c1w : c0w;
-                    uint8_t* cdst = a2.codes + (cc + rr) * (R >> 1) + G * 32;
-                    if (nblk == 4 && (R & 31) == 0) {
+                    uint8_t* cdst = a1.codes + row * (C >> 1) + G * 32;
+                    if (nblk == 4 && (C & 31) == 0) {
                         reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
                         reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
                     } else {
 #pragma unroll
                         for (int b = 0; b < 4; ++b)
-                            if (b < nblk)
-                                reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+                            if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
                     }
+                    *sdst = sw;
                 }
-                *s0 = sw0;
-                *s1p = sw1;
             }
+        }
+
+        // ---- column-wise operand: logical rows cc, cc + 1 of S^T, blocks kb0, kb0 + 1
+        if (ok2) {
+            const int64_t cc = c0 + 2 * pc;
+            const int64_t G = r0 / 64;
+            const int64_t kb0 = G * 4 + 2 * ch;
+            if (G < ngroups_t && cc < rows_pad_t) {
+                uint16_t* s0 = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc, kb0, ngroups_t));
+                uint16_t* s1p = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc + 1, kb0, ngroups_t));
+                const int nblk = (int)max64(0, min64(2, nkb_t - kb0));
+                if (cc >= C || nblk == 0) {                      // C is even: both rows are padding
+                    *s0 = 0;
+                    *s1p = 0;
+                } else {
+                    uint32_t sw0 = 0, sw1 = 0, c0w[4], c1w[4];
+#pragma unroll
+                    for (int b = 0; b < 2; ++b) {
+                        c0w[2 * b] = c0w[2 * b + 1] = c1w[2 * b] = c1w[2 * b + 1] = 0u;
+                        if (b < nblk) {
+                            uint32_t w[16];
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) {
+                                const int r = ch * 32 + b * 16 + u;
+                                w[u] = *reinterpret_cast<const uint32_t*>(tile + dq_chunk(pb, r, pchunk) + pword * 4);
+                            }
+                            const int64_t kc = (kb0 + b) * 16;
+                            float v[16];
+                            uint32_t sb;
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) v[u] = bf16_lo(w[u]);
+                            encode_block16<RHT2, SR2>(v, s2, rtab2, (uint64_t)(cc * R + kc), a2, &sb, &c0w[2 * b],
+                                                      &c0w[2 * b + 1]);
+                            sw0 |= sb << (8 * b);
+#pragma unroll
+                            for (int u = 0; u < 16; ++u) v[u] = bf16_hi(w[u]);
+                            encode_block16<RHT2, SR2>(v, s2, rtab2, (uint64_t)((cc + 1) * R + kc), a2, &sb,
+                                                      &c1w[2 * b], &c1w[2 * b + 1]);
+                            sw1 |= sb << (8 * b);
+                        }
+                    }
+#pragma unroll
+                    for (int q = 0; q < 2; ++q) {
+                        const uint32_t* cw = q ? c1w : c0w;
+                        uint8_t* cdst = a2.codes + (cc + q) * (R >> 1) + kb0 * 8;
+                        if (nblk == 2 && (R & 31) == 0) {
+                            *reinterpret_cast<uint4*>(cdst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                        } else {
+#pragma unroll
+                            for (int b = 0; b < 2; ++b)
+                                if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+                        }
+                    }
+                    *s0 = (uint16_t)sw0;
+                    *s1p = (uint16_t)sw1;
+                }
+            }
+        }
+        __syncthreads();                                         // slot s fully read
+        if (threadIdx.x == 0) {
+            const int64_t tn = t + (int64_t)kDqStages * gridDim.x;
+            if (tn < ntiles) issue(tn, s);
+        }
+    }
+    // drain: no copy may still be writing into this CTA's shared memory
+    if (threadIdx.x == 0 && abort_flag) {
+        for (int k = 0; k < kDqStages; ++k) {
+            const int ii = i + k;
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)ii * gridDim.x;
+            if (t < ntiles) mbar_wait_bounded(&full[ii % kDqStages], (uint32_t)(ii / kDqStages) & 1u, nullptr);
         }
     }
 }
@@ -268,7 +277,7 @@ constexpr int kAmaxSmem = kAmaxStages * kAmaxTileBytes + 64;
 
 template <bool RHT_COLS>
 __global__ void __launch_bounds__(kQuantThreads, 2) k_amax_stream(const __grid_constant__ CUtensorMap map,
-                                                                  int64_t srows, int64_t scols, uint32_t mask,
+                                                                  int64_t srows, int64_t scols, const RhtSigns sg,
                                                                   float* out_plain, float* out_t) {
     extern __shared__ __align__(128) uint8_t amax_smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(amax_smem + kAmaxStages * kAmaxTileBytes);
@@ -318,10 +327,10 @@ __global__ void __launch_bounds__(kQuantThreads, 2) k_amax_stream(const __grid_c
                 float v[16];
 #pragma unroll
                 for (int r = 0; r < 16; ++r) v[r] = bf16_lo(w[r]);
-                m = max(m, rht16_absmax_bits_nan(v, mask));
+                m = max(m, rht16_absmax_bits_nan(v, sg));
 #pragma unroll
                 for (int r = 0; r < 16; ++r) v[r] = bf16_hi(w[r]);
-                m = max(m, rht16_absmax_bits_nan(v, mask));
+                m = max(m, rht16_absmax_bits_nan(v, sg));
             }
         }
         __syncthreads();                              // slot s fully read

@@ -29,7 +29,7 @@ struct MxArgs {
     int64_t rows, k, ld;       // logical [rows x k] = stored (non-transposed view)
     uint8_t* codes;            // [rows x k/2]
     uint8_t* scales;           // swizzled E8M0, 32-element blocks
-    uint32_t rht_mask;
+    RhtSigns rht;              // RHT-16 sign multipliers (RHT variant only)
 };
 
 // E8M0 code of a block from its max |value| as float bits; 0xFF (NaN) for a
@@ -91,7 +91,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_mx_quant_rows(const MxArgs
                     uint32_t m = 0;
 #pragma unroll
                     for (int h = 0; h < 2; ++h) {
-                        rht16_first3(v + 16 * h, a.rht_mask);
+                        rht16_first3(v + 16 * h, a.rht);
                         float s[8];
                         rht16_pair_mags(v + 16 * h, s);
 #pragma unroll

@@ -97,16 +97,30 @@ EncodeTiledFn encode_fn() {
 
 // A stored bf16 array [rows x cols] (leading dimension ld) in the streamed
 // amax's tiles: box 256 columns x 64 rows, no swizzle, zeros beyond.
-bool make_bf16_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+// 2D map of a stored bf16 array [rows x cols] (leading dimension ld) with a
+// box of box_rows x box_cols elements.
+bool make_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
+                   uint32_t box_rows, CUtensorMapSwizzle swizzle) {
     EncodeTiledFn f = encode_fn();
     if (!f) return false;
     const cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
     const cuuint64_t strides[1] = {(cuuint64_t)(ld * 2)};
-    const cuuint32_t box[2] = {(cuuint32_t)kAmaxTileCols, (cuuint32_t)kAmaxTileRows};
+    const cuuint32_t box[2] = {box_cols, box_rows};
     const cuuint32_t estr[2] = {1u, 1u};
     return f(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_bf16_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld) {
+    return make_bf16_map(m, ptr, rows, cols, ld, kAmaxTileCols, kAmaxTileRows, CU_TENSOR_MAP_SWIZZLE_NONE);
+}
+
+// RHT-16 sign multipliers of a 16-bit mask (all +1 for mask 0).
+RhtSigns rht_signs(uint32_t mask) {
+    RhtSigns sg;
+    for (int j = 0; j < 16; ++j) sg.s[j] = ((mask >> j) & 1u) ? -1.0f : 1.0f;
+    return sg;
 }
 
 // Streamed amax of a stored array (plain, and with RHT down the columns when
@@ -128,8 +142,9 @@ nvfp4_status launch_amax_stream(const void* ptr, int64_t srows, int64_t scols, i
     if (!make_bf16_tile_map(&map, ptr, srows, scols, ld)) return NVFP4_ERR_CUDA;
     const int64_t tiles = cdiv(srows, kAmaxTileRows) * cdiv(scols, kAmaxTileCols);
     const int g = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
-    if (mask) k_amax_stream<true><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, mask, out_plain, out_t);
-    else k_amax_stream<false><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, 0, out_plain, out_t);
+    const RhtSigns sg = rht_signs(mask);
+    if (mask) k_amax_stream<true><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t);
+    else k_amax_stream<false><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t);
     return launch_status();
 }
 
@@ -150,10 +165,10 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
         }
     } else if (!x.transposed) {
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
-            p, x.rows, x.cols, x.ld, mask, out);
+            p, x.rows, x.cols, x.ld, rht_signs(mask), out);
     } else {
         k_amax_rht_cols<<<grid_for(cdiv(x.rows, 2) * (x.cols / 16), kQuantThreads, 4), kQuantThreads,
-                          0, st>>>(p, x.cols, x.rows, x.ld, mask, out);
+                          0, st>>>(p, x.cols, x.rows, x.ld, rht_signs(mask), out);
     }
     return launch_status();
 }
@@ -239,7 +254,7 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.src_is_senc = src_is_senc;
     a.gs_out = out->global_scale;
     a.gs_out2 = out_t ? out_t->global_scale : nullptr;
-    a.rht_mask = mask;
+    a.rht = rht_signs(mask);
     set_sr_keys(&a, seed);
     a.stream_id = stream_id;
     const bool sr = round == NVFP4_SR;
@@ -295,34 +310,39 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
 
 // ------------------------------------------------------------------ dual ---
 template <bool SR1, bool SR2, bool RHT2>
-nvfp4_status launch_dual_t(const DualArgs& d, dim3 grid, cudaStream_t st) {
+nvfp4_status launch_dual_t(const CUtensorMap& map, const DualArgs& d, int grid, cudaStream_t st) {
     static std::atomic<int> ready[kMaxDevices];
     int dev = 0;
     cudaGetDevice(&dev);
     if (dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
     if (!ready[dev].load()) {
         if (cudaFuncSetAttribute(k_quant_dual<SR1, SR2, RHT2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 kDualSmem) != cudaSuccess)
+                                 kDqSmem) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         ready[dev].store(1);
     }
-    k_quant_dual<SR1, SR2, RHT2><<<grid, kQuantThreads, kDualSmem, st>>>(d);
+    k_quant_dual<SR1, SR2, RHT2><<<grid, kQuantThreads, kDqSmem, st>>>(map, d);
     return launch_status();
 }
 
 nvfp4_status launch_dual(const DualArgs& d, bool sr1, bool sr2, bool rht2, cudaStream_t st) {
+    CUtensorMap map;
+    if (!make_bf16_map(&map, d.row.x, d.row.rows, d.row.k, d.row.ld, kDqBoxCols, kDqRows,
+                       CU_TENSOR_MAP_SWIZZLE_128B))
+        return NVFP4_ERR_CUDA;
     const int64_t rows_pad = cdiv(d.row.rows, 128) * 128;
-    const dim3 grid((unsigned)cdiv(d.row.k, kDualCols), (unsigned)(rows_pad / kDualRows));
+    const int64_t tiles = (rows_pad / kDqRows) * cdiv(d.row.k, kDqCols);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
     const int sel = (sr1 ? 4 : 0) | (sr2 ? 2 : 0) | (rht2 ? 1 : 0);
     switch (sel) {
-        case 0: return launch_dual_t<false, false, false>(d, grid, st);
-        case 1: return launch_dual_t<false, false, true>(d, grid, st);
-        case 2: return launch_dual_t<false, true, false>(d, grid, st);
-        case 3: return launch_dual_t<false, true, true>(d, grid, st);
-        case 4: return launch_dual_t<true, false, false>(d, grid, st);
-        case 5: return launch_dual_t<true, false, true>(d, grid, st);
-        case 6: return launch_dual_t<true, true, false>(d, grid, st);
-        default: return launch_dual_t<true, true, true>(d, grid, st);
+        case 0: return launch_dual_t<false, false, false>(map, d, grid, st);
+        case 1: return launch_dual_t<false, false, true>(map, d, grid, st);
+        case 2: return launch_dual_t<false, true, false>(map, d, grid, st);
+        case 3: return launch_dual_t<false, true, true>(map, d, grid, st);
+        case 4: return launch_dual_t<true, false, false>(map, d, grid, st);
+        case 5: return launch_dual_t<true, false, true>(map, d, grid, st);
+        case 6: return launch_dual_t<true, true, false>(map, d, grid, st);
+        default: return launch_dual_t<true, true, true>(map, d, grid, st);
     }
 }
 
@@ -561,7 +581,7 @@ nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4
     a2.gs_out = out_t->global_scale;
     a2.codes = out_t->codes;
     a2.scales = out_t->scales;
-    a2.rht_mask = rht_mask_t;
+    a2.rht = rht_signs(rht_mask_t);
     a2.stream_id = stream_id_t;
     a2.write_primary = 1;
     set_sr_keys(&a2, seed_t);
@@ -669,7 +689,7 @@ nvfp4_status nvfp4_mx_quantize(nvfp4_bf16_view x, uint32_t rht_mask, nvfp4_q* ou
     a.ld = x.ld;
     a.codes = out->codes;
     a.scales = out->scales;
-    a.rht_mask = rht_mask;
+    a.rht = rht_signs(rht_mask);
     const int64_t items = cdiv(x.rows, 128) * 128 * cdiv(x.cols / 32, 4) * 2;
     const int g = grid_for(items, kQuantThreads, 8);
     if (rht_mask) k_mx_quant_rows<true><<<g, kQuantThreads, 0, stream>>>(a);

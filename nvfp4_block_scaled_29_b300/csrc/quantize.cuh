@@ -127,8 +127,8 @@ __device__ __forceinline__ void block_max_to_global(uint32_t m, float* out) {
 // integer maximum of the non-negative pair magnitudes (see rht16_pair_mags);
 // a non-finite magnitude (where a +-Inf pair can also make a NaN output)
 // falls back to the full last stage.  v is clobbered.
-__device__ __forceinline__ uint32_t rht16_absmax_bits_nan(float* v, uint32_t mask) {
-    rht16_first3(v, mask);
+__device__ __forceinline__ uint32_t rht16_absmax_bits_nan(float* v, const RhtSigns& sg) {
+    rht16_first3(v, sg);
     float s[8];
     rht16_pair_mags(v, s);
     uint32_t m = 0;
@@ -220,7 +220,7 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_amax_plain(const uint16_t*
 // max |RHT16(x)| over 16-chunks along the stored rows (non-transposed view).
 __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t* __restrict__ p,
                                                                  int64_t rows, int64_t k,
-                                                                 int64_t ld, uint32_t mask,
+                                                                 int64_t ld, const RhtSigns sg,
                                                                  float* out) {
     uint32_t m = 0;
     const uint32_t nkb = (uint32_t)(k >> 4);
@@ -232,7 +232,7 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
         float v[16];
         unpack8(ldg_stream(src), v);
         unpack8(ldg_stream(src + 1), v + 8);
-        m = max(m, rht16_absmax_bits_nan(v, mask));
+        m = max(m, rht16_absmax_bits_nan(v, sg));
     }
     block_max_to_global(m, out);
 }
@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
 // row), transformed one column at a time.
 __global__ void __launch_bounds__(kQuantThreads, 4) k_amax_rht_cols(const uint16_t* __restrict__ p,
                                                                     int64_t srows, int64_t scols,
-                                                                    int64_t ld, uint32_t mask,
+                                                                    int64_t ld, const RhtSigns sg,
                                                                     float* out) {
     uint32_t m = 0;
     const int64_t ncp = (scols + 1) >> 1, nkb = srows >> 4;
@@ -261,10 +261,10 @@ __global__ void __launch_bounds__(kQuantThreads, 4) k_amax_rht_cols(const uint16
         float v[16];
 #pragma unroll
         for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
-        m = max(m, rht16_absmax_bits_nan(v, mask));
+        m = max(m, rht16_absmax_bits_nan(v, sg));
 #pragma unroll
         for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
-        m = max(m, rht16_absmax_bits_nan(v, mask));
+        m = max(m, rht16_absmax_bits_nan(v, sg));
     }
     block_max_to_global(m, out);
 }
@@ -289,7 +289,7 @@ struct QuantArgs {
     float* gs_out2;             // copy of S_enc for the transposed operand (nullable)
     uint8_t* codes;             // [rows x k/2]
     uint8_t* scales;            // swizzled
-    uint32_t rht_mask;
+    RhtSigns rht;               // RHT-16 sign multipliers (RHT kernels only)
     uint64_t stream_id;
     uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10)
     // 2D transposed emit (optional)
@@ -329,7 +329,7 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
                                                uint32_t* code_lo, uint32_t* code_hi,
                                                uint32_t amax_bits = ~0u) {
     if (RHT) {
-        rht16_first3(v, a.rht_mask);
+        rht16_first3(v, a.rht);
         float s[8];
         rht16_pair_mags(v, s);
         const float m = fmaxf(fmax3(s[0], s[1], s[2]), fmax3(fmax3(s[3], s[4], s[5]), s[6], s[7]));
@@ -553,7 +553,7 @@ __global__ void __launch_bounds__(k2DThreads) k_quant2d(const QuantArgs a) {
             const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64 + b * 16);
             unpack8(ldg_stream(src), v[b]);
             unpack8(ldg_stream(src + 1), v[b] + 8);
-            if (RHT) rht16(v[b], a.rht_mask);
+            if (RHT) rht16(v[b], a.rht);
             lmax[b] = absmax_bits16(v[b]);
         } else {
 #pragma unroll

@@ -142,3 +142,20 @@ def test_dual_rejects_bad_calls(nv):
     a = torch.ones(1, device="cuda")
     with pytest.raises(nv.Nvfp4Error):
         nv.nvfp4_quantize_dual(d, a, 0, 0, 0, q, 0, a.clone(), 0, 0, 0, qt)
+
+
+def test_quantize_dual_many_tiles_per_cta(nv):
+    """1024 x 16384: 1024 tiles of 64 x 256, several per persistent CTA, so the
+    shared-memory ring wraps; SR on both sides and RHT on the column side."""
+    rows, cols = 1024, 16384
+    s = _data(rows, cols, 77, "t")
+    d = dev_bf16(s)
+    a, at = nv.nvfp4_amax_dual(d, MASK)
+    q, qt = nv.QTensor(rows, cols), nv.QTensor(cols, rows)
+    nv.nvfp4_quantize_dual(d, a, nv.NVFP4_SR, 17, 1, q, MASK, at, nv.NVFP4_SR, 17, 2, qt)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK
+    ref = oracle.quantize(s, sr=True, seed=17, stream_id=1)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "dual rows, many tiles")
+    ref_t = oracle.quantize(s, transposed=True, rht_mask=MASK, sr=True, seed=17, stream_id=2)
+    assert_q_equal(qt, ref_t.codes, ref_t.scales, ref_t.s_enc, "dual cols, many tiles")
