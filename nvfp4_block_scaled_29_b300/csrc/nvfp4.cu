@@ -199,14 +199,32 @@ void launch_q1d(const QuantArgs& a, bool transposed, cudaStream_t st) {
     }
 }
 
-template <bool RHT, bool SR>
-void launch_q2d(const QuantArgs& a, bool emit_t, cudaStream_t st) {
-    const dim3 grid((unsigned)cdiv(a.k, 128), (unsigned)(cdiv(a.rows, 128) * 2));
-    if (emit_t) {
-        if constexpr (!RHT) k_quant2d<false, SR, true><<<grid, k2DThreads, 0, st>>>(a);
-    } else {
-        k_quant2d<RHT, SR, false><<<grid, k2DThreads, 0, st>>>(a);
+template <bool RHT, bool SR, bool EMIT_T>
+nvfp4_status launch_q2d_t(const CUtensorMap& map, const QuantArgs& a, int grid, cudaStream_t st) {
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+    if (!ready[dev].load()) {
+        if (cudaFuncSetAttribute(k_quant2d<RHT, SR, EMIT_T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 kQ2Smem) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ready[dev].store(1);
     }
+    k_quant2d<RHT, SR, EMIT_T><<<grid, k2DThreads, kQ2Smem, st>>>(map, a);
+    return launch_status();
+}
+
+template <bool RHT, bool SR>
+nvfp4_status launch_q2d(const QuantArgs& a, bool emit_t, cudaStream_t st) {
+    CUtensorMap map;
+    if (!make_bf16_map(&map, a.x, a.rows, a.k, a.ld, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return NVFP4_ERR_CUDA;
+    const int64_t tiles = (cdiv(a.rows, 128) * 2) * cdiv(a.k, 128);
+    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * kQ2CtasPerSm));
+    if (emit_t) {
+        if constexpr (!RHT) return launch_q2d_t<false, SR, true>(map, a, grid, st);
+        return NVFP4_ERR_INVALID_ARG;
+    }
+    return launch_q2d_t<RHT, SR, false>(map, a, grid, st);
 }
 
 nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float* amax_dev,
@@ -284,14 +302,8 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
         a.scales_t = out_t ? out_t->scales : nullptr;
         a.idx_transposed = 0;
         const bool emit = out_t != nullptr;
-        if (mask) {
-            if (sr) launch_q2d<true, true>(a, false, st);
-            else launch_q2d<true, false>(a, false, st);
-        } else {
-            if (sr) launch_q2d<false, true>(a, emit, st);
-            else launch_q2d<false, false>(a, emit, st);
-        }
-        return launch_status();
+        if (mask) return sr ? launch_q2d<true, true>(a, false, st) : launch_q2d<true, false>(a, false, st);
+        return sr ? launch_q2d<false, true>(a, emit, st) : launch_q2d<false, false>(a, emit, st);
     }
     // 16x16 on a transposed view: quantise the stored [k x rows] array; its
     // primary output is the caller's out_t, its transposed emit the caller's out.
@@ -303,9 +315,7 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.codes_t = out->codes;
     a.scales_t = out->scales;
     a.idx_transposed = 1;
-    if (sr) launch_q2d<false, true>(a, true, st);
-    else launch_q2d<false, false>(a, true, st);
-    return launch_status();
+    return sr ? launch_q2d<false, true>(a, true, st) : launch_q2d<false, false>(a, true, st);
 }
 
 // ------------------------------------------------------------------ dual ---

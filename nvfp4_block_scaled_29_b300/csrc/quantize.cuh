@@ -21,8 +21,10 @@
 //    lane); the 16x16 block amax is a 4-step shuffle reduction.  The
 //    transposed operand is emitted from a shared-memory nibble tile.
 #pragma once
+#include <cuda.h>
 #include <cstdint>
 #include "codec.cuh"
+#include "ptx.cuh"
 #include "status.cuh"
 
 namespace nvfp4 {
@@ -529,150 +531,215 @@ __device__ __forceinline__ int tile_word(int R, int w) {
     return rp * 16 + qp * 4 + (w & 3);
 }
 
+// Persistent CTAs walk the 64-row x 128-column tiles (covering the
+// 128-padded row count) through a ring of kQ2Stages shared-memory slots.  A
+// tile arrives as two 64 x 64 boxes (TMA, 128-byte swizzle: 16-byte chunk c
+// of row r of a box at chunk c ^ (r & 7); zeros beyond the array), so that a
+// quarter warp's reads of one chunk of 8 consecutive rows hit distinct banks.
+constexpr int kQ2Stages = 3;
+constexpr int kQ2BoxBytes = 64 * 64 * 2;                           // 8 KB
+constexpr int kQ2TileBytes = 2 * kQ2BoxBytes;                      // 16 KB
+constexpr int kQ2Smem = kQ2Stages * kQ2TileBytes + 1024 + 64;      // + alignment slack, barriers
+constexpr int kQ2CtasPerSm = 4;
+
 template <bool RHT, bool SR, bool EMIT_T>
-__global__ void __launch_bounds__(k2DThreads) k_quant2d(const QuantArgs a) {
+__global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __grid_constant__ CUtensorMap map,
+                                                                      const __grid_constant__ QuantArgs a) {
+    extern __shared__ uint8_t q2_raw[];
+    uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q2_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(ring + kQ2Stages * kQ2TileBytes);
     __shared__ __align__(16) uint32_t tile_codes[64 * 16];
     __shared__ uint8_t tile_sb[4][8];          // [row block][k block]
+    __shared__ int abort_flag;
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nkb = a.k >> 4;
     const int64_t ngroups = (nkb + 3) >> 2;
-    const int64_t row0 = (int64_t)blockIdx.y * 64;
-    const int64_t r = row0 + warp * 16 + (lane & 15);
-    const int64_t g = (int64_t)blockIdx.x * 2 + (lane >> 4);
-    const bool row_ok = r < a.rows;
-    const bool grp_ok = g < ngroups;
-    const int nblk = grp_ok ? (int)min64(4, nkb - g * 4) : 0;
-
-    float v[4][16];
-    uint32_t lmax[4];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        if (row_ok && b < nblk) {
-            const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64 + b * 16);
-            unpack8(ldg_stream(src), v[b]);
-            unpack8(ldg_stream(src + 1), v[b] + 8);
-            if (RHT) rht16(v[b], a.rht);
-            lmax[b] = absmax_bits16(v[b]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < 16; ++j) v[b][j] = 0.0f;
-            lmax[b] = 0u;
-        }
-    }
-    // 16x16 block amax: reduce over the 16 lanes holding the block's rows.
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-#pragma unroll
-        for (int off = 1; off < 16; off <<= 1)
-            lmax[b] = max(lmax[b], __shfl_xor_sync(0xFFFFFFFFu, lmax[b], off));
-    }
-    uint32_t sw = 0, cw[8];
-#pragma unroll
-    for (int b = 0; b < 4; ++b) {
-        const uint32_t sb = (b < nblk) ? block_scale_code(__uint_as_float(lmax[b]), s_enc) : 0u;
-        const float r_b = (b < nblk) ? encode_factor(s_enc, sb) : 0.0f;
-        sw |= sb << (8 * b);
-#pragma unroll
-        for (int j = 0; j < 16; ++j) v[b][j] = __fmul_rn(v[b][j], r_b);
-        if (SR) {
-            uint32_t lo = 0, hi = 0;
-            if (row_ok && b < nblk) {
-                const int64_t c0 = g * 64 + b * 16;
-                if (a.idx_transposed) {
-                    // index in the transposed logical layout: (r, c) -> c * rows + r;
-                    // rows is a multiple of 16, so every element of the strip
-                    // takes the same word ((r % 16) / 4) and element position
-                    // (r % 4) of its own Philox block.
-                    const int wsel = (r >> 2) & 3, pos = r & 3;
-#pragma unroll
-                    for (int j = 0; j < 16; ++j) {
-                        const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
-                        const uint4 rb = sr_words16(idx >> 4, a.stream_id, a.sr_key);
-                        const uint32_t w = wsel == 0 ? rb.x : wsel == 1 ? rb.y : wsel == 2 ? rb.z : rb.w;
-                        const uint32_t q = e2m1_sr_at(v[b][j], w, pos);
-                        if (j < 8) lo |= q << (4 * j);
-                        else hi |= q << (4 * (j - 8));
-                    }
-                } else {
-                    const uint64_t idx0 = (uint64_t)(r * a.k + c0);
-                    e2m1x16_sr(v[b], sr_words16(idx0 >> 4, a.stream_id, a.sr_key), &lo, &hi);
-                }
-            }
-            cw[2 * b] = lo;
-            cw[2 * b + 1] = hi;
-        } else {
-            cw[2 * b] = e2m1x8_rne(v[b]);
-            cw[2 * b + 1] = e2m1x8_rne(v[b] + 8);
-        }
-    }
-    // primary operand
-    if (a.write_primary && grp_ok) {
-        uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
-        if (r < ((a.rows + 127) & ~int64_t(127))) *sdst = row_ok ? sw : 0u;
-        if (row_ok) {
-            uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
-            if (nblk == 4 && (a.k & 31) == 0) {
-                reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-            } else {
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    if (b < nblk)
-                        reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-            }
-        }
-    }
-    if (!EMIT_T) return;
-    // transposed operand: rows = k, k = a.rows (a multiple of 16 here)
-    {
-        const int R = warp * 16 + (lane & 15);
-        const bool live = row_ok && grp_ok;
-        const int h = lane >> 4;
-        *reinterpret_cast<uint4*>(&tile_codes[tile_word(R, 8 * h)]) =
-            live ? make_uint4(cw[0], cw[1], cw[2], cw[3]) : make_uint4(0, 0, 0, 0);
-        *reinterpret_cast<uint4*>(&tile_codes[tile_word(R, 8 * h + 4)]) =
-            live ? make_uint4(cw[4], cw[5], cw[6], cw[7]) : make_uint4(0, 0, 0, 0);
-        if ((lane & 15) == 0) {
-#pragma unroll
-            for (int b = 0; b < 4; ++b) tile_sb[warp][h * 4 + b] = (sw >> (8 * b)) & 0xFFu;
-        }
+    const int64_t row_tiles = ((a.rows + 127) & ~int64_t(127)) / 64;
+    const int64_t col_tiles = (a.k + 127) / 128;
+    const int64_t ntiles = row_tiles * col_tiles;
+    if (threadIdx.x == 0) {
+        for (int st = 0; st < kQ2Stages; ++st) mbar_init(&full[st], 1);
+        abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&map);
     }
     __syncthreads();
-    const int64_t kt = a.rows;                                     // k of the transposed operand
-    const int64_t ngroups_t = ((kt >> 4) + 3) >> 2;
-    const int64_t gt = row0 >> 6;                                  // 4 blocks of 16 rows
-    if (gt >= ngroups_t) return;                                   // beyond the padded columns
-    {
-        // scales: thread = one row (stored column) of the transposed operand
-        const int64_t ct = (int64_t)blockIdx.x * 128 + threadIdx.x;
-        const int64_t ct_pad = (a.k + 127) & ~int64_t(127);
-        if (ct < ct_pad) {
-            uint32_t* sdst_t =
-                reinterpret_cast<uint32_t*>(a.scales_t + scale_offset(ct, gt * 4, ngroups_t));
-            const int kb_local = threadIdx.x >> 4;
-            *sdst_t = ct >= a.k ? 0u
-                                : (uint32_t)tile_sb[0][kb_local] | ((uint32_t)tile_sb[1][kb_local] << 8) |
-                                      ((uint32_t)tile_sb[2][kb_local] << 16) |
-                                      ((uint32_t)tile_sb[3][kb_local] << 24);
+    auto issue = [&](int64_t t, int st) {
+        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+        mbar_arrive_expect_tx(&full[st], kQ2TileBytes);
+        tma_load_2d(ring + st * kQ2TileBytes, &map, &full[st], (int32_t)(tc * 128), (int32_t)(tr * 64));
+        tma_load_2d(ring + st * kQ2TileBytes + kQ2BoxBytes, &map, &full[st], (int32_t)(tc * 128 + 64),
+                    (int32_t)(tr * 64));
+    };
+    if (threadIdx.x == 0)
+        for (int st = 0; st < kQ2Stages; ++st) {
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)st * gridDim.x;
+            if (t < ntiles) issue(t, st);
+        }
+    const int lr = warp * 16 + (lane & 15);    // tile row of this lane
+    const int lg = lane >> 4;                  // 64-column half of the tile (= box)
+
+    int it = 0;
+    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++it) {
+        const int slot = it % kQ2Stages;
+        const bool got = mbar_wait_bounded(&full[slot], (uint32_t)(it / kQ2Stages) & 1u, &abort_flag);
+        __syncthreads();                       // every thread saw the same outcome
+        if (abort_flag || !got) break;
+        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+        const int64_t row0 = tr * 64;
+        const int64_t r = row0 + lr;
+        const int64_t g = tc * 2 + lg;
+        const bool row_ok = r < a.rows;
+        const bool grp_ok = g < ngroups;
+        const int nblk = grp_ok ? (int)min64(4, nkb - g * 4) : 0;
+
+        float v[4][16];
+        uint32_t lmax[4];
+        {
+            const uint8_t* tile = ring + slot * kQ2TileBytes + lg * kQ2BoxBytes + lr * 128;
+#pragma unroll
+            for (int b = 0; b < 4; ++b) {
+                if (row_ok && b < nblk) {
+                    unpack8(*reinterpret_cast<const uint4*>(tile + (((2 * b) ^ (lr & 7)) << 4)), v[b]);
+                    unpack8(*reinterpret_cast<const uint4*>(tile + (((2 * b + 1) ^ (lr & 7)) << 4)), v[b] + 8);
+                    if (RHT) rht16(v[b], a.rht);
+                    lmax[b] = absmax_bits16(v[b]);
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 16; ++j) v[b][j] = 0.0f;
+                    lmax[b] = 0u;
+                }
+            }
+        }
+        __syncthreads();                       // slot fully read: refill it
+        if (threadIdx.x == 0) {
+            const int64_t tn = t + (int64_t)kQ2Stages * gridDim.x;
+            if (tn < ntiles) issue(tn, slot);
+        }
+        // 16x16 block amax: reduce over the 16 lanes holding the block's rows.
+    #pragma unroll
+        for (int b = 0; b < 4; ++b) {
+    #pragma unroll
+            for (int off = 1; off < 16; off <<= 1)
+                lmax[b] = max(lmax[b], __shfl_xor_sync(0xFFFFFFFFu, lmax[b], off));
+        }
+        uint32_t sw = 0, cw[8];
+    #pragma unroll
+        for (int b = 0; b < 4; ++b) {
+            const uint32_t sb = (b < nblk) ? block_scale_code(__uint_as_float(lmax[b]), s_enc) : 0u;
+            const float r_b = (b < nblk) ? encode_factor(s_enc, sb) : 0.0f;
+            sw |= sb << (8 * b);
+    #pragma unroll
+            for (int j = 0; j < 16; ++j) v[b][j] = __fmul_rn(v[b][j], r_b);
+            if (SR) {
+                uint32_t lo = 0, hi = 0;
+                if (row_ok && b < nblk) {
+                    const int64_t c0 = g * 64 + b * 16;
+                    if (a.idx_transposed) {
+                        // index in the transposed logical layout: (r, c) -> c * rows + r;
+                        // rows is a multiple of 16, so every element of the strip
+                        // takes the same word ((r % 16) / 4) and element position
+                        // (r % 4) of its own Philox block.
+                        const int wsel = (r >> 2) & 3, pos = r & 3;
+    #pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
+                            const uint4 rb = sr_words16(idx >> 4, a.stream_id, a.sr_key);
+                            const uint32_t w = wsel == 0 ? rb.x : wsel == 1 ? rb.y : wsel == 2 ? rb.z : rb.w;
+                            const uint32_t q = e2m1_sr_at(v[b][j], w, pos);
+                            if (j < 8) lo |= q << (4 * j);
+                            else hi |= q << (4 * (j - 8));
+                        }
+                    } else {
+                        const uint64_t idx0 = (uint64_t)(r * a.k + c0);
+                        e2m1x16_sr(v[b], sr_words16(idx0 >> 4, a.stream_id, a.sr_key), &lo, &hi);
+                    }
+                }
+                cw[2 * b] = lo;
+                cw[2 * b + 1] = hi;
+            } else {
+                cw[2 * b] = e2m1x8_rne(v[b]);
+                cw[2 * b + 1] = e2m1x8_rne(v[b] + 8);
+            }
+        }
+        // primary operand
+        if (a.write_primary && grp_ok) {
+            uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
+            if (r < ((a.rows + 127) & ~int64_t(127))) *sdst = row_ok ? sw : 0u;
+            if (row_ok) {
+                uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
+                if (nblk == 4 && (a.k & 31) == 0) {
+                    reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                    reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+                } else {
+    #pragma unroll
+                    for (int b = 0; b < 4; ++b)
+                        if (b < nblk)
+                            reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+                }
+            }
+        }
+        if (EMIT_T) {
+            // transposed operand: rows = k, k = a.rows (a multiple of 16 here)
+            {
+                const int R = warp * 16 + (lane & 15);
+                const bool live = row_ok && grp_ok;
+                const int h = lane >> 4;
+                *reinterpret_cast<uint4*>(&tile_codes[tile_word(R, 8 * h)]) =
+                    live ? make_uint4(cw[0], cw[1], cw[2], cw[3]) : make_uint4(0, 0, 0, 0);
+                *reinterpret_cast<uint4*>(&tile_codes[tile_word(R, 8 * h + 4)]) =
+                    live ? make_uint4(cw[4], cw[5], cw[6], cw[7]) : make_uint4(0, 0, 0, 0);
+                if ((lane & 15) == 0) {
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) tile_sb[warp][h * 4 + b] = (sw >> (8 * b)) & 0xFFu;
+                }
+            }
+            __syncthreads();
+            const int64_t kt = a.rows;                                 // k of the transposed operand
+            const int64_t ngroups_t = ((kt >> 4) + 3) >> 2;
+            const int64_t gt = row0 >> 6;                              // 4 blocks of 16 rows
+            if (gt < ngroups_t) {                                      // else beyond the padded columns
+                // scales: thread = one row (stored column) of the transposed operand
+                const int64_t ct = tc * 128 + threadIdx.x;
+                const int64_t ct_pad = (a.k + 127) & ~int64_t(127);
+                if (ct < ct_pad) {
+                    uint32_t* sdst_t =
+                        reinterpret_cast<uint32_t*>(a.scales_t + scale_offset(ct, gt * 4, ngroups_t));
+                    const int kb_local = threadIdx.x >> 4;
+                    *sdst_t = ct >= a.k ? 0u
+                                        : (uint32_t)tile_sb[0][kb_local] | ((uint32_t)tile_sb[1][kb_local] << 8) |
+                                              ((uint32_t)tile_sb[2][kb_local] << 16) |
+                                              ((uint32_t)tile_sb[3][kb_local] << 24);
+                }
+                // codes: thread = 8 stored rows (rb) x 8 stored columns (cb) of the
+                // tile, transposed in registers; a warp writes 4 columns x 32
+                // contiguous bytes.
+                const int rb = threadIdx.x & 7, cb = threadIdx.x >> 3;
+                const int64_t rows_here = min64(64, a.rows - row0);    // multiple of 16 when > 0
+                if (rb * 8 < rows_here) {
+                    uint32_t x[8];
+#pragma unroll
+                    for (int q = 0; q < 8; ++q) x[q] = tile_codes[tile_word(rb * 8 + q, cb)];
+                    transpose8x8_nibbles(x);
+                    const int64_t c0 = tc * 128 + cb * 8;
+                    uint8_t* cdst = a.codes_t + c0 * (kt >> 1) + (row0 >> 1) + rb * 4;
+#pragma unroll
+                    for (int n = 0; n < 8; ++n)
+                        if (c0 + n < a.k) *reinterpret_cast<uint32_t*>(cdst + n * (kt >> 1)) = x[n];
+                }
+            }
         }
     }
-    if (row0 >= a.rows) return;
-    // codes: thread = 8 stored rows (rb) x 8 stored columns (cb) of the tile,
-    // transposed in registers; a warp writes 4 columns x 32 contiguous bytes.
-    const int rb = threadIdx.x & 7, cb = threadIdx.x >> 3;
-    const int64_t rows_here = min64(64, a.rows - row0);            // multiple of 16
-    if (rb * 8 >= rows_here) return;
-    uint32_t x[8];
-#pragma unroll
-    for (int i = 0; i < 8; ++i) x[i] = tile_codes[tile_word(rb * 8 + i, cb)];
-    transpose8x8_nibbles(x);
-    const int64_t c0 = (int64_t)blockIdx.x * 128 + cb * 8;
-    uint8_t* cdst = a.codes_t + c0 * (kt >> 1) + (row0 >> 1) + rb * 4;
-#pragma unroll
-    for (int n = 0; n < 8; ++n)
-        if (c0 + n < a.k) *reinterpret_cast<uint32_t*>(cdst + n * (kt >> 1)) = x[n];
+    // drain: no copy may still be writing into this CTA's shared memory
+    if (threadIdx.x == 0 && abort_flag) {
+        for (int k = 0; k < kQ2Stages; ++k) {
+            const int ii = it + k;
+            const int64_t t = (int64_t)blockIdx.x + (int64_t)ii * gridDim.x;
+            if (t < ntiles) mbar_wait_bounded(&full[ii % kQ2Stages], (uint32_t)(ii / kQ2Stages) & 1u, nullptr);
+        }
+    }
 }
 
 // ======================================================== dequantise ======

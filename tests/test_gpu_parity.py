@@ -142,6 +142,19 @@ def test_quantize_2d(nv, rows, k, sr, emit_t):
         assert_q_equal(qt, codes_t, scales_t, ref.s_enc, f"2d-T {rows}x{k} sr={sr}")
 
 
+@pytest.mark.parametrize("sr", [False, True])
+def test_quantize_2d_many_tiles_per_cta(nv, sr):
+    """4096 x 4096: 2048 tiles of 64 x 128, several per persistent CTA, so the
+    shared-memory ring wraps; with the transposed emit."""
+    rows, k = 4096, 4096
+    w = synth.normal_bf16((rows, k), 31, 0.02)
+    q, qt, _ = gpu_quantize(nv, dev_bf16(w), block2d=True, sr=sr, seed=3, sid=2, emit_t=True)
+    ref = oracle.quantize(w, block2d=True, sr=sr, seed=3, stream_id=2)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, f"2d many tiles sr={sr}")
+    codes_t, scales_t = expected_transpose(ref)
+    assert_q_equal(qt, codes_t, scales_t, ref.s_enc, f"2d-T many tiles sr={sr}")
+
+
 @pytest.mark.parametrize("rows,k", [(37, 64), (5, 16), (130, 96)])
 def test_quantize_2d_ragged_rows(nv, rows, k):
     w = synth.normal_bf16((rows, k), 3000 + rows, 0.02)
