@@ -230,7 +230,9 @@ def _upload_operand(nv, codes, scales_plain, s_enc, rows, k):
                                    (130, 260, 320), (384, 256, 1024), (128, 128, 4160),
                                    # several CTA-pair units, M- and N-fastest tile walks
                                    (512, 512, 512), (500, 300, 96), (1024, 768, 1280), (2048, 256, 512),
-                                   (512, 4096, 256)])
+                                   (512, 4096, 256),
+                                   # 384-column pair tiles, several units per pair
+                                   (2048, 6144, 512)])
 @pytest.mark.parametrize("bf16", [False, True])
 def test_gemm_random_operands(nv, M, N, K, bf16):
     ca, sa = synth.random_operand(M, K, M + 7 * K)
