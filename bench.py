@@ -118,8 +118,9 @@ class ClockSampler:
 class Step:
     """Device buffers and the launch sequence of one linear-layer step."""
 
-    def __init__(self, nv, torch, host, path: str = "dual"):
+    def __init__(self, nv, torch, host, path: str = "dual", sr_round=None):
         self.nv, self.torch = nv, torch
+        self.sr_round = nv.NVFP4_SR if sr_round is None else sr_round
         dev = "cuda"
         self.stream = torch.cuda.current_stream()
         self.x = torch.empty((TOKENS, HIDDEN), dtype=torch.bfloat16, device=dev)
@@ -163,7 +164,7 @@ class Step:
         operands (dual-axis amax and quantise); "separate": every operand by
         its own amax and quantiser call."""
         nv, a = self.nv, self.amax
-        rne, sr = nv.NVFP4_RNE, nv.NVFP4_SR
+        rne, sr = nv.NVFP4_RNE, self.sr_round
         x, w, dy = TOKENS * HIDDEN, FFN * HIDDEN, TOKENS * FFN
         fwd_w = [("amax_w", lambda: nv.nvfp4_amax(self.w, 0, a[1:2]), w * B_AMAX, False),
                  ("q2d_w", lambda: nv.nvfp4_quantize_2d(self.w, a[1:2], rne, 0, 0, self.qw, self.qwt),
@@ -226,6 +227,8 @@ PROFILE_CASES = {
     "amax_dual_dy": lambda s: s.nv.nvfp4_amax_dual(s.dy, s.mask, s.amax[2:3], s.amax[3:4]),
     "quant_dual_dy": lambda s: s.nv.nvfp4_quantize_dual(s.dy, s.amax[2:3], s.nv.NVFP4_SR, SR_SEED, 1, s.qdy, s.mask,
                                                         s.amax[3:4], s.nv.NVFP4_SR, SR_SEED, 2, s.qdyt),
+    "quant_dual_dy_hw": lambda s: s.nv.nvfp4_quantize_dual(s.dy, s.amax[2:3], s.nv.NVFP4_SR_HW, SR_SEED, 1, s.qdy,
+                                                           s.mask, s.amax[3:4], s.nv.NVFP4_SR_HW, SR_SEED, 2, s.qdyt),
     "quant_dual_x": lambda s: s.nv.nvfp4_quantize_dual(s.x, s.amax[0:1], s.nv.NVFP4_RNE, 0, 0, s.qx, s.mask,
                                                        s.amax[4:5], s.nv.NVFP4_RNE, 0, 0, s.qxt),
 }
@@ -328,6 +331,9 @@ def main():
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP4 comparison timing")
     ap.add_argument("--path", default="dual", choices=["dual", "separate"],
                     help="dual: X and dY read once each for both operands; separate: one call per operand")
+    ap.add_argument("--sr", default="philox16", choices=["philox16", "hw"],
+                    help="rounding of dY: philox16 = NVFP4_SR (16 independent Philox bits per element), "
+                         "hw = NVFP4_SR_HW (random bits in the hardware SR conversion's layout)")
     ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
                     help="after one full untimed step, launch only this call --steps times "
                          "(a target for ncu -k; prints nothing)")
@@ -353,7 +359,7 @@ def main():
     host["y"] = torch.empty((TOKENS, FFN), dtype=torch.int16).pin_memory()
     host["dx"] = torch.empty((TOKENS, HIDDEN), dtype=torch.int16).pin_memory()
     host["dw"] = torch.empty((FFN, HIDDEN), dtype=torch.int16).pin_memory()
-    step = Step(nv, torch, host, args.path)
+    step = Step(nv, torch, host, args.path, nv.NVFP4_SR_HW if args.sr == "hw" else nv.NVFP4_SR)
     gemm_idx = [j for j, p in enumerate(step.seq) if p[3]]
     quant_idx = [j for j, p in enumerate(step.seq) if not p[3]]
     torch.cuda.synchronize()
@@ -443,6 +449,8 @@ def main():
         "data": "synthetic (seeded N(0,1)+outliers, N(0,0.02^2), 1e-3*t3)",
         "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
                    "path": args.path,
+                   "sr": ("NVFP4_SR_HW: random bits in the hardware SR conversion's layout" if args.sr == "hw"
+                          else "NVFP4_SR: 16 independent Philox4x32-10 bits per element"),
                    "l2": "flushed before each step (256 MiB device write, untimed)",
                    "parallelism": f"replicas x{world}"},
         "gemm_tflops": gemm_tflops,
@@ -468,6 +476,8 @@ def main():
     if not args.no_mx:
         out["mxfp4"] = time_mxfp4(nv, torch, step)
         out["autograd"] = time_autograd(torch, step)
+        if args.path == "dual" and args.sr == "philox16":
+            out["sr_hw"] = time_sr_hw(nv, torch, step, out["phase_ms"], ms_per_step)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_step_sample(rows=96, pts=2048)
         out["cpu_baseline"].pop("seconds_per_step_extrapolated", None)
@@ -504,6 +514,32 @@ def time_autograd(torch, step, reps: int = 10) -> dict:
         ts.append(e0.elapsed_time(e1))
     ms = st.median(ts)
     return {"ms_per_step": round(ms, 4), "tflops": STEP_FLOPS / (ms * 1e-3) / 1e12}
+
+
+def time_sr_hw(nv, torch, step, phase_ms: dict, ms_per_step: float, reps: int = 10) -> dict:
+    """The dual-axis quantise of dY with rounding mode NVFP4_SR_HW (the same
+    rule, random bits in the hardware SR conversion's layout), CUDA events
+    after an L2 flush, and the step time with that phase in place of the
+    NVFP4_SR one."""
+    import statistics as st
+    a = step.amax
+
+    def once():
+        nv.nvfp4_quantize_dual(step.dy, a[2:3], nv.NVFP4_SR_HW, SR_SEED, 1, step.qdy, step.mask, a[3:4],
+                               nv.NVFP4_SR_HW, SR_SEED, 2, step.qdyt)
+
+    once()
+    ts = []
+    for _ in range(reps):
+        step.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); once(); e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    q_ms = st.median(ts)
+    ms = ms_per_step - phase_ms["quant_dual_dy"] + q_ms
+    return {"quant_dual_dy_ms": round(q_ms, 4), "step_ms": round(ms, 4),
+            "step_tflops": STEP_FLOPS / (ms * 1e-3) / 1e12}
 
 
 def time_mxfp4(nv, torch, step, reps: int = 10) -> dict:

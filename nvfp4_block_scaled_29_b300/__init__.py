@@ -37,6 +37,7 @@ NVFP4_ERR_TIMEOUT = 5
 NVFP4_ERR_CUDA = 6
 NVFP4_RNE = 0
 NVFP4_SR = 1
+NVFP4_SR_HW = 2              # the same rule, random bits in the hardware conversion's layout
 
 
 class Nvfp4Error(RuntimeError):

@@ -110,18 +110,90 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const uint32_t* key) {
     return c;
 }
 
-// Random words of the 16 elements idx = 16*g .. 16*g+15 of a quantised
-// operand: the Philox block of counter (g, stream_id); element idx reads
-// word (idx % 16) / 4.
+// NVFP4_SR_HW: random words of the 16 elements idx = 16*g .. 16*g+15 of a
+// quantised operand: the Philox block of counter (g, stream_id); element idx
+// reads word (idx % 16) / 4.
 __device__ __forceinline__ uint4 sr_words16(uint64_t g, uint64_t stream_id, const uint32_t* key) {
     return philox4x32_10(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
                                     (uint32_t)(stream_id >> 32)),
                          key);
 }
 
-// ------------------------------------------------------ stochastic E2M1 ---
-// Stochastic rounding to E2M1 by the hardware conversion with random bits:
-// each value takes a 16-bit integer r from the 32-bit word w and rounds up
+// ------------------------------------- stochastic E2M1, software (NVFP4_SR) --
+// Philox4x32-10 with every output word complemented, with the round keys
+// precomputed: key[2r], key[2r+1] = (k0 + r * 0x9E3779B9, k1 + r *
+// 0xBB67AE85) for rounds r = 0..8, and the complements of the round-9 keys
+// in key[18], key[19] (the complement of the two XOR-ed output words is folded
+// into them; the two low-product words take one NOT each).
+__device__ __forceinline__ uint4 philox4x32_10_not(uint4 c, const uint32_t* key) {
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u;
+        const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57u;
+        const uint32_t lo1 = (uint32_t)p1, lo0 = (uint32_t)p0;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ key[2 * round], round == 9 ? ~lo1 : lo1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ key[2 * round + 1], round == 9 ? ~lo0 : lo0);
+    }
+    return c;
+}
+
+// Stochastic-rounding words of the 8 elements idx = 8*g .. 8*g+7 of a
+// quantised operand: the Philox block of counter (g, stream_id) under the key
+// schedule `key` (see philox4x32_10_not), complemented, so that the 16-bit
+// slice of element j (word j/2, low half first) holds rp = 65535 - u16.
+__device__ __forceinline__ uint4 sr_rp8(uint64_t g, uint64_t stream_id, const uint32_t* key) {
+    return philox4x32_10_not(make_uint4((uint32_t)g, (uint32_t)(g >> 32), (uint32_t)stream_id,
+                                        (uint32_t)(stream_id >> 32)),
+                             key);
+}
+
+// dp2a selectors: rp * 64 from the low (SEL_LO) or high (SEL_HI) half-word.
+constexpr uint32_t SR_SEL_LO = 0x40u, SR_SEL_HI = 0x4000u;
+
+// Stochastic E2M1 rounding of one value v = x * r_b (rounding mode
+// NVFP4_SR: 16 independent random bits per element), realised as "add random
+// bits below the kept precision, then truncate".  With lo <= |v| < hi the
+// neighbouring grid values, the rule is: round up iff u16 < F = floor(frac *
+// 2^16), frac = (|v| - lo) / (hi - lo).
+//  * On [1, 16) the E2M1 grid (with 8, 12, 16 beyond the top, all of which
+//    saturate to 6) is 2^e x {1, 1.5}: the kept bits are the exponent and
+//    mantissa bit 22, and mantissa bits 21..6 hold F.  Adding rp = 65535 - u16
+//    at bit 6 carries into the kept bits exactly when F > u16.
+//  * Below 1 (grid 0, 0.5, 1: spacing 0.5) |v| is first moved to [1, 2) by a
+//    round-toward-zero add of c = 1.0 (the truncation is below 2^-17, so F is
+//    unchanged) and moved back by an exact subtraction of c.  For |v| >= 1,
+//    c = 0 and both adds are exact no-ops.
+//  * |v| < 16 always holds (|x| <= amax_b and s_b is at least 2/3 of
+//    amax_b * S_enc / 6 whenever it is non-zero), so the add never reaches
+//    the exponent field's top.
+// dp2a forms rp * 64 + bits(|v| + c) from the selected half-word of the
+// complemented Philox word in one instruction.  The result is the chosen
+// grid value, sign kept (the RNE conversion then returns its code unchanged).
+__device__ __forceinline__ float sr_grid_value(float v, uint32_t rp_word, uint32_t sel) {
+    const float a = fabsf(v);
+    float c;
+    asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(c) : "f"(a));
+    const float a2 = __fadd_rz(a, c);
+    uint32_t qb;
+    asm("dp2a.lo.u32.u32 %0, %1, %2, %3;" : "=r"(qb) : "r"(rp_word), "r"(sel), "r"(__float_as_uint(a2)));
+    const float q = __fsub_rn(__uint_as_float(qb & 0xFFC00000u), c);
+    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(v) & 0x80000000u));
+}
+
+// Eight values -> eight SR codes (element 0 in the lowest nibble), rp = the
+// complemented Philox block of these 8 elements.
+__device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 rp) {
+    const uint32_t w[4] = {rp.x, rp.y, rp.z, rp.w};
+    float g[8];
+#pragma unroll
+    for (int j = 0; j < 8; ++j) g[j] = sr_grid_value(v[j], w[j >> 1], (j & 1) ? SR_SEL_HI : SR_SEL_LO);
+    return e2m1x8_rne(g);
+}
+
+// --------------------------- stochastic E2M1, hardware layout (NVFP4_SR_HW) --
+// Stochastic rounding to E2M1 by the hardware conversion with random bits
+// (rounding mode NVFP4_SR_HW): each value takes a 16-bit integer r from the
+// 32-bit word w and rounds up
 // iff floor(frac * 2^16) + r >= 2^16 (frac: its position between the two
 // neighbouring grid values), saturating at 6, sign kept.  Of the four
 // values of one conversion, the last operand takes r = L = (byte 2, byte 0)

@@ -78,7 +78,8 @@ __device__ __forceinline__ uint32_t dq_chunk(int b, int r, int c) {
     return (uint32_t)(b * kDqBoxBytes + r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <bool SR1, bool SR2, bool RHT2>
+// SR1, SR2: rounding of each operand, 0 = RNE, 1 = NVFP4_SR, 2 = NVFP4_SR_HW.
+template <int SR1, int SR2, bool RHT2>
 __global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_constant__ CUtensorMap map,
                                                                  const __grid_constant__ DualArgs d) {
     extern __shared__ uint8_t dq_raw[];
@@ -166,7 +167,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_co
                             unpack8(lo, v);
                             unpack8(hi, v + 8);
                             uint32_t sb;
-                            encode_block16<false, SR1>(v, s1, rtab1, (uint64_t)(row * C + G * 64 + b * 16), a1, &sb,
+                            encode_block16<false, SR1 != 0, SR1 == 2>(v, s1, rtab1, (uint64_t)(row * C + G * 64 + b * 16), a1, &sb,
                                                        &cw[2 * b], &cw[2 * b + 1], absmax_bits16_packed(lo, hi));
                             sw |= sb << (8 * b);
                         }
@@ -214,12 +215,12 @@ __global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_co
                             uint32_t sb;
 #pragma unroll
                             for (int u = 0; u < 16; ++u) v[u] = bf16_lo(w[u]);
-                            encode_block16<RHT2, SR2>(v, s2, rtab2, (uint64_t)(cc * R + kc), a2, &sb, &c0w[2 * b],
+                            encode_block16<RHT2, SR2 != 0, SR2 == 2>(v, s2, rtab2, (uint64_t)(cc * R + kc), a2, &sb, &c0w[2 * b],
                                                       &c0w[2 * b + 1]);
                             sw0 |= sb << (8 * b);
 #pragma unroll
                             for (int u = 0; u < 16; ++u) v[u] = bf16_hi(w[u]);
-                            encode_block16<RHT2, SR2>(v, s2, rtab2, (uint64_t)((cc + 1) * R + kc), a2, &sb,
+                            encode_block16<RHT2, SR2 != 0, SR2 == 2>(v, s2, rtab2, (uint64_t)((cc + 1) * R + kc), a2, &sb,
                                                       &c1w[2 * b], &c1w[2 * b + 1]);
                             sw1 |= sb << (8 * b);
                         }

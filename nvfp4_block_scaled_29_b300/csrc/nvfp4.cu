@@ -174,16 +174,22 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
 }
 
 // -------------------------------------------------------------- quantise ---
-// Philox round keys of the seed (see philox4x32_10).
-void set_sr_keys(QuantArgs* a, uint64_t seed) {
+// Philox round keys of the seed and the rounding mode's generator: the
+// software rounding (NVFP4_SR) runs philox4x32_10_not, whose round-9 pair is
+// complemented; NVFP4_SR_HW runs the plain philox4x32_10.
+void set_sr_keys(QuantArgs* a, uint64_t seed, nvfp4_round round) {
     uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
+    const bool hw = round == NVFP4_SR_HW;
     for (int r = 0; r < 10; ++r) {
-        a->sr_key[2 * r] = k0;
-        a->sr_key[2 * r + 1] = k1;
+        a->sr_key[2 * r] = (r == 9 && !hw) ? ~k0 : k0;
+        a->sr_key[2 * r + 1] = (r == 9 && !hw) ? ~k1 : k1;
         k0 += 0x9E3779B9u;
         k1 += 0xBB67AE85u;
     }
+    a->sr_hw = hw ? 1 : 0;
 }
+
+bool valid_round(nvfp4_round r) { return r == NVFP4_RNE || r == NVFP4_SR || r == NVFP4_SR_HW; }
 
 template <bool RHT, bool SR>
 void launch_q1d(const QuantArgs& a, bool transposed, cudaStream_t st) {
@@ -233,7 +239,7 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     nvfp4_status s = check_view(x, true);
     if (s != NVFP4_OK) return s;
     if (mask > 0xFFFFu) return NVFP4_ERR_INVALID_ARG;
-    if (round != NVFP4_RNE && round != NVFP4_SR) return NVFP4_ERR_INVALID_ARG;
+    if (!valid_round(round)) return NVFP4_ERR_INVALID_ARG;
     if ((s = check_q(out, x.rows, x.cols)) != NVFP4_OK) return s;
     if (out_t != nullptr) {
         if (!block2d || mask != 0) return NVFP4_ERR_INVALID_ARG;
@@ -273,9 +279,9 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.gs_out = out->global_scale;
     a.gs_out2 = out_t ? out_t->global_scale : nullptr;
     a.rht = rht_signs(mask);
-    set_sr_keys(&a, seed);
+    set_sr_keys(&a, seed, round);
     a.stream_id = stream_id;
-    const bool sr = round == NVFP4_SR;
+    const bool sr = round != NVFP4_RNE;
 
     if (!block2d) {
         a.rows = x.rows;
@@ -319,7 +325,7 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
 }
 
 // ------------------------------------------------------------------ dual ---
-template <bool SR1, bool SR2, bool RHT2>
+template <int SR1, int SR2, bool RHT2>
 nvfp4_status launch_dual_t(const CUtensorMap& map, const DualArgs& d, int grid, cudaStream_t st) {
     static std::atomic<int> ready[kMaxDevices];
     int dev = 0;
@@ -335,7 +341,23 @@ nvfp4_status launch_dual_t(const CUtensorMap& map, const DualArgs& d, int grid, 
     return launch_status();
 }
 
-nvfp4_status launch_dual(const DualArgs& d, bool sr1, bool sr2, bool rht2, cudaStream_t st) {
+template <int SR1, int SR2>
+nvfp4_status launch_dual_rht(const CUtensorMap& map, const DualArgs& d, bool rht2, int grid, cudaStream_t st) {
+    return rht2 ? launch_dual_t<SR1, SR2, true>(map, d, grid, st) : launch_dual_t<SR1, SR2, false>(map, d, grid, st);
+}
+
+template <int SR1>
+nvfp4_status launch_dual_sr2(const CUtensorMap& map, const DualArgs& d, int sr2, bool rht2, int grid,
+                             cudaStream_t st) {
+    switch (sr2) {
+        case 0: return launch_dual_rht<SR1, 0>(map, d, rht2, grid, st);
+        case 1: return launch_dual_rht<SR1, 1>(map, d, rht2, grid, st);
+        default: return launch_dual_rht<SR1, 2>(map, d, rht2, grid, st);
+    }
+}
+
+// sr1, sr2: 0 = RNE, 1 = NVFP4_SR, 2 = NVFP4_SR_HW
+nvfp4_status launch_dual(const DualArgs& d, int sr1, int sr2, bool rht2, cudaStream_t st) {
     CUtensorMap map;
     if (!make_bf16_map(&map, d.row.x, d.row.rows, d.row.k, d.row.ld, kDqBoxCols, kDqRows,
                        CU_TENSOR_MAP_SWIZZLE_128B))
@@ -343,16 +365,10 @@ nvfp4_status launch_dual(const DualArgs& d, bool sr1, bool sr2, bool rht2, cudaS
     const int64_t rows_pad = cdiv(d.row.rows, 128) * 128;
     const int64_t tiles = (rows_pad / kDqRows) * cdiv(d.row.k, kDqCols);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
-    const int sel = (sr1 ? 4 : 0) | (sr2 ? 2 : 0) | (rht2 ? 1 : 0);
-    switch (sel) {
-        case 0: return launch_dual_t<false, false, false>(map, d, grid, st);
-        case 1: return launch_dual_t<false, false, true>(map, d, grid, st);
-        case 2: return launch_dual_t<false, true, false>(map, d, grid, st);
-        case 3: return launch_dual_t<false, true, true>(map, d, grid, st);
-        case 4: return launch_dual_t<true, false, false>(map, d, grid, st);
-        case 5: return launch_dual_t<true, false, true>(map, d, grid, st);
-        case 6: return launch_dual_t<true, true, false>(map, d, grid, st);
-        default: return launch_dual_t<true, true, true>(map, d, grid, st);
+    switch (sr1) {
+        case 0: return launch_dual_sr2<0>(map, d, sr2, rht2, grid, st);
+        case 1: return launch_dual_sr2<1>(map, d, sr2, rht2, grid, st);
+        default: return launch_dual_sr2<2>(map, d, sr2, rht2, grid, st);
     }
 }
 
@@ -553,7 +569,7 @@ nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4
     nvfp4_status s = check_view(x, true);
     if (s != NVFP4_OK) return s;
     if (x.transposed != 0 || rht_mask_t > 0xFFFFu) return NVFP4_ERR_INVALID_ARG;
-    if ((round != NVFP4_RNE && round != NVFP4_SR) || (round_t != NVFP4_RNE && round_t != NVFP4_SR))
+    if (!valid_round(round) || !valid_round(round_t))
         return NVFP4_ERR_INVALID_ARG;
     if (x.rows % 16 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if ((s = check_q(out, x.rows, x.cols)) != NVFP4_OK) return s;
@@ -581,7 +597,7 @@ nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4
     a1.scales = out->scales;
     a1.stream_id = stream_id;
     a1.write_primary = 1;
-    set_sr_keys(&a1, seed);
+    set_sr_keys(&a1, seed, round);
     QuantArgs& a2 = d.col;
     a2.x = a1.x;
     a2.ld = x.ld;
@@ -594,8 +610,8 @@ nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4
     a2.rht = rht_signs(rht_mask_t);
     a2.stream_id = stream_id_t;
     a2.write_primary = 1;
-    set_sr_keys(&a2, seed_t);
-    return launch_dual(d, round == NVFP4_SR, round_t == NVFP4_SR, rht_mask_t != 0, stream);
+    set_sr_keys(&a2, seed_t, round_t);
+    return launch_dual(d, (int)round, (int)round_t, rht_mask_t != 0, stream);
 }
 
 nvfp4_status nvfp4_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int64_t ld,

@@ -293,7 +293,9 @@ struct QuantArgs {
     uint8_t* scales;            // swizzled
     RhtSigns rht;               // RHT-16 sign multipliers (RHT kernels only)
     uint64_t stream_id;
-    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10)
+    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10_not for the
+                                // software rounding, philox4x32_10 for sr_hw)
+    int sr_hw;                  // 1: NVFP4_SR_HW random-bit layout (hardware conversion)
     // 2D transposed emit (optional)
     uint8_t* codes_t;           // [k x rows/2]
     uint8_t* scales_t;
@@ -325,7 +327,9 @@ __device__ __forceinline__ void init_rtab(float* rtab, float s_enc) {
 
 // Encode one 16-element block.  amax_bits: the block's max |value| as float
 // bits when already known (raw bf16 input), or ~0u to compute it here.
-template <bool RHT, bool SR>
+// HW: the stochastic rounding's random-bit layout, 1 = NVFP4_SR_HW, 0 =
+// NVFP4_SR, -1 = taken from a.sr_hw at run time.
+template <bool RHT, bool SR, int HW = -1>
 __device__ __forceinline__ void encode_block16(float* v, float s_enc, const float* rtab, uint64_t idx0,
                                                const QuantArgs& a, uint32_t* sb_out,
                                                uint32_t* code_lo, uint32_t* code_hi,
@@ -346,7 +350,12 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
 #pragma unroll
     for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], r_b);
     if (SR) {
-        e2m1x16_sr(v, sr_words16(idx0 >> 4, a.stream_id, a.sr_key), code_lo, code_hi);
+        if (HW == 1 || (HW < 0 && a.sr_hw)) {
+            e2m1x16_sr(v, sr_words16(idx0 >> 4, a.stream_id, a.sr_key), code_lo, code_hi);
+        } else {
+            *code_lo = e2m1x8_sr(v, sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+            *code_hi = e2m1x8_sr(v + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+        }
     } else {
         *code_lo = e2m1x8_rne(v);
         *code_hi = e2m1x8_rne(v + 8);
@@ -355,7 +364,7 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
 
 // Non-transposed view: thread item = (row, group of 4 blocks).
 template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads, RHT && SR ? 2 : 3) k_quant1d_rows(const QuantArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, SR ? 2 : 3) k_quant1d_rows(const QuantArgs a) {
     __shared__ float rtab[128];
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
@@ -637,13 +646,13 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                 uint32_t lo = 0, hi = 0;
                 if (row_ok && b < nblk) {
                     const int64_t c0 = g * 64 + b * 16;
-                    if (a.idx_transposed) {
+                    if (a.idx_transposed && a.sr_hw) {
                         // index in the transposed logical layout: (r, c) -> c * rows + r;
                         // rows is a multiple of 16, so every element of the strip
                         // takes the same word ((r % 16) / 4) and element position
                         // (r % 4) of its own Philox block.
                         const int wsel = (r >> 2) & 3, pos = r & 3;
-    #pragma unroll
+#pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
                             const uint4 rb = sr_words16(idx >> 4, a.stream_id, a.sr_key);
@@ -652,9 +661,28 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                             if (j < 8) lo |= q << (4 * j);
                             else hi |= q << (4 * (j - 8));
                         }
-                    } else {
+                    } else if (a.idx_transposed) {
+                        // every element of the strip takes the same slice (r & 7)
+                        // of its own Philox block
+                        const uint32_t sel = (r & 1) ? SR_SEL_HI : SR_SEL_LO;
+                        const uint32_t wsel = (uint32_t)(r & 7) >> 1;
+                        float gv[16];
+#pragma unroll
+                        for (int j = 0; j < 16; ++j) {
+                            const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
+                            const uint4 rb = sr_rp8(idx >> 3, a.stream_id, a.sr_key);
+                            const uint32_t w = wsel == 0 ? rb.x : wsel == 1 ? rb.y : wsel == 2 ? rb.z : rb.w;
+                            gv[j] = sr_grid_value(v[b][j], w, sel);
+                        }
+                        lo = e2m1x8_rne(gv);
+                        hi = e2m1x8_rne(gv + 8);
+                    } else if (a.sr_hw) {
                         const uint64_t idx0 = (uint64_t)(r * a.k + c0);
                         e2m1x16_sr(v[b], sr_words16(idx0 >> 4, a.stream_id, a.sr_key), &lo, &hi);
+                    } else {
+                        const uint64_t idx0 = (uint64_t)(r * a.k + c0);
+                        lo = e2m1x8_sr(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+                        hi = e2m1x8_sr(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
                     }
                 }
                 cw[2 * b] = lo;

@@ -11,7 +11,11 @@ pre-training":
     operand W^T come from one encoding (bullet 4);
   * the 16-point random Hadamard transform on the wgrad inputs dY^T and X^T,
     one sign mask shared by both (bullet 3);
-  * stochastic rounding of dY (bullet 5); X and W round to nearest.
+  * stochastic rounding of dY (bullet 5); X and W round to nearest.  The
+    rounding mode of dY is NVFP4_SR (16 independent Philox bits per element)
+    or NVFP4_SR_HW (the same rule with the random bits in the layout of the
+    hardware FP4 stochastic-rounding conversion, 32 bits per 4 elements;
+    faster).
 
 X and dY are each read once for both of their operands (nvfp4_amax_dual /
 nvfp4_quantize_dual).  The forward saves the quantised X^T and W^T for the
@@ -30,7 +34,7 @@ import math
 
 import torch
 
-from . import (NVFP4_RNE, NVFP4_SR, QTensor, nvfp4_amax, nvfp4_amax_dual, nvfp4_gemm,
+from . import (NVFP4_RNE, NVFP4_SR, NVFP4_SR_HW, QTensor, nvfp4_amax, nvfp4_amax_dual, nvfp4_gemm,
                nvfp4_quantize_2d, nvfp4_quantize_dual, nvfp4_rht_mask_from_seed)
 
 # Philox stream ids of the two stochastic-rounding draws of a step
@@ -49,10 +53,11 @@ class NVFP4LinearFunction(torch.autograd.Function):
     """y = x w^T with x [tokens x in], w [out x in] (bf16, CUDA); returns y bf16.
 
     seed selects the Philox stream of this call's stochastic rounding; rht_mask
-    the 16-bit Hadamard sign mask (one per call, shared by dY^T and X^T)."""
+    the 16-bit Hadamard sign mask (one per call, shared by dY^T and X^T);
+    sr_round the rounding mode of dY (NVFP4_SR or NVFP4_SR_HW)."""
 
     @staticmethod
-    def forward(ctx, x: torch.Tensor, w: torch.Tensor, seed: int, rht_mask: int):
+    def forward(ctx, x: torch.Tensor, w: torch.Tensor, seed: int, rht_mask: int, sr_round: int = NVFP4_SR):
         tokens, k_in = x.shape
         k_out = w.shape[0]
         _check_shapes(tokens, k_in, k_out)
@@ -68,7 +73,7 @@ class NVFP4LinearFunction(torch.autograd.Function):
         y = torch.empty((tokens, k_out), dtype=torch.bfloat16, device=x.device)
         nvfp4_gemm(qx, qw, y)
         ctx.q = (qxt, qwt)
-        ctx.seed, ctx.rht_mask = seed, rht_mask
+        ctx.seed, ctx.rht_mask, ctx.sr_round = seed, rht_mask, sr_round
         return y
 
     @staticmethod
@@ -80,14 +85,14 @@ class NVFP4LinearFunction(torch.autograd.Function):
         amax = torch.empty((2,), dtype=torch.float32, device=dy.device)
         qdy, qdyt = QTensor(tokens, k_out), QTensor(k_out, tokens)
         nvfp4_amax_dual(dy, ctx.rht_mask, amax[0:1], amax[1:2])
-        nvfp4_quantize_dual(dy, amax[0:1], NVFP4_SR, ctx.seed, STREAM_DGRAD, qdy, ctx.rht_mask, amax[1:2],
-                            NVFP4_SR, ctx.seed, STREAM_WGRAD, qdyt)
+        nvfp4_quantize_dual(dy, amax[0:1], ctx.sr_round, ctx.seed, STREAM_DGRAD, qdy, ctx.rht_mask, amax[1:2],
+                            ctx.sr_round, ctx.seed, STREAM_WGRAD, qdyt)
         dx = torch.empty((tokens, k_in), dtype=torch.bfloat16, device=dy.device)
         dw = torch.empty((k_out, k_in), dtype=torch.bfloat16, device=dy.device)
         nvfp4_gemm(qdy, qwt, dx)                  # dX = dY W
         nvfp4_gemm(qdyt, qxt, dw)                 # dW = dY^T X, k = tokens, RHT on both
         ctx.q = None
-        return dx, dw, None, None
+        return dx, dw, None, None, None
 
 
 class NVFP4Linear(torch.nn.Module):
@@ -100,10 +105,13 @@ class NVFP4Linear(torch.nn.Module):
     independent rounding noise while a run stays reproducible."""
 
     def __init__(self, in_features: int, out_features: int, *, precision: str = "nvfp4",
-                 seed: int = 0, device="cuda", dtype=torch.bfloat16):
+                 seed: int = 0, device="cuda", dtype=torch.bfloat16, sr_round: int = NVFP4_SR):
         super().__init__()
         if precision not in ("nvfp4", "bf16"):
             raise ValueError("precision must be 'nvfp4' or 'bf16'")
+        if sr_round not in (NVFP4_SR, NVFP4_SR_HW):
+            raise ValueError("sr_round must be NVFP4_SR or NVFP4_SR_HW")
+        self.sr_round = sr_round
         self.in_features, self.out_features = in_features, out_features
         self.precision = precision
         self.seed = seed
@@ -127,7 +135,7 @@ class NVFP4Linear(torch.nn.Module):
             s = self.call_seed()
             # mask 0 would switch the transform off in the C ABI: use 1 instead
             mask = nvfp4_rht_mask_from_seed(s ^ 0x5EED) or 1
-            y = NVFP4LinearFunction.apply(x2.to(torch.bfloat16), self.weight, s, mask)
+            y = NVFP4LinearFunction.apply(x2.to(torch.bfloat16), self.weight, s, mask, self.sr_round)
         self.calls += 1
         return y.reshape(*lead, self.out_features)
 

@@ -81,6 +81,8 @@ def lib():
             L.orc_rht_mask_from_seed.argtypes = [ctypes.c_uint64]
             L.orc_sr_r16_of_word.restype = ctypes.c_uint32
             L.orc_sr_r16_of_word.argtypes = [ctypes.c_uint32, ctypes.c_int]
+            L.orc_sr_bits16_hw.restype = ctypes.c_uint32
+            L.orc_sr_bits16_hw.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
             L.orc_sr_bits16.restype = ctypes.c_uint32
             L.orc_sr_bits16.argtypes = [ctypes.c_uint64, ctypes.c_uint64, ctypes.c_uint64]
             L.orc_rht16.restype = None
@@ -162,9 +164,9 @@ def e2m1_rne(v: float) -> int:
     return lib().orc_e2m1_rne(v)
 
 
-def e2m1_sr(v: float, r16: int) -> int:
-    """Stochastic E2M1 code of v: up iff floor(frac * 2^16) + r16 >= 2^16."""
-    return lib().orc_e2m1_sr(v, r16)
+def e2m1_sr(v: float, u16: int) -> int:
+    """Stochastic E2M1 code of v: up iff u16 < floor(frac * 2^16)."""
+    return lib().orc_e2m1_sr(v, u16)
 
 
 def e4m3_value(code: int) -> float:
@@ -191,13 +193,18 @@ def rht_mask_from_seed(seed: int) -> int:
     return lib().orc_rht_mask_from_seed(seed)
 
 
+def sr_bits16(seed: int, stream_id: int, idx: int) -> int:
+    return lib().orc_sr_bits16(seed, stream_id, idx)
+
+
 def sr_r16_of_word(w: int, p: int) -> int:
-    """16-bit random integer of element p (0..3) of the 32-bit word w."""
+    """Second layout: integer r of element p (0..3) of the 32-bit word w."""
     return lib().orc_sr_r16_of_word(w, p)
 
 
-def sr_bits16(seed: int, stream_id: int, idx: int) -> int:
-    return lib().orc_sr_bits16(seed, stream_id, idx)
+def sr_bits16_hw(seed: int, stream_id: int, idx: int) -> int:
+    """Second layout: the u16 (= 65535 - r) of element idx."""
+    return lib().orc_sr_bits16_hw(seed, stream_id, idx)
 
 
 def rht16(x, mask: int) -> np.ndarray:
@@ -279,8 +286,11 @@ def _row_chunks(rows: int, threads: int, align: int):
 def quantize(x: np.ndarray, *, transposed: bool = False, rht_mask: int = 0, block2d: bool = False,
              amax_v: float | None = None, sr: bool = False, seed: int = 0, stream_id: int = 0,
              threads: int | None = None, rows_range=None, ranges=None,
-             swizzle: bool = True) -> Quantized:
+             swizzle: bool = True, sr_hw: bool = False) -> Quantized:
     """Steps 1-6: quantise the logical operand of bf16 array x.
+
+    sr: stochastic rounding with 16 independent random bits per element;
+    sr_hw (with sr): the second random-bit layout (sr_bits16_hw).
 
     amax_v defaults to ``amax(x, transposed, rht_mask)``.  ``rows_range`` (or
     a list ``ranges`` of (lo, hi)) restricts the rows computed -- the other
@@ -305,7 +315,7 @@ def quantize(x: np.ndarray, *, transposed: bool = False, rht_mask: int = 0, bloc
 
     def run(ch):
         return lib().orc_quantize(_p(x, ctypes.c_uint16), rows, k, ld, int(transposed), rht_mask,
-                                  int(block2d), amax_v, int(sr), seed, stream_id, ch[0], ch[1],
+                                  int(block2d), amax_v, (2 if sr_hw else 1) if sr else 0, seed, stream_id, ch[0], ch[1],
                                   _p(codes, ctypes.c_uint8), _p(scales, ctypes.c_uint8))
 
     if len(chunks) == 1:

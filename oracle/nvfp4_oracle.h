@@ -49,13 +49,14 @@ uint16_t orc_f32_to_bf16_rne(float f);
 /* ---- Philox4x32-10 [PHX] ------------------------------------------------ */
 void     orc_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
 uint32_t orc_rht_mask_from_seed(uint64_t seed);    /* low 16 bits of word 0 of Philox(ctr=0, key=seed) */
-/* 16-bit random integer of element p (0..3) of a 32-bit random word */
-uint32_t orc_sr_r16_of_word(uint32_t w, int p);
-/* 16-bit random integer for element index idx of a quantised operand */
+/* 16-bit random slice for element index idx of a quantised operand */
 uint32_t orc_sr_bits16(uint64_t seed, uint64_t stream_id, uint64_t idx);
-/* stochastic E2M1 rounding of v given its 16-bit random integer:
- * up iff floor(frac * 2^16) + r16 >= 2^16 */
-uint8_t  orc_e2m1_sr(float v, uint32_t r16);
+/* second layout (rounding mode 2): integer r of element p (0..3) of a
+ * 32-bit word, and the u16 = 65535 - r of element idx */
+uint32_t orc_sr_r16_of_word(uint32_t w, int p);
+uint32_t orc_sr_bits16_hw(uint64_t seed, uint64_t stream_id, uint64_t idx);
+/* stochastic E2M1 rounding of v given its 16 random bits: up iff u16 < floor(frac * 2^16) */
+uint8_t  orc_e2m1_sr(float v, uint32_t u16);
 
 /* ---- random Hadamard transform, 16 points ------------------------------ */
 void orc_rht16(const float in[16], uint32_t mask, float out[16]);
@@ -76,7 +77,8 @@ int   orc_global_scale(float amax, float* s_enc);
 /* Quantise logical rows [row_begin, row_end) of the bf16 operand.
  *  block2d: 0 -> 1x16 blocks along k; 1 -> 16x16 blocks (row_begin/row_end
  *           must then be multiples of 16, except row_end == rows).
- *  round:   0 -> RNE, 1 -> stochastic (seed, stream_id).
+ *  round:   0 -> RNE, 1 -> stochastic (seed, stream_id), 2 -> stochastic with
+ *           the second random-bit layout (orc_sr_bits16_hw).
  *  codes:   [rows x k/2] bytes (full-size buffer; only the range is written)
  *  scales:  plain [rows x k/16] E4M3 bytes (full-size buffer)
  * Returns 0, or -1 if amax is not finite.                                  */

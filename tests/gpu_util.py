@@ -20,13 +20,13 @@ def dev_bf16(a: np.ndarray, ld: int | None = None) -> torch.Tensor:
 
 
 def gpu_quantize(nv, x_dev, *, transposed=False, mask=0, block2d=False, sr=False, seed=0, sid=0,
-                 own_amax=False, emit_t=False):
+                 own_amax=False, emit_t=False, sr_hw=False):
     """Quantise through the C ABI; returns (q, q_t or None, amax tensor or None)."""
     r, c = x_dev.shape
     rows, k = (c, r) if transposed else (r, c)
     out = nv.QTensor(rows, k, block2d)
     out_t = nv.QTensor(k, rows, True) if emit_t else None
-    rnd = nv.NVFP4_SR if sr else nv.NVFP4_RNE
+    rnd = (nv.NVFP4_SR_HW if sr_hw else nv.NVFP4_SR) if sr else nv.NVFP4_RNE
     amax = None if own_amax else nv.nvfp4_amax(x_dev, mask, transposed=transposed)
     if mask:
         nv.nvfp4_rht_quantize(x_dev, mask, amax, rnd, seed, sid, out, transposed=transposed)

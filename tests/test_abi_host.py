@@ -84,6 +84,7 @@ def test_validation_rejects_bad_calls(nv):
     assert L.nvfp4_quantize_1d(good, None, 0, 0, 0, ctypes.byref(_q(nv, 16, 64)), None) == nv.NVFP4_ERR_INVALID_ARG
     assert L.nvfp4_quantize_1d(good, None, 0, 0, 0, None, None) == nv.NVFP4_ERR_INVALID_ARG
     assert L.nvfp4_quantize_1d(good, None, 7, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
+    assert L.nvfp4_quantize_1d(good, None, 3, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
     # amax aliasing the output global scale
     assert L.nvfp4_quantize_1d(good, ctypes.c_void_p(0x3000), 0, 0, 0, ctypes.byref(q), None) == nv.NVFP4_ERR_INVALID_ARG
     # RHT mask out of range / zero for rht_quantize
