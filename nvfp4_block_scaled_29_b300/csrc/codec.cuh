@@ -119,7 +119,7 @@ __device__ __forceinline__ uint4 sr_words16(uint64_t g, uint64_t stream_id, cons
                          key);
 }
 
-// ------------------------------------- stochastic E2M1, software (NVFP4_SR) --
+// ---------------------------------------------- stochastic E2M1 (NVFP4_SR) --
 // Philox4x32-10 with every output word complemented, with the round keys
 // precomputed: key[2r], key[2r+1] = (k0 + r * 0x9E3779B9, k1 + r *
 // 0xBB67AE85) for rounds r = 0..8, and the complements of the round-9 keys
@@ -147,47 +147,37 @@ __device__ __forceinline__ uint4 sr_rp8(uint64_t g, uint64_t stream_id, const ui
                              key);
 }
 
-// dp2a selectors: rp * 64 from the low (SEL_LO) or high (SEL_HI) half-word.
-constexpr uint32_t SR_SEL_LO = 0x40u, SR_SEL_HI = 0x4000u;
-
-// Stochastic E2M1 rounding of one value v = x * r_b (rounding mode
-// NVFP4_SR: 16 independent random bits per element), realised as "add random
-// bits below the kept precision, then truncate".  With lo <= |v| < hi the
-// neighbouring grid values, the rule is: round up iff u16 < F = floor(frac *
-// 2^16), frac = (|v| - lo) / (hi - lo).
-//  * On [1, 16) the E2M1 grid (with 8, 12, 16 beyond the top, all of which
-//    saturate to 6) is 2^e x {1, 1.5}: the kept bits are the exponent and
-//    mantissa bit 22, and mantissa bits 21..6 hold F.  Adding rp = 65535 - u16
-//    at bit 6 carries into the kept bits exactly when F > u16.
-//  * Below 1 (grid 0, 0.5, 1: spacing 0.5) |v| is first moved to [1, 2) by a
-//    round-toward-zero add of c = 1.0 (the truncation is below 2^-17, so F is
-//    unchanged) and moved back by an exact subtraction of c.  For |v| >= 1,
-//    c = 0 and both adds are exact no-ops.
-//  * |v| < 16 always holds (|x| <= amax_b and s_b is at least 2/3 of
-//    amax_b * S_enc / 6 whenever it is non-zero), so the add never reaches
-//    the exponent field's top.
-// dp2a forms rp * 64 + bits(|v| + c) from the selected half-word of the
-// complemented Philox word in one instruction.  The result is the chosen
-// grid value, sign kept (the RNE conversion then returns its code unchanged).
-__device__ __forceinline__ float sr_grid_value(float v, uint32_t rp_word, uint32_t sel) {
-    const float a = fabsf(v);
-    float c;
-    asm("set.lt.f32.f32 %0, %1, 0f3F800000;" : "=f"(c) : "f"(a));
-    const float a2 = __fadd_rz(a, c);
-    uint32_t qb;
-    asm("dp2a.lo.u32.u32 %0, %1, %2, %3;" : "=r"(qb) : "r"(rp_word), "r"(sel), "r"(__float_as_uint(a2)));
-    const float q = __fsub_rn(__uint_as_float(qb & 0xFFC00000u), c);
-    return __uint_as_float(__float_as_uint(q) | (__float_as_uint(v) & 0x80000000u));
+// NVFP4_SR on the hardware stochastic-rounding conversion, two values at a
+// time.  The conversion (cvt.rs.satfinite.e2m1x4.f32, operands a, b, e, f)
+// rounds the value in operand position f with r = L = (byte 2, byte 0) of its
+// random word and the value in position b with r = H = (byte 3, byte 1), up
+// iff floor(frac * 2^16) + r >= 2^16; positions a and e get 0, which converts
+// to code 0 whatever the bits.  A byte permutation of the complemented Philox
+// word (halves rp = 65535 - u16 of the two elements) puts the even element's
+// rp in L and the odd element's in H, so each element rounds up iff
+// u16 < floor(frac * 2^16) with its own 16 bits: exactly the NVFP4_SR rule.
+// Returns the byte code(v_even) | code(v_odd) << 4.  A single value takes its
+// half-word's position (f for the low half, b for the high) with 0 in the other
+// (e2m1_sr_rp_at).
+__device__ __forceinline__ uint32_t e2m1x2_sr_rp(float v_even, float v_odd, uint32_t rp_word) {
+    const uint32_t rb = __byte_perm(rp_word, 0u, 0x3120u);
+    uint16_t d;
+    asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
+        : "=h"(d)
+        : "f"(0.0f), "f"(v_odd), "f"(0.0f), "f"(v_even), "r"(rb));
+    const uint32_t x = d;                     // code(v_even) in bits 0-3, code(v_odd) in bits 8-11
+    return (x | (x >> 4)) & 0xFFu;
 }
 
-// Eight values -> eight SR codes (element 0 in the lowest nibble), rp = the
-// complemented Philox block of these 8 elements.
-__device__ __forceinline__ uint32_t e2m1x8_sr(const float* v, uint4 rp) {
-    const uint32_t w[4] = {rp.x, rp.y, rp.z, rp.w};
-    float g[8];
-#pragma unroll
-    for (int j = 0; j < 8; ++j) g[j] = sr_grid_value(v[j], w[j >> 1], (j & 1) ? SR_SEL_HI : SR_SEL_LO);
-    return e2m1x8_rne(g);
+__device__ __forceinline__ uint32_t e2m1_sr_rp_at(float v, uint32_t rp_word, bool high_half) {
+    return high_half ? (e2m1x2_sr_rp(0.0f, v, rp_word) >> 4) : (e2m1x2_sr_rp(v, 0.0f, rp_word) & 0xFu);
+}
+
+// Eight values -> eight NVFP4_SR codes (element 0 in the lowest nibble), rp =
+// the complemented Philox block of these 8 elements (sr_rp8).
+__device__ __forceinline__ uint32_t e2m1x8_sr_cvt(const float* v, uint4 rp) {
+    return e2m1x2_sr_rp(v[0], v[1], rp.x) | (e2m1x2_sr_rp(v[2], v[3], rp.y) << 8) |
+           (e2m1x2_sr_rp(v[4], v[5], rp.z) << 16) | (e2m1x2_sr_rp(v[6], v[7], rp.w) << 24);
 }
 
 // --------------------------- stochastic E2M1, hardware layout (NVFP4_SR_HW) --

@@ -353,8 +353,8 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
         if (HW == 1 || (HW < 0 && a.sr_hw)) {
             e2m1x16_sr(v, sr_words16(idx0 >> 4, a.stream_id, a.sr_key), code_lo, code_hi);
         } else {
-            *code_lo = e2m1x8_sr(v, sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
-            *code_hi = e2m1x8_sr(v + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+            *code_lo = e2m1x8_sr_cvt(v, sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+            *code_hi = e2m1x8_sr_cvt(v + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
         }
     } else {
         *code_lo = e2m1x8_rne(v);
@@ -664,25 +664,23 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                     } else if (a.idx_transposed) {
                         // every element of the strip takes the same slice (r & 7)
                         // of its own Philox block
-                        const uint32_t sel = (r & 1) ? SR_SEL_HI : SR_SEL_LO;
                         const uint32_t wsel = (uint32_t)(r & 7) >> 1;
-                        float gv[16];
 #pragma unroll
                         for (int j = 0; j < 16; ++j) {
                             const uint64_t idx = (uint64_t)((c0 + j) * a.rows + r);
                             const uint4 rb = sr_rp8(idx >> 3, a.stream_id, a.sr_key);
                             const uint32_t w = wsel == 0 ? rb.x : wsel == 1 ? rb.y : wsel == 2 ? rb.z : rb.w;
-                            gv[j] = sr_grid_value(v[b][j], w, sel);
+                            const uint32_t q = e2m1_sr_rp_at(v[b][j], w, (r & 1) != 0);
+                            if (j < 8) lo |= q << (4 * j);
+                            else hi |= q << (4 * (j - 8));
                         }
-                        lo = e2m1x8_rne(gv);
-                        hi = e2m1x8_rne(gv + 8);
                     } else if (a.sr_hw) {
                         const uint64_t idx0 = (uint64_t)(r * a.k + c0);
                         e2m1x16_sr(v[b], sr_words16(idx0 >> 4, a.stream_id, a.sr_key), &lo, &hi);
                     } else {
                         const uint64_t idx0 = (uint64_t)(r * a.k + c0);
-                        lo = e2m1x8_sr(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
-                        hi = e2m1x8_sr(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+                        lo = e2m1x8_sr_cvt(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+                        hi = e2m1x8_sr_cvt(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
                     }
                 }
                 cw[2 * b] = lo;
