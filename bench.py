@@ -462,7 +462,8 @@ def main():
                      "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s x 6 (nominal dense FP4:BF16)"},
         "roofline_quantize": {"bound": "hbm", "achieved": quant_gbs, "peak": hbm_peak, "unit": "GB/s",
                               "frac": quant_gbs / hbm_peak,
-                              "traffic": traffic.get("quant_dual_dy" if args.path == "dual" else "quant_sr_dy"),
+                              "traffic": traffic.get(("quant_dual_dy_hw" if args.sr == "hw" else "quant_dual_dy")
+                                                     if args.path == "dual" else "quant_sr_dy"),
                               "traffic_note": ("dual-axis SR quantise of dY (one launch)" if args.path == "dual"
                                                else "1x16 SR quantise of dY (one launch)"),
                               "peak_source": f"{peak_src} HBM copy"},
