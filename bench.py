@@ -118,9 +118,16 @@ class ClockSampler:
 class Step:
     """Device buffers and the launch sequence of one linear-layer step."""
 
-    def __init__(self, nv, torch, host, path: str = "dual", sr_round=None):
+    def __init__(self, nv, torch, host, path: str = "dual", sr_round=None, streams: int = 1):
         self.nv, self.torch = nv, torch
         self.sr_round = nv.NVFP4_SR if sr_round is None else sr_round
+        # forward: the W chain (amax, 16x16 quantise) runs on a second stream beside
+        # the X chain and joins the main stream before the forward GEMM
+        self.side = torch.cuda.Stream() if (streams == 2 and path == "dual") else None
+        self.fork = torch.cuda.Event()
+        self.join = torch.cuda.Event()
+        self.ev_start = torch.cuda.Event(enable_timing=True)
+        self.ev_end = torch.cuda.Event(enable_timing=True)
         dev = "cuda"
         self.stream = torch.cuda.current_stream()
         self.x = torch.empty((TOKENS, HIDDEN), dtype=torch.bfloat16, device=dev)
@@ -173,11 +180,13 @@ class Step:
         gemm_dgrad = ("gemm_dgrad", lambda: nv.nvfp4_gemm(self.qdy, self.qwt, self.dx), 0, True)
         gemm_wgrad = ("gemm_wgrad", lambda: nv.nvfp4_gemm(self.qdyt, self.qxt, self.dw), 0, True)
         if path == "dual":
+            # the W chain first (on the side stream when there is one), then the X chain
             return [
+                *fwd_w,
                 ("amax_dual_x", lambda: nv.nvfp4_amax_dual(self.x, self.mask, a[0:1], a[4:5]), x * B_AMAX, False),
                 ("quant_dual_x", lambda: nv.nvfp4_quantize_dual(self.x, a[0:1], rne, 0, 0, self.qx, self.mask,
                                                                 a[4:5], rne, 0, 0, self.qxt), x * B_QDUAL, False),
-                *fwd_w, gemm_fwd,
+                gemm_fwd,
                 ("amax_dual_dy", lambda: nv.nvfp4_amax_dual(self.dy, self.mask, a[2:3], a[3:4]), dy * B_AMAX, False),
                 ("quant_dual_dy", lambda: nv.nvfp4_quantize_dual(self.dy, a[2:3], sr, SR_SEED, 1, self.qdy, self.mask,
                                                                  a[3:4], sr, SR_SEED, 2, self.qdyt), dy * B_QDUAL, False),
@@ -199,13 +208,30 @@ class Step:
             gemm_wgrad]
 
     def run(self, timed: bool):
-        ev = self.ev
-        for j, (_, call, _, _) in enumerate(self.seq):
-            if timed:
-                ev[2 * j].record()
-            call()
-            if timed:
-                ev[2 * j + 1].record()
+        """Enqueue one step.  With a side stream, the W-chain launches (amax_w,
+        q2d_w) go to it after a fork event from the main stream, and the main
+        stream waits for them before the forward GEMM; the step is timed by
+        events on the main stream around everything."""
+        torch, ev = self.torch, self.ev
+        main = torch.cuda.current_stream()
+        if timed:
+            self.ev_start.record(main)
+        if self.side is not None:
+            self.fork.record(main)
+            self.side.wait_event(self.fork)
+        for j, (name, call, _, _) in enumerate(self.seq):
+            s = self.side if (self.side is not None and name in ("amax_w", "q2d_w")) else main
+            if name == "gemm_fwd" and self.side is not None:
+                self.join.record(self.side)
+                main.wait_event(self.join)
+            with torch.cuda.stream(s):
+                if timed:
+                    ev[2 * j].record(s)
+                call()
+                if timed:
+                    ev[2 * j + 1].record(s)
+        if timed:
+            self.ev_end.record(main)
 
     def phase_times(self):
         """ms of each launch of the last timed step."""
@@ -331,6 +357,9 @@ def main():
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP4 comparison timing")
     ap.add_argument("--path", default="dual", choices=["dual", "separate"],
                     help="dual: X and dY read once each for both operands; separate: one call per operand")
+    ap.add_argument("--streams", type=int, default=1, choices=[1, 2],
+                    help="2: the forward W chain (amax, 16x16 quantise) on a second stream beside the X chain "
+                         "(dual path only; the persistent kernels each fill the GPU, so the gain is small)")
     ap.add_argument("--sr", default="philox16", choices=["philox16", "hw"],
                     help="rounding of dY: philox16 = NVFP4_SR (16 independent Philox bits per element), "
                          "hw = NVFP4_SR_HW (random bits in the hardware SR conversion's layout)")
@@ -359,7 +388,7 @@ def main():
     host["y"] = torch.empty((TOKENS, FFN), dtype=torch.int16).pin_memory()
     host["dx"] = torch.empty((TOKENS, HIDDEN), dtype=torch.int16).pin_memory()
     host["dw"] = torch.empty((FFN, HIDDEN), dtype=torch.int16).pin_memory()
-    step = Step(nv, torch, host, args.path, nv.NVFP4_SR_HW if args.sr == "hw" else nv.NVFP4_SR)
+    step = Step(nv, torch, host, args.path, nv.NVFP4_SR_HW if args.sr == "hw" else nv.NVFP4_SR, args.streams)
     gemm_idx = [j for j, p in enumerate(step.seq) if p[3]]
     quant_idx = [j for j, p in enumerate(step.seq) if not p[3]]
     torch.cuda.synchronize()
@@ -395,7 +424,7 @@ def main():
             step.run(timed=True)
             torch.cuda.synchronize()
             ph = step.phase_times()
-            step_ms.append(step.ev[0].elapsed_time(step.ev[-1]))
+            step_ms.append(step.ev_start.elapsed_time(step.ev_end))
             gemm_ms.extend(ph[j] for j in gemm_idx)
             quant_ms.append(sum(ph[j] for j in quant_idx))
         barrier()
@@ -449,6 +478,8 @@ def main():
         "data": "synthetic (seeded N(0,1)+outliers, N(0,0.02^2), 1e-3*t3)",
         "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
                    "path": args.path,
+                   "streams": ("2: forward W chain on a second stream beside the X chain; phase_ms overlap"
+                               if step.side is not None else "1"),
                    "sr": ("NVFP4_SR_HW: random bits in the hardware SR conversion's layout" if args.sr == "hw"
                           else "NVFP4_SR: 16 independent Philox4x32-10 bits per element"),
                    "l2": "flushed before each step (256 MiB device write, untimed)",

@@ -41,6 +41,18 @@ from . import (NVFP4_RNE, NVFP4_SR, NVFP4_SR_HW, QTensor, nvfp4_amax, nvfp4_amax
 STREAM_DGRAD, STREAM_WGRAD = 1, 2
 
 
+_SIDE_STREAMS: dict = {}
+
+
+def _side_stream(device) -> "torch.cuda.Stream":
+    """One side stream per device, for the weight's quantisation."""
+    idx = torch.device(device).index
+    idx = torch.cuda.current_device() if idx is None else idx
+    if idx not in _SIDE_STREAMS:
+        _SIDE_STREAMS[idx] = torch.cuda.Stream(device=idx)
+    return _SIDE_STREAMS[idx]
+
+
 def _check_shapes(tokens: int, k_in: int, k_out: int):
     # every GEMM reduction dimension (k_in: fprop, k_out: dgrad, tokens:
     # wgrad) must be a multiple of 32
@@ -65,11 +77,23 @@ class NVFP4LinearFunction(torch.autograd.Function):
         w = w.contiguous()
         amax = torch.empty((3,), dtype=torch.float32, device=x.device)
         qx, qxt = QTensor(tokens, k_in), QTensor(k_in, tokens)
+        qw, qwt = QTensor(k_out, k_in, True), QTensor(k_in, k_out, True)
+        # W's amax and 16x16 quantise run on a side stream beside X's
+        main, side = torch.cuda.current_stream(x.device), _side_stream(x.device)
+        fork = torch.cuda.Event()
+        fork.record(main)
+        side.wait_event(fork)
+        with torch.cuda.stream(side):
+            nvfp4_amax(w, 0, amax[2:3])
+            nvfp4_quantize_2d(w, amax[2:3], NVFP4_RNE, 0, 0, qw, qwt)
+        # buffers made on the main stream and used on the side stream
+        for t in (w, amax, qw.codes, qw.scales, qw.global_scale, qwt.codes, qwt.scales, qwt.global_scale):
+            t.record_stream(side)
         nvfp4_amax_dual(x, rht_mask, amax[0:1], amax[1:2])
         nvfp4_quantize_dual(x, amax[0:1], NVFP4_RNE, 0, 0, qx, rht_mask, amax[1:2], NVFP4_RNE, 0, 0, qxt)
-        qw, qwt = QTensor(k_out, k_in, True), QTensor(k_in, k_out, True)
-        nvfp4_amax(w, 0, amax[2:3])
-        nvfp4_quantize_2d(w, amax[2:3], NVFP4_RNE, 0, 0, qw, qwt)
+        join = torch.cuda.Event()
+        join.record(side)
+        main.wait_event(join)
         y = torch.empty((tokens, k_out), dtype=torch.bfloat16, device=x.device)
         nvfp4_gemm(qx, qw, y)
         ctx.q = (qxt, qwt)
