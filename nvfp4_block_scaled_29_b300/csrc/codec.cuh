@@ -222,26 +222,61 @@ __device__ __forceinline__ uint32_t e2m1_sr_at(float v, uint32_t w, int p) {
 // Sign multipliers of the diagonal: s[j] = -1 where bit j of the 16-bit mask
 // is set, else +1.  Passed by value as a kernel parameter, so that the
 // butterflies take them straight from the constant bank.
+// The butterflies run on packed two-lane FP32 operations (add/sub/mul/fma
+// .f32x2: per lane the same IEEE RN result as the scalar instruction) over
+// register pairs P[k] = (v[k], v[k + 8]), k = 0..7: stages h = 1, 2, 4 combine
+// pair k with pair k + h, so both lanes of a packed operation belong to the
+// same stage.  p[k] = (s_k, s_{k+8}) and n[k] = -p[k] are the signs in that
+// layout.
 struct RhtSigns {
-    float s[16];
+    float2 p[8];
+    float2 n[8];
 };
 
+__device__ __forceinline__ float2 fsub2_rn(float2 a, float2 b) {
+    float2 d;
+    asm("{\n\t.reg .b64 ra, rb, rd;\n\tmov.b64 ra, {%2, %3};\n\tmov.b64 rb, {%4, %5};\n\t"
+        "sub.rn.f32x2 rd, ra, rb;\n\tmov.b64 {%0, %1}, rd;\n\t}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
 __device__ __forceinline__ void rht16_first3(float* v, const RhtSigns& sg) {
+    float2 P[8];
 #pragma unroll
-    for (int i = 0; i < 16; i += 2) {
-        const float a = __fmul_rn(v[i], sg.s[i]), b = v[i + 1];
-        v[i] = __fmaf_rn(sg.s[i + 1], b, a);
-        v[i + 1] = __fmaf_rn(-sg.s[i + 1], b, a);
+    for (int k = 0; k < 8; ++k) P[k] = make_float2(v[k], v[k + 8]);
+#pragma unroll
+    for (int k = 0; k < 8; k += 2) {
+        const float2 a = __fmul2_rn(P[k], sg.p[k]), b = P[k + 1];
+        P[k] = __ffma2_rn(sg.p[k + 1], b, a);
+        P[k + 1] = __ffma2_rn(sg.n[k + 1], b, a);
     }
 #pragma unroll
     for (int h = 2; h < 8; h <<= 1) {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            if (i & h) continue;
-            const float a = v[i], b = v[i + h];
-            v[i] = __fadd_rn(a, b);
-            v[i + h] = __fsub_rn(a, b);
+        for (int k = 0; k < 8; ++k) {
+            if (k & h) continue;
+            const float2 a = P[k], b = P[k + h];
+            P[k] = __fadd2_rn(a, b);
+            P[k + h] = fsub2_rn(a, b);
         }
+    }
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        v[k] = P[k].x;
+        v[k + 8] = P[k].y;
+    }
+}
+
+// v[j] = fp32(v[j] * f) for all 16 elements, on packed pairs (v[k], v[k + 8]).
+__device__ __forceinline__ void scale16(float* v, float f) {
+    const float2 ff = make_float2(f, f);
+#pragma unroll
+    for (int k = 0; k < 8; ++k) {
+        const float2 r = __fmul2_rn(make_float2(v[k], v[k + 8]), ff);
+        v[k] = r.x;
+        v[k + 8] = r.y;
     }
 }
 
@@ -264,8 +299,7 @@ __device__ __forceinline__ void rht16_last(float* v) {
         v[i] = __fadd_rn(a, b);
         v[i + 8] = __fsub_rn(a, b);
     }
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], 0.25f);
+    scale16(v, 0.25f);
 }
 
 __device__ __forceinline__ void rht16(float* v, const RhtSigns& sg) {

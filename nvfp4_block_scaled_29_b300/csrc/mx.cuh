@@ -51,7 +51,7 @@ __device__ __forceinline__ float mx_inv_scale(uint32_t code) {
 // adjacent in the MMA layout).  Groups run to a whole 4-block scale tile so
 // that the tile's padding bytes are written as 0.
 template <bool RHT>
-__global__ void __launch_bounds__(kQuantThreads, 3) k_mx_quant_rows(const MxArgs a) {
+__global__ void __launch_bounds__(kQuantThreads, RHT ? 2 : 3) k_mx_quant_rows(const MxArgs a) {
     const int64_t nb = a.k >> 5;                                  // 32-element blocks per row
     const int64_t col_tiles = (nb + 3) >> 2;
     const uint32_t ngroups = (uint32_t)(col_tiles * 2);

@@ -119,7 +119,11 @@ bool make_bf16_tile_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t c
 // RHT-16 sign multipliers of a 16-bit mask (all +1 for mask 0).
 RhtSigns rht_signs(uint32_t mask) {
     RhtSigns sg;
-    for (int j = 0; j < 16; ++j) sg.s[j] = ((mask >> j) & 1u) ? -1.0f : 1.0f;
+    auto sgn = [&](int j) { return ((mask >> j) & 1u) ? -1.0f : 1.0f; };
+    for (int k = 0; k < 8; ++k) {
+        sg.p[k] = make_float2(sgn(k), sgn(k + 8));
+        sg.n[k] = make_float2(-sgn(k), -sgn(k + 8));
+    }
     return sg;
 }
 
@@ -167,7 +171,7 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
             p, x.rows, x.cols, x.ld, rht_signs(mask), out);
     } else {
-        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 2) * (x.cols / 16), kQuantThreads, 4), kQuantThreads,
+        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 2) * (x.cols / 16), kQuantThreads, 3), kQuantThreads,
                           0, st>>>(p, x.cols, x.rows, x.ld, rht_signs(mask), out);
     }
     return launch_status();

@@ -243,7 +243,7 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
 // the logical k runs along the stored rows).  One thread: 16 stored rows x
 // 2 stored columns (4-byte loads; a warp covers 128 contiguous bytes of a
 // row), transformed one column at a time.
-__global__ void __launch_bounds__(kQuantThreads, 4) k_amax_rht_cols(const uint16_t* __restrict__ p,
+__global__ void __launch_bounds__(kQuantThreads, 3) k_amax_rht_cols(const uint16_t* __restrict__ p,
                                                                     int64_t srows, int64_t scols,
                                                                     int64_t ld, const RhtSigns sg,
                                                                     float* out) {
@@ -347,8 +347,7 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
     const uint32_t sb = block_scale_code(__uint_as_float(amax_bits), s_enc);
     const float r_b = rtab[sb];
     *sb_out = sb;
-#pragma unroll
-    for (int j = 0; j < 16; ++j) v[j] = __fmul_rn(v[j], r_b);
+    scale16(v, r_b);
     if (SR) {
         if (HW == 1 || (HW < 0 && a.sr_hw)) {
             e2m1x16_sr(v, sr_words16(idx0 >> 4, a.stream_id, a.sr_key), code_lo, code_hi);
@@ -640,8 +639,7 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
             const uint32_t sb = (b < nblk) ? block_scale_code(__uint_as_float(lmax[b]), s_enc) : 0u;
             const float r_b = (b < nblk) ? encode_factor(s_enc, sb) : 0.0f;
             sw |= sb << (8 * b);
-    #pragma unroll
-            for (int j = 0; j < 16; ++j) v[b][j] = __fmul_rn(v[b][j], r_b);
+            scale16(v[b], r_b);
             if (SR) {
                 uint32_t lo = 0, hi = 0;
                 if (row_ok && b < nblk) {
