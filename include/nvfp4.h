@@ -242,6 +242,16 @@ size_t nvfp4_scale_bytes(int64_t rows, int64_t k);
 /* Static text of a status code.                                             */
 const char* nvfp4_status_string(nvfp4_status s);
 
+/* Test-only fault injection for failure detection (no GPU fault, trap or
+ * hang).  mode 1: the next streamed amax launch (nvfp4_amax_dual, or
+ * nvfp4_amax on a strided view without RHT) does not issue the copy of its
+ * first tile.  That tile's bounded wait expires after about 2 s, the kernel
+ * drains its other copies and returns, and nvfp4_get_status then reports
+ * NVFP4_ERR_TIMEOUT; the amax written by that call is undefined.  The
+ * injection applies once and then clears.  mode 0 clears it.  Returns
+ * NVFP4_ERR_INVALID_ARG for any other mode. */
+nvfp4_status nvfp4_debug_inject(int mode);
+
 #ifdef __cplusplus
 }
 #endif

@@ -102,6 +102,8 @@ def _load():
     L.nvfp4_scale_bytes.restype = ctypes.c_size_t
     L.nvfp4_status_string.argtypes = [st]
     L.nvfp4_status_string.restype = ctypes.c_char_p
+    L.nvfp4_debug_inject.argtypes = [ctypes.c_int]
+    L.nvfp4_debug_inject.restype = st
     return L
 
 
@@ -288,6 +290,13 @@ def nvfp4_rht_mask_from_seed(seed: int) -> int:
 
 def nvfp4_get_status(stream=None) -> int:
     return int(lib.nvfp4_get_status(_stream(stream)))
+
+
+def nvfp4_debug_inject(mode: int) -> int:
+    """Test-only fault injection: mode 1 makes the next streamed amax launch
+    skip the copy of its first tile, so that its bounded wait expires and
+    nvfp4_get_status reports NVFP4_ERR_TIMEOUT (see include/nvfp4.h)."""
+    return _check(int(lib.nvfp4_debug_inject(mode)), "nvfp4_debug_inject")
 
 
 def nvfp4_scale_bytes(rows: int, k: int) -> int:

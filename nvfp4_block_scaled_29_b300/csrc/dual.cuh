@@ -276,10 +276,14 @@ constexpr int kAmaxTileBytes = kAmaxTileRows * kAmaxTileCols * 2;
 constexpr int kAmaxStages = 3;
 constexpr int kAmaxSmem = kAmaxStages * kAmaxTileBytes + 64;
 
+// fi_skip_tile >= 0 (test-only fault injection): that tile's copy is never
+// issued, so its consumers' bounded wait expires and the kernel reports
+// NVFP4_DEV_TIMEOUT instead of hanging.
 template <bool RHT_COLS>
 __global__ void __launch_bounds__(kQuantThreads, 2) k_amax_stream(const __grid_constant__ CUtensorMap map,
                                                                   int64_t srows, int64_t scols, const RhtSigns sg,
-                                                                  float* out_plain, float* out_t) {
+                                                                  float* out_plain, float* out_t,
+                                                                  int64_t fi_skip_tile) {
     extern __shared__ __align__(128) uint8_t amax_smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(amax_smem + kAmaxStages * kAmaxTileBytes);
     __shared__ int abort_flag;
@@ -294,6 +298,7 @@ __global__ void __launch_bounds__(kQuantThreads, 2) k_amax_stream(const __grid_c
     }
     __syncthreads();
     auto issue = [&](int64_t t, int s) {
+        if (t == fi_skip_tile) return;
         const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
         mbar_arrive_expect_tx(&full[s], kAmaxTileBytes);
         tma_load_2d(amax_smem + s * kAmaxTileBytes, &map, &full[s], (int32_t)(tc * kAmaxTileCols),

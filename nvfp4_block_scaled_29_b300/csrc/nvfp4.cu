@@ -97,6 +97,10 @@ EncodeTiledFn encode_fn() {
 
 // A stored bf16 array [rows x cols] (leading dimension ld) in the streamed
 // amax's tiles: box 256 columns x 64 rows, no swizzle, zeros beyond.
+// Test-only fault injection (nvfp4_debug_inject): 1 = the next streamed amax
+// launch skips the copy of its first tile.
+std::atomic<int> g_fault_injection{0};
+
 // 2D map of a stored bf16 array [rows x cols] (leading dimension ld) with a
 // box of box_rows x box_cols elements.
 bool make_bf16_map(CUtensorMap* m, const void* ptr, int64_t rows, int64_t cols, int64_t ld, uint32_t box_cols,
@@ -147,8 +151,9 @@ nvfp4_status launch_amax_stream(const void* ptr, int64_t srows, int64_t scols, i
     const int64_t tiles = cdiv(srows, kAmaxTileRows) * cdiv(scols, kAmaxTileCols);
     const int g = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
     const RhtSigns sg = rht_signs(mask);
-    if (mask) k_amax_stream<true><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t);
-    else k_amax_stream<false><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t);
+    const int64_t skip = g_fault_injection.exchange(0) == 1 ? 0 : -1;   // test-only, one launch
+    if (mask) k_amax_stream<true><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t, skip);
+    else k_amax_stream<false><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t, skip);
     return launch_status();
 }
 
@@ -809,6 +814,12 @@ nvfp4_status nvfp4_get_status(cudaStream_t stream) {
 size_t nvfp4_scale_bytes(int64_t rows, int64_t k) {
     if (rows <= 0 || k <= 0) return 0;
     return (size_t)(cdiv(rows, 128) * cdiv(k / 16, 4) * 512);
+}
+
+nvfp4_status nvfp4_debug_inject(int mode) {
+    if (mode != 0 && mode != 1) return NVFP4_ERR_INVALID_ARG;
+    g_fault_injection.store(mode);
+    return NVFP4_OK;
 }
 
 const char* nvfp4_status_string(nvfp4_status s) {
