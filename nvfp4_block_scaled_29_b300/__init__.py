@@ -301,3 +301,42 @@ def nvfp4_debug_inject(mode: int) -> int:
 
 def nvfp4_scale_bytes(rows: int, k: int) -> int:
     return int(lib.nvfp4_scale_bytes(rows, k))
+
+
+# ------------------------------------------------------------------ tracing --
+# NVFP4_TRACE=1: every call of the functions above logs its name, its tensor
+# arguments' shapes and its host enqueue time (the calls are asynchronous) to
+# stderr.  NVFP4_TRACE=sync also synchronises the device before and after the
+# call, so the logged time covers its kernels.
+def _trace_wrap(fn, sync: bool):
+    import functools
+    import sys
+    import time
+
+    def desc(a):
+        if isinstance(a, torch.Tensor):
+            return "x".join(map(str, a.shape)) + ":" + str(a.dtype).replace("torch.", "")
+        if isinstance(a, (QTensor, MxQTensor)):
+            return f"q{a.rows}x{a.k}"
+        return repr(a) if isinstance(a, (int, float)) else type(a).__name__
+
+    @functools.wraps(fn)
+    def traced(*args, **kw):
+        if sync and torch.cuda.is_available():
+            torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        r = fn(*args, **kw)
+        if sync and torch.cuda.is_available():
+            torch.cuda.synchronize()
+        us = (time.perf_counter() - t0) * 1e6
+        print(f"[nvfp4] {fn.__name__}({', '.join(desc(a) for a in args)}) {us:.1f} us"
+              f"{' (device)' if sync else ' (enqueue)'}", file=sys.stderr)
+        return r
+
+    return traced
+
+
+_TRACE = os.environ.get("NVFP4_TRACE", "")
+if _TRACE in ("1", "sync"):
+    for _name in [n for n in list(globals()) if n.startswith("nvfp4_") and callable(globals()[n])]:
+        globals()[_name] = _trace_wrap(globals()[_name], _TRACE == "sync")
