@@ -183,9 +183,10 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
 }
 
 // -------------------------------------------------------------- quantise ---
-// Philox round keys of the seed and the rounding mode's generator: the
-// software rounding (NVFP4_SR) runs philox4x32_10_not, whose round-9 pair is
-// complemented; NVFP4_SR_HW runs the plain philox4x32_10.
+// Philox round keys of the seed and the rounding mode's generator: NVFP4_SR
+// runs philox4x32_10_not (complemented words, so that each half-word is
+// 65535 - u16), whose round-9 pair is complemented; NVFP4_SR_HW runs the plain
+// philox4x32_10.
 void set_sr_keys(QuantArgs* a, uint64_t seed, nvfp4_round round) {
     uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
     const bool hw = round == NVFP4_SR_HW;

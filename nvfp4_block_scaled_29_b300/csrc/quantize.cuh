@@ -293,8 +293,8 @@ struct QuantArgs {
     uint8_t* scales;            // swizzled
     RhtSigns rht;               // RHT-16 sign multipliers (RHT kernels only)
     uint64_t stream_id;
-    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10_not for the
-                                // software rounding, philox4x32_10 for sr_hw)
+    uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10_not for
+                                // NVFP4_SR, philox4x32_10 for NVFP4_SR_HW)
     int sr_hw;                  // 1: NVFP4_SR_HW random-bit layout (hardware conversion)
     // 2D transposed emit (optional)
     uint8_t* codes_t;           // [k x rows/2]
