@@ -127,8 +127,9 @@ nvfp4_status nvfp4_amax(nvfp4_bf16_view x, uint32_t rht_mask, float* amax_dev,
 /* 1x16 quantisation ([NVB] bullets 1, 2, 5; [SAI] global scale).
  * x: logical [rows x k], k % 16 == 0.  amax_dev: the tensor's amax as written
  * by nvfp4_amax (same view, same RHT setting); NULL makes the call compute it
- * first, using out->global_scale as the temporary.  round: RNE or SR (seed,
- * stream_id select the Philox stream; ignored for RNE).  out: rows and k must
+ * first, using out->global_scale as the temporary.  round: NVFP4_RNE,
+ * NVFP4_SR or NVFP4_SR_HW (seed, stream_id select the Philox stream; ignored
+ * for RNE).  out: rows and k must
  * equal x's; codes rows*k/2 bytes, scales nvfp4_scale_bytes(rows, k) bytes,
  * global_scale 1 float; all written (scale padding with 0).                 */
 nvfp4_status nvfp4_quantize_1d(nvfp4_bf16_view x, const float* amax_dev, nvfp4_round round,
