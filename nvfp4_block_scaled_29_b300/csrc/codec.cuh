@@ -156,28 +156,31 @@ __device__ __forceinline__ uint4 sr_rp8(uint64_t g, uint64_t stream_id, const ui
 // word (halves rp = 65535 - u16 of the two elements) puts the even element's
 // rp in L and the odd element's in H, so each element rounds up iff
 // u16 < floor(frac * 2^16) with its own 16 bits: exactly the NVFP4_SR rule.
-// Returns the byte code(v_even) | code(v_odd) << 4.  A single value takes its
-// half-word's position (f for the low half, b for the high) with 0 in the other
-// (e2m1_sr_rp_at).
+// Returns the conversion's 16 bits: code(v_even) in bits 0-3, code(v_odd) in
+// bits 8-11, zeros elsewhere.  A single value takes its half-word's position
+// (f for the low half, b for the high) with 0 in the other (e2m1_sr_rp_at).
 __device__ __forceinline__ uint32_t e2m1x2_sr_rp(float v_even, float v_odd, uint32_t rp_word) {
     const uint32_t rb = __byte_perm(rp_word, 0u, 0x3120u);
     uint16_t d;
     asm("cvt.rs.satfinite.e2m1x4.f32 %0, {%1, %2, %3, %4}, %5;"
         : "=h"(d)
         : "f"(0.0f), "f"(v_odd), "f"(0.0f), "f"(v_even), "r"(rb));
-    const uint32_t x = d;                     // code(v_even) in bits 0-3, code(v_odd) in bits 8-11
-    return (x | (x >> 4)) & 0xFFu;
+    return d;
 }
 
 __device__ __forceinline__ uint32_t e2m1_sr_rp_at(float v, uint32_t rp_word, bool high_half) {
-    return high_half ? (e2m1x2_sr_rp(0.0f, v, rp_word) >> 4) : (e2m1x2_sr_rp(v, 0.0f, rp_word) & 0xFu);
+    return high_half ? (e2m1x2_sr_rp(0.0f, v, rp_word) >> 8) & 0xFu : (e2m1x2_sr_rp(v, 0.0f, rp_word) & 0xFu);
 }
 
 // Eight values -> eight NVFP4_SR codes (element 0 in the lowest nibble), rp =
-// the complemented Philox block of these 8 elements (sr_rp8).
+// the complemented Philox block of these 8 elements (sr_rp8).  Two conversion
+// results join into one word with codes c0..c3 in the low nibbles of bytes
+// 0..3; t | (t >> 4) then holds c0 | c1 << 4 in byte 0 and c2 | c3 << 4 in
+// byte 2, and one byte permutation gathers those bytes of the two halves.
 __device__ __forceinline__ uint32_t e2m1x8_sr_cvt(const float* v, uint4 rp) {
-    return e2m1x2_sr_rp(v[0], v[1], rp.x) | (e2m1x2_sr_rp(v[2], v[3], rp.y) << 8) |
-           (e2m1x2_sr_rp(v[4], v[5], rp.z) << 16) | (e2m1x2_sr_rp(v[6], v[7], rp.w) << 24);
+    const uint32_t t01 = __byte_perm(e2m1x2_sr_rp(v[0], v[1], rp.x), e2m1x2_sr_rp(v[2], v[3], rp.y), 0x5410u);
+    const uint32_t t23 = __byte_perm(e2m1x2_sr_rp(v[4], v[5], rp.z), e2m1x2_sr_rp(v[6], v[7], rp.w), 0x5410u);
+    return __byte_perm(t01 | (t01 >> 4), t23 | (t23 >> 4), 0x6420u);
 }
 
 // --------------------------- stochastic E2M1, hardware layout (NVFP4_SR_HW) --
