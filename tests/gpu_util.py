@@ -81,3 +81,26 @@ def gemm_bound_check(y_gpu: np.ndarray, y_ref: np.ndarray, ab: np.ndarray, bf16:
         i = np.unravel_index(np.argmax(err - bound), err.shape)
         raise AssertionError(f"{what}: {np.count_nonzero(~ok)} of {ok.size} outside the bound; worst at "
                              f"{i}: gpu {y[i]!r} ref {y_ref[i]!r} sum|ab| {ab[i]!r}")
+
+
+def sample_ranges(rows, n, length, align, seed):
+    """Row ranges for sampled checks: the first and last `length` rows and n
+    random ranges in between, starts aligned to `align`."""
+    rng = np.random.default_rng(seed)
+    starts = sorted(set(int(s) // align * align for s in rng.integers(0, rows - length, n)))
+    return [(0, length)] + [(s, s + length) for s in starts] + [(rows - length, rows)]
+
+
+def check_sampled(gpu, ref, ranges, rows, k, what):
+    """Codes and scales of a GPU operand (codes, swizzled scales, S_enc) equal
+    the oracle's on the sampled row ranges; S_enc equal; scale padding zero."""
+    codes, scales_swz, s_enc = gpu
+    plain = oracle.unswizzle_scales(scales_swz[:oracle.scale_bytes(rows, k)], rows, k)
+    for lo, hi in ranges:
+        np.testing.assert_array_equal(codes[lo:hi], ref.codes[lo:hi], err_msg=f"{what} codes rows {lo}:{hi}")
+        np.testing.assert_array_equal(plain[lo:hi], ref.scales_plain[lo:hi], err_msg=f"{what} scales rows {lo}:{hi}")
+    assert s_enc == np.float32(ref.s_enc), what
+    # padding of the scale layout is zero
+    full = np.zeros(oracle.scale_bytes(rows, k), np.uint8)
+    pad_mask = oracle.swizzle_scales(np.ones((rows, k // 16), np.uint8), rows, k) == 0
+    assert not scales_swz[:full.size][pad_mask].any(), f"{what}: non-zero scale padding"

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 import synth
-from gpu_util import dev_bf16, gemm_bound_check
+from gpu_util import check_sampled as _check_sampled, dev_bf16, gemm_bound_check, sample_ranges as _ranges
 
 pytestmark = [pytest.mark.gpu, pytest.mark.slow]
 
@@ -68,25 +68,6 @@ def step(nv):
            "qxt": host(qxt), "y": y.float().cpu().numpy(), "dx": dxo.float().cpu().numpy(),
            "dw": dwo.float().cpu().numpy()}
     return out
-
-
-def _ranges(rows, n, length, align, seed):
-    rng = np.random.default_rng(seed)
-    starts = sorted(set(int(s) // align * align for s in rng.integers(0, rows - length, n)))
-    return [(0, length)] + [(s, s + length) for s in starts] + [(rows - length, rows)]
-
-
-def _check_sampled(gpu, ref, ranges, rows, k, what):
-    codes, scales_swz, s_enc = gpu
-    plain = oracle.unswizzle_scales(scales_swz[:oracle.scale_bytes(rows, k)], rows, k)
-    for lo, hi in ranges:
-        np.testing.assert_array_equal(codes[lo:hi], ref.codes[lo:hi], err_msg=f"{what} codes rows {lo}:{hi}")
-        np.testing.assert_array_equal(plain[lo:hi], ref.scales_plain[lo:hi], err_msg=f"{what} scales rows {lo}:{hi}")
-    assert s_enc == np.float32(ref.s_enc), what
-    # padding of the scale layout is zero
-    full = np.zeros(oracle.scale_bytes(rows, k), np.uint8)
-    pad_mask = oracle.swizzle_scales(np.ones((rows, k // 16), np.uint8), rows, k) == 0
-    assert not scales_swz[:full.size][pad_mask].any(), f"{what}: non-zero scale padding"
 
 
 def test_amax_values(step):
