@@ -119,6 +119,25 @@ def test_philox_known_answers(golden_dir):
         np.testing.assert_array_equal(oracle.philox4x32_10(w[:4], w[4:6]), np.array(w[6:], np.uint32))
 
 
+def test_philox_matches_curand_host_call(tmp_path_factory):
+    """The oracle's Philox4x32-10 equals the CUDA toolkit's cuRAND block
+    function (called on the host, black box) on random and edge counters/keys."""
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not available")
+    exe = str(tmp_path_factory.mktemp("hp") / "host_philox")
+    subprocess.check_call([nvcc, "-O2", "-o", exe, os.path.join(ROOT, "tests", "helpers", "host_philox.cu")])
+    rng = np.random.default_rng(21)
+    recs = rng.integers(0, 1 << 32, (2000, 6), dtype=np.uint64).astype(np.uint32)
+    edge = np.array([[0, 0, 0, 0, 0, 0], [0xFFFFFFFF] * 6, [1, 0, 0, 0, 0, 0], [0, 0, 0, 1, 0xDEADBEEF, 0]],
+                    np.uint32)
+    recs = np.concatenate([recs, edge])
+    r = subprocess.run([exe], input=recs.tobytes(), capture_output=True, check=True)
+    lib = np.frombuffer(r.stdout, dtype=np.uint32).reshape(-1, 4)
+    for rec, want in zip(recs, lib):
+        np.testing.assert_array_equal(oracle.philox4x32_10(rec[:4], rec[4:6]), want)
+
+
 def test_philox_bit_statistics():
     bits = np.array([oracle.sr_bits16(123, 7, i) for i in range(200000)], dtype=np.uint32)
     # every one of the 16 bit positions is set about half the time (5 sigma)
