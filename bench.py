@@ -305,6 +305,13 @@ def torch_int16(torch):
     return torch.int16
 
 
+def input_digests(**arrays) -> dict:
+    """sha256 of each synthetic input's bytes (bf16 bit patterns), so a run's
+    inputs can be matched against any other run's."""
+    import hashlib
+    return {k: hashlib.sha256(np.ascontiguousarray(v).tobytes()).hexdigest() for k, v in arrays.items()}
+
+
 def make_host_inputs():
     import synth
     x = synth.activations(SEED_X)
@@ -423,6 +430,7 @@ def main():
     import nvfp4_block_scaled_29_b300 as nv
 
     xh, wh, dyh = make_host_inputs()
+    digests = input_digests(x=xh, w=wh, dy=dyh)
     host = {"x": torch.from_numpy(xh.view(np.int16)).pin_memory(),
             "w": torch.from_numpy(wh.view(np.int16)).pin_memory(),
             "dy": torch.from_numpy(dyh.view(np.int16)).pin_memory()}
@@ -515,6 +523,7 @@ def main():
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp4-e2m1 x e4m3-scaled, fp32 accumulate (bf16 in/out)",
         "data": "synthetic (seeded N(0,1)+outliers, N(0,0.02^2), 1e-3*t3)",
+        "inputs_sha256": digests,
         "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
                    "path": args.path,
                    "streams": ("2: forward W chain on a second stream beside the X chain; phase_ms overlap"

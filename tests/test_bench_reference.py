@@ -23,3 +23,18 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"]
+
+
+def test_input_digests_are_stable():
+    """The bench's input digests depend only on the seeded generators."""
+    sys.path.insert(0, ROOT)
+    import numpy as np
+
+    import bench
+    import synth
+    a = bench.input_digests(x=synth.normal_bf16((64, 128), 5, 1.0, 0.0005, 100.0))
+    b = bench.input_digests(x=synth.normal_bf16((64, 128), 5, 1.0, 0.0005, 100.0))
+    c = bench.input_digests(x=synth.normal_bf16((64, 128), 6, 1.0, 0.0005, 100.0))
+    assert a == b and a != c and len(a["x"]) == 64
+    assert bench.input_digests(z=np.zeros(4, np.uint16))["z"] == \
+        "af5570f5a1810b7af78caf4bc70a660f0df51e42baf91d4de5b2328de0e83dfc"
