@@ -339,8 +339,7 @@ template <int SR1, int SR2, bool RHT2>
 nvfp4_status launch_dual_t(const CUtensorMap& map, const DualArgs& d, int grid, cudaStream_t st) {
     static std::atomic<int> ready[kMaxDevices];
     int dev = 0;
-    cudaGetDevice(&dev);
-    if (dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
     if (!ready[dev].load()) {
         if (cudaFuncSetAttribute(k_quant_dual<SR1, SR2, RHT2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kDqSmem) != cudaSuccess)
@@ -487,7 +486,7 @@ nvfp4_status launch_gemm_pair(const GemmMaps& mp, const gemm::Args& g, cudaStrea
     cfg.numAttrs = 1;
     static std::atomic<int> cache[kMaxDevices];
     int dev = 0;
-    cudaGetDevice(&dev);
+    if (cudaGetDevice(&dev) != cudaSuccess) return NVFP4_ERR_CUDA;
     int n = (dev >= 0 && dev < kMaxDevices) ? cache[dev].load() : 0;
     if (n <= 0) {
         cfg.gridDim = dim3((unsigned)(device_sm_count() / 2 * 2));
