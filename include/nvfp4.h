@@ -89,7 +89,9 @@ typedef enum {
     NVFP4_ERR_MISALIGNED = 3,       /* pointer or leading dimension not 16-byte aligned  */
     NVFP4_ERR_NONFINITE = 4,        /* amax was NaN or Inf (device-side, via get_status) */
     NVFP4_ERR_TIMEOUT = 5,          /* a bounded device wait expired (device-side)       */
-    NVFP4_ERR_CUDA = 6              /* a CUDA runtime call failed                        */
+    NVFP4_ERR_CUDA = 6,             /* a CUDA runtime call failed                        */
+    NVFP4_ERR_LAUNCH = 7            /* a kernel got less dynamic shared memory than it   */
+                                    /* needs and returned early (device-side)            */
 } nvfp4_status;
 
 typedef enum { NVFP4_RNE = 0, NVFP4_SR = 1, NVFP4_SR_HW = 2 } nvfp4_round;
@@ -233,8 +235,9 @@ nvfp4_status nvfp4_mx_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is
 uint32_t nvfp4_rht_mask_from_seed(uint64_t seed);
 
 /* Synchronises `stream`, returns the device-side status recorded since the
- * last call (NVFP4_ERR_TIMEOUT before NVFP4_ERR_NONFINITE before NVFP4_OK,
- * NVFP4_ERR_CUDA if the stream reports a CUDA error) and clears it.        */
+ * last call (NVFP4_ERR_LAUNCH before NVFP4_ERR_TIMEOUT before
+ * NVFP4_ERR_NONFINITE before NVFP4_OK, NVFP4_ERR_CUDA if the stream reports
+ * a CUDA error) and clears it.                                              */
 nvfp4_status nvfp4_get_status(cudaStream_t stream);
 
 /* Size in bytes of the swizzled scale buffer of a [rows x k] operand.       */

@@ -35,6 +35,7 @@ NVFP4_ERR_MISALIGNED = 3
 NVFP4_ERR_NONFINITE = 4
 NVFP4_ERR_TIMEOUT = 5
 NVFP4_ERR_CUDA = 6
+NVFP4_ERR_LAUNCH = 7
 NVFP4_RNE = 0
 NVFP4_SR = 1
 NVFP4_SR_HW = 2              # the same rule, random bits in the hardware conversion's layout

@@ -11,7 +11,6 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIB = os.path.join(HERE, "libnvfp4.so")
 SOURCES = ["nvfp4.cu"]
-HEADERS = ["codec.cuh", "gemm.cuh", "ptx.cuh", "quantize.cuh", "status.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",
@@ -30,8 +29,13 @@ def nvcc() -> str:
 
 
 def _inputs():
-    files = [os.path.join(CSRC, s) for s in SOURCES + HEADERS]
+    """Every file the library is compiled from: the sources, every kernel
+    header under csrc/ (found by listing, so a new header is tracked too) and
+    the public header."""
+    files = [os.path.join(CSRC, s) for s in SOURCES]
+    files += sorted(os.path.join(CSRC, f) for f in os.listdir(CSRC) if f.endswith((".cuh", ".h")))
     files.append(os.path.join(ROOT, "include", "nvfp4.h"))
+    files.append(os.path.abspath(__file__))
     return files
 
 

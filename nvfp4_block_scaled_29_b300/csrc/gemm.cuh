@@ -168,7 +168,7 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
         const uint32_t pad = (uint32_t)(smem - smem_raw);
         if (pad + (uint32_t)(smem_bytes_for(TMA_EPI) - 1024) > dyn) {
-            if (threadIdx.x == 0) record_device_error(NVFP4_DEV_TIMEOUT);
+            if (threadIdx.x == 0) record_device_error(NVFP4_DEV_LAUNCH);
             return;
         }
     }

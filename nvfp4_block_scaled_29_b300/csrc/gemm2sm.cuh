@@ -106,7 +106,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         asm("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dyn));
         const uint32_t pad = (uint32_t)(smem - smem_raw);
         if (pad + (uint32_t)(smem_bytes_for(TMA_EPI, MX) - 1024) > dyn) {
-            if (threadIdx.x == 0) record_device_error(NVFP4_DEV_TIMEOUT);
+            if (threadIdx.x == 0) record_device_error(NVFP4_DEV_LAUNCH);
             return;
         }
     }
@@ -239,7 +239,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                 }
                 const uint32_t t = tmem_base + lane_base + TMEM_SF_BASE + stage * F::SF_COLS;
                 tmem_st_32x32b_x16(t, r);
-                if (MX) {
+                if constexpr (MX) {
                     tmem_st_32x32b_x8(t + 16, r + 16);
                 } else {
                     tmem_st_32x32b_x16(t + 16, r + 16);

@@ -64,10 +64,12 @@ nvfp4_status check_view(const nvfp4_bf16_view& x, bool need_k16) {
     return NVFP4_OK;
 }
 
-nvfp4_status check_q(const nvfp4_q* q, int64_t rows, int64_t k) {
+// A quantised operand of logical shape [rows x k]: NVFP4 operands need their
+// global scale, MXFP4 operands (need_gs = false) have none.
+nvfp4_status check_q(const nvfp4_q* q, int64_t rows, int64_t k, bool need_gs = true) {
     if (q == nullptr) return NVFP4_ERR_INVALID_ARG;
     if (q->rows != rows || q->k != k) return NVFP4_ERR_INVALID_ARG;
-    if (q->global_scale == nullptr || !aligned(q->global_scale, 4)) return NVFP4_ERR_INVALID_ARG;
+    if (need_gs && (q->global_scale == nullptr || !aligned(q->global_scale, 4))) return NVFP4_ERR_INVALID_ARG;
     if (rows == 0 || k == 0) return NVFP4_OK;
     if (q->codes == nullptr || q->scales == nullptr) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(q->codes, 16) || !aligned(q->scales, 16)) return NVFP4_ERR_MISALIGNED;
@@ -753,11 +755,10 @@ nvfp4_status nvfp4_mx_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is
     const int64_t M = a->rows, N = b->rows, K = a->k;
     if (K % 32 != 0) return NVFP4_ERR_UNSUPPORTED_SHAPE;
     if (M > INT32_MAX || N > INT32_MAX || K > INT32_MAX) return NVFP4_ERR_UNSUPPORTED_SHAPE;
+    nvfp4_status s;
+    if ((s = check_q(a, M, K, false)) != NVFP4_OK) return s;
+    if ((s = check_q(b, N, K, false)) != NVFP4_OK) return s;
     if (M == 0 || N == 0) return NVFP4_OK;
-    for (const nvfp4_q* q : {a, b}) {
-        if (K > 0 && (q->codes == nullptr || q->scales == nullptr)) return NVFP4_ERR_INVALID_ARG;
-        if (!aligned(q->codes, 16) || !aligned(q->scales, 16)) return NVFP4_ERR_MISALIGNED;
-    }
     const int64_t esz = d_is_bf16 ? 2 : 4;
     if (d == nullptr || ldd < N) return NVFP4_ERR_INVALID_ARG;
     if (!aligned(d, 16) || (ldd * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
@@ -806,6 +807,7 @@ nvfp4_status nvfp4_get_status(cudaStream_t stream) {
                                 stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (word & NVFP4_DEV_LAUNCH) return NVFP4_ERR_LAUNCH;
     if (word & NVFP4_DEV_TIMEOUT) return NVFP4_ERR_TIMEOUT;
     if (word & NVFP4_DEV_NONFINITE) return NVFP4_ERR_NONFINITE;
     return NVFP4_OK;
@@ -831,6 +833,7 @@ const char* nvfp4_status_string(nvfp4_status s) {
         case NVFP4_ERR_NONFINITE: return "non-finite amax";
         case NVFP4_ERR_TIMEOUT: return "device wait timed out";
         case NVFP4_ERR_CUDA: return "CUDA error";
+        case NVFP4_ERR_LAUNCH: return "kernel launched with too little dynamic shared memory";
     }
     return "unknown status";
 }

@@ -197,27 +197,6 @@ __device__ __forceinline__ void mbar_arrive_cluster(uint32_t cluster_addr) {
                  : "memory");
 }
 
-// 2D tensor load multicast to the CTAs of `mask`: the same shared-memory
-// offset and the mbarrier at the same offset in each destination CTA.
-__device__ __forceinline__ void tma_load_2d_mc(void* dst, const void* desc, uint64_t* bar,
-                                               int32_t x, int32_t y, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
-        ".multicast::cluster [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(smem_addr(bar)), "h"(mask)
-        : "memory");
-}
-
-// 1D bulk copy global -> shared multicast to the CTAs of `mask`.
-__device__ __forceinline__ void bulk_load_mc(void* dst, const void* src, uint32_t bytes,
-                                             uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar)), "h"(mask)
-        : "memory");
-}
-
 // 3D tiled tensor load into shared memory, completing on `bar`.
 __device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_t* bar, int32_t x, int32_t y,
                                             int32_t z) {

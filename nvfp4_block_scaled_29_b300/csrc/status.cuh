@@ -1,8 +1,9 @@
 // status.cuh -- the device-side status word of libnvfp4.
 //
 // Kernels never trap: a condition they cannot handle (a non-finite amax
-// reaching a quantiser, a pipeline wait that exceeded its time limit) sets a
-// bit here and the kernel returns.  nvfp4_get_status() reads and clears it.
+// reaching a quantiser, a pipeline wait that exceeded its time limit, a launch
+// with too little dynamic shared memory) sets a bit here and the kernel
+// returns.  nvfp4_get_status() reads and clears it.
 #pragma once
 #include <cstdint>
 
@@ -11,6 +12,7 @@ namespace nvfp4 {
 enum : uint32_t {
     NVFP4_DEV_NONFINITE = 1u,
     NVFP4_DEV_TIMEOUT = 2u,
+    NVFP4_DEV_LAUNCH = 4u,     // a kernel was launched with less dynamic shared memory than it needs
 };
 
 // The library is one translation unit (nvfp4.cu includes every kernel

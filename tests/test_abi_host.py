@@ -150,3 +150,32 @@ def test_mx_helpers_and_validation(nv):
     a2 = nv.QStruct(0x1000, 0x2000, None, 128, 48, 0)
     b2 = nv.QStruct(0x3000, 0x4000, None, 256, 48, 0)
     assert L.nvfp4_mx_gemm(ctypes.byref(a2), ctypes.byref(b2), 0x5000, 0, 256, None) == nv.NVFP4_ERR_UNSUPPORTED_SHAPE
+
+
+def test_build_tracks_every_kernel_header(tmp_path, monkeypatch):
+    """Every header under csrc/ is an input of the build, so editing one of
+    them (the CTA-pair GEMM, the dual quantiser, MXFP4, ...) rebuilds the
+    library instead of keeping a stale one."""
+    from nvfp4_block_scaled_29_b300 import build
+    inputs = set(build._inputs())
+    for f in os.listdir(build.CSRC):
+        if f.endswith((".cuh", ".cu", ".h")):
+            assert os.path.join(build.CSRC, f) in inputs, f
+    fake = tmp_path / "libnvfp4.so"
+    fake.write_bytes(b"")
+    monkeypatch.setattr(build, "LIB", str(fake))
+    newest = max(os.path.getmtime(f) for f in inputs)
+    os.utime(fake, (newest + 10, newest + 10))
+    assert build.up_to_date()
+    dual = os.path.join(build.CSRC, "dual.cuh")
+    t = os.path.getmtime(dual)
+    os.utime(fake, (t - 10, t - 10))       # dual.cuh is now newer than the library
+    assert not build.up_to_date()
+
+
+def test_launch_status_has_its_own_code(nv):
+    lib = ctypes.CDLL(nv.LIB_PATH)
+    lib.nvfp4_status_string.restype = ctypes.c_char_p
+    assert nv.NVFP4_ERR_LAUNCH == 7
+    assert b"shared memory" in lib.nvfp4_status_string(nv.NVFP4_ERR_LAUNCH)
+    assert lib.nvfp4_status_string(nv.NVFP4_ERR_TIMEOUT) != lib.nvfp4_status_string(nv.NVFP4_ERR_LAUNCH)
