@@ -94,12 +94,32 @@ __host__ __device__ constexpr uint32_t make_idesc() {
     return (1u << 7) | (1u << 10) | ((uint32_t)(BN >> 3) << 17) | ((uint32_t)(BM >> 4) << 24);
 }
 
+// alpha = 1 / (S_A * S_B), carried as m * p: m an FP32 number in the normal
+// range and p a power of two.  1/(S_A S_B) spans about 2^-256 .. 2^233 (each
+// S_enc lies in [2688 / bf16 max, FLT_MAX]), far beyond FP32's normal range;
+// rounding it to one FP32 number would leave a subnormal alpha with fewer
+// than 24 significant bits (or zero) when both operands have a tiny amax.
+// D = fp32(fp32(acc * m) * p): with p = 1 (the usual case) this is
+// fp32(acc * fp32(alpha)); otherwise the second product is exact unless its
+// result is itself outside the normal range.
+struct Alpha {
+    float m, p;
+    __device__ __forceinline__ float apply(float acc) const { return __fmul_rn(__fmul_rn(acc, m), p); }
+};
+
+__device__ __forceinline__ Alpha make_alpha(float s_a, float s_b) {
+    const double a = 1.0 / ((double)s_a * (double)s_b);
+    if (a < 0x1p-126) return Alpha{(float)(a * 0x1p80), 0x1p-80f};
+    if (a > 0x1p127) return Alpha{(float)fmin(a * 0x1p-80, 0x1.fffffep127), 0x1p80f};
+    return Alpha{(float)a, 1.0f};
+}
+
 __device__ __forceinline__ void store_chunk(const Args& a, int64_t row, int64_t col0,
-                                            const uint32_t* acc, float alpha) {
+                                            const uint32_t* acc, Alpha alpha) {
     if (row >= a.M) return;
     float v[32];
 #pragma unroll
-    for (int j = 0; j < 32; ++j) v[j] = __fmul_rn(__uint_as_float(acc[j]), alpha);
+    for (int j = 0; j < 32; ++j) v[j] = alpha.apply(__uint_as_float(acc[j]));
     const bool full = col0 + 32 <= a.N;
     if (a.d_bf16) {
         uint16_t* dst = reinterpret_cast<uint16_t*>(a.d) + row * a.ldd + col0;
@@ -137,12 +157,12 @@ __device__ __forceinline__ void store_chunk(const Args& a, int64_t row, int64_t 
 // four 64-column blocks, each 32 rows x 128 bytes in the 128-byte swizzle
 // (16-byte unit u of row r at unit u ^ (r % 8)), stored by TMA.
 __device__ __forceinline__ void stage_bf16_chunk(uint32_t stg, int c, int lane, const uint32_t* acc,
-                                                 float alpha) {
+                                                 Alpha alpha) {
     uint32_t p[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(__fmul_rn(__uint_as_float(acc[2 * j]), alpha),
-                                                 __fmul_rn(__uint_as_float(acc[2 * j + 1]), alpha));
+        __nv_bfloat162 h = __floats2bfloat162_rn(alpha.apply(__uint_as_float(acc[2 * j])),
+                                                 alpha.apply(__uint_as_float(acc[2 * j + 1])));
         p[j] = *reinterpret_cast<uint32_t*>(&h);
     }
     const uint32_t blk = stg + (uint32_t)(c >> 1) * (32 * 128) + (uint32_t)lane * 128;
@@ -340,7 +360,7 @@ k_gemm_nvfp4(const __grid_constant__ CUtensorMap tma_a, const __grid_constant__ 
     } else {
         // --------------------------------------------------- epilogue ----
         const int quarter = warp & 3;
-        const float alpha = (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
+        const Alpha alpha = make_alpha(*args.gs_a, *args.gs_b);
         const uint32_t stg = smem_addr(epi_stage) + (uint32_t)(warp - 2) * EPI_WARP_BYTES;
         const uint64_t out_policy = l2_policy_evict_first();   // D is written once
         int local = 0;

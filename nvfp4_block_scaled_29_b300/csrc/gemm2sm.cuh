@@ -331,7 +331,7 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
         const int col0 = warp >= 10 ? BN / 2 : 0;
         const int ew = warp < 6 ? warp - 2 : warp - 6;
         // MXFP4 has no tensor scales: D is the plain sum of the scaled products
-        const float alpha = MX ? 1.0f : (float)(1.0 / ((double)(*args.gs_a) * (double)(*args.gs_b)));
+        const gemm::Alpha alpha = MX ? gemm::Alpha{1.0f, 1.0f} : gemm::make_alpha(*args.gs_a, *args.gs_b);
         const uint32_t stg = smem_addr(epi_stage) + (uint32_t)ew * EPI_BLOCK;
         const uint64_t out_policy = l2_policy_evict_first();   // D is written once
         int local = 0;
@@ -353,8 +353,8 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
                         __nv_bfloat162 hv = __floats2bfloat162_rn(
-                            __fmul_rn(__uint_as_float(acc[c & 1][2 * j]), alpha),
-                            __fmul_rn(__uint_as_float(acc[c & 1][2 * j + 1]), alpha));
+                            alpha.apply(__uint_as_float(acc[c & 1][2 * j])),
+                            alpha.apply(__uint_as_float(acc[c & 1][2 * j + 1])));
                         packed[(c & 3) * 8 + j] = *reinterpret_cast<uint32_t*>(&hv);
                     }
                     if (c == 3 || c == BN / 32 - 1) {

@@ -288,6 +288,128 @@ def test_gemm_scale_rows_are_distinct(nv, M):
     gemm_bound_check(d.cpu().numpy(), y_ref, ab, False, "per-row scales")
 
 
+def _full_range_scales(rows, k, seed):
+    """E4M3 decode-scale bytes over the whole finite range 0x00-0x7E: uniform
+    draws, then whole zero-scale blocks (0x00), subnormal codes 0x01-0x07 and
+    the largest code 0x7E (448) planted in about 6%, 12% and 3% of the blocks."""
+    rng = np.random.default_rng(seed)
+    s = rng.integers(0x00, 0x7F, size=(rows, k // 16), dtype=np.uint8)
+    u = rng.random(s.shape)
+    s[u < 0.06] = 0x00
+    sub = (u >= 0.06) & (u < 0.18)
+    s[sub] = rng.integers(0x01, 0x08, size=int(sub.sum()), dtype=np.uint8)
+    s[(u >= 0.18) & (u < 0.21)] = 0x7E
+    return s
+
+
+@pytest.mark.parametrize("M,N,K", [(256, 512, 512), (128, 256, 320), (1024, 768, 1280), (384, 200, 4096)])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_gemm_full_e4m3_scale_range(nv, M, N, K, bf16):
+    """Block scales over every finite E4M3 code, including zero-scale blocks,
+    the subnormal codes 0x01-0x07 (2^-9 .. 7 * 2^-9) and 0x7E: the tensor
+    core's UE4M3 scale decoding must match the format's value set ([NVB]
+    recipe bullet 2: E4M3 block scales; [SAI] "Core architectural changes of
+    the MVFP4 format").  (128, 256, 320) and (384, 200, 4096) run the
+    single-CTA kernel (odd 128-row tile count)."""
+    rng = np.random.default_rng(M * 3 + N + K)
+    ca = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
+    cb = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
+    sa, sb = _full_range_scales(M, K, M + K), _full_range_scales(N, K, N + 2 * K)
+    assert (sa == 0).any() and ((sa >= 1) & (sa <= 7)).any() and (sa == 0x7E).any()
+    SA, SB = np.float32(2.5), np.float32(0.375)
+    ga, swa = _upload_operand(nv, ca, sa, SA, M, K)
+    gb, swb = _upload_operand(nv, cb, sb, SB, N, K)
+    d = torch.empty((M, ((N + 7) // 8) * 8), dtype=torch.bfloat16 if bf16 else torch.float32,
+                    device="cuda")[:, :N]
+    d.fill_(float("nan"))
+    nv.nvfp4_gemm(ga, gb, d)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK
+    y_ref, ab = oracle.gemm_full(ca, swa, SA, cb, swb, SB, M, N, K)
+    gemm_bound_check(d.float().cpu().numpy(), y_ref, ab, bf16, f"full scale range {M}x{N}x{K} bf16={bf16}")
+
+
+def test_gemm_subnormal_scale_products_exact(nv):
+    """Only subnormal and zero scales, codes 1.0: every product of two block
+    scales is a small exact binary64 number and the FP32 sums are exact, so
+    D must equal the oracle exactly."""
+    M, N, K = 256, 256, 256
+    rng = np.random.default_rng(11)
+    ca = np.full((M, K // 2), 0x22, np.uint8)
+    cb = np.full((N, K // 2), 0x22, np.uint8)
+    sa = rng.integers(0, 8, size=(M, K // 16), dtype=np.uint8)
+    sb = rng.integers(0, 8, size=(N, K // 16), dtype=np.uint8)
+    ga, swa = _upload_operand(nv, ca, sa, 1.0, M, K)
+    gb, swb = _upload_operand(nv, cb, sb, 1.0, N, K)
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    nv.nvfp4_gemm(ga, gb, d)
+    torch.cuda.synchronize()
+    y_ref, _ = oracle.gemm_full(ca, swa, 1.0, cb, swb, 1.0, M, N, K)
+    np.testing.assert_array_equal(d.cpu().numpy().astype(np.float64), y_ref)
+
+
+def _tiny_amax_data(rows, k, seed, magnitude):
+    """bf16 data ~ N(0,1) * magnitude (a magnitude below 7.9e-36 makes the
+    tensor's S_enc = 2688 / amax overflow to FLT_MAX)."""
+    g = np.random.default_rng(seed)
+    x = (g.standard_normal((rows, k)) * magnitude).astype(np.float32)
+    return synth._to_bf16_bits(x)
+
+
+@pytest.mark.parametrize("tiny", ["a", "ab"])
+@pytest.mark.parametrize("bf16", [False, True])
+def test_gemm_alpha_from_saturated_global_scale(nv, tiny, bf16):
+    """An operand whose amax is tiny (S_enc saturates to FLT_MAX): alpha =
+    1 / (S_A S_B) falls into FP32's subnormal range ("a") or below it ("ab",
+    both operands tiny: the exact products underflow FP32 altogether).  The
+    quantised operands must equal the oracle's and D must stay within the
+    bound of the binary64 reference."""
+    M, N, K = 256, 256, 512
+    x = _tiny_amax_data(M, K, 21, 1e-37)
+    w = _tiny_amax_data(N, K, 22, 1e-37) if tiny == "ab" else synth.normal_bf16((N, K), 23, 0.02)
+    qx, _, _ = gpu_quantize(nv, dev_bf16(x))
+    qw, _, _ = gpu_quantize(nv, dev_bf16(w), block2d=True)
+    ox, ow = oracle.quantize(x), oracle.quantize(w, block2d=True)
+    assert_q_equal(qx, ox.codes, ox.scales, ox.s_enc, "tiny X")
+    assert_q_equal(qw, ow.codes, ow.scales, ow.s_enc, "W")
+    assert ox.s_enc == np.float32(np.finfo(np.float32).max)
+    d = torch.empty((M, N), dtype=torch.bfloat16 if bf16 else torch.float32, device="cuda")
+    nv.nvfp4_gemm(qx, qw, d)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK
+    y_ref, ab = oracle.gemm_full(ox.codes, ox.scales, ox.s_enc, ow.codes, ow.scales, ow.s_enc, M, N, K)
+    alpha = 1.0 / (float(ox.s_enc) * float(ow.s_enc))
+    assert alpha < 2.0 ** -126                                 # outside FP32's normal range
+    gemm_bound_check(d.float().cpu().numpy(), y_ref, ab, bf16, f"saturated S_enc ({tiny}) bf16={bf16}")
+    if tiny == "a":
+        assert np.count_nonzero(d.float().cpu().numpy()) > 0.9 * M * N
+
+
+def test_quantize_gemm_subnormal_block_scales(nv):
+    """Quantise -> GEMM with subnormal E4M3 block scales made by the
+    quantiser itself: one huge outlier sets S_enc, and blocks of small values
+    beside it get decode scales 0x01-0x07 (or 0).  Codes and scales must equal
+    the oracle's, and D must be within the bound."""
+    M, N, K = 256, 256, 1024
+    g = np.random.default_rng(31)
+    xf = (g.standard_normal((M, K)) * 0.05).astype(np.float32)
+    xf[7, 100] = 1.0e4
+    x = synth._to_bf16_bits(xf)
+    w = synth.normal_bf16((N, K), 32, 0.02)
+    qx, _, _ = gpu_quantize(nv, dev_bf16(x))
+    qw, _, _ = gpu_quantize(nv, dev_bf16(w), block2d=True)
+    ox, ow = oracle.quantize(x), oracle.quantize(w, block2d=True)
+    assert_q_equal(qx, ox.codes, ox.scales, ox.s_enc, "X with subnormal block scales")
+    assert_q_equal(qw, ow.codes, ow.scales, ow.s_enc, "W")
+    plain = ox.scales_plain
+    assert ((plain >= 1) & (plain <= 7)).mean() > 0.5, "the case must produce subnormal scales"
+    d = torch.empty((M, N), dtype=torch.float32, device="cuda")
+    nv.nvfp4_gemm(qx, qw, d)
+    torch.cuda.synchronize()
+    y_ref, ab = oracle.gemm_full(ox.codes, ox.scales, ox.s_enc, ow.codes, ow.scales, ow.s_enc, M, N, K)
+    gemm_bound_check(d.cpu().numpy(), y_ref, ab, False, "subnormal block scales")
+
+
 # --------------------------------------------------- tiny forward linear ---
 def test_tiny_forward_linear(nv):
     """The tiny forward workload end to end: X [128 x 256] 1x16 RNE, W
