@@ -105,6 +105,8 @@ def _load():
     L.nvfp4_status_string.restype = ctypes.c_char_p
     L.nvfp4_debug_inject.argtypes = [ctypes.c_int]
     L.nvfp4_debug_inject.restype = st
+    L.nvfp4_debug_check_div6.argtypes = [ctypes.c_uint32, ctypes.c_uint32, vp, vp, vp]
+    L.nvfp4_debug_check_div6.restype = st
     return L
 
 
@@ -298,6 +300,19 @@ def nvfp4_debug_inject(mode: int) -> int:
     skip the copy of its first tile, so that its bounded wait expires and
     nvfp4_get_status reports NVFP4_ERR_TIMEOUT (see include/nvfp4.h)."""
     return _check(int(lib.nvfp4_debug_inject(mode)), "nvfp4_debug_inject")
+
+
+def nvfp4_debug_check_div6(lo_bits: int, hi_bits: int, *, stream=None):
+    """Test-only: (mismatches, smallest mismatching bit pattern or None) of the
+    kernels' amax_b / 6 against IEEE division, over float bit patterns in
+    [lo_bits, hi_bits) (see include/nvfp4.h)."""
+    cnt = torch.empty((1,), dtype=torch.int64, device="cuda")
+    first = torch.empty((1,), dtype=torch.int32, device="cuda")
+    _check(lib.nvfp4_debug_check_div6(lo_bits, hi_bits, cnt.data_ptr(), first.data_ptr(), _stream(stream)),
+           "nvfp4_debug_check_div6")
+    n = int(cnt.cpu()[0])
+    f = int(first.cpu()[0]) & 0xFFFFFFFF
+    return n, (None if f == 0xFFFFFFFF else f)
 
 
 def nvfp4_scale_bytes(rows: int, k: int) -> int:

@@ -504,6 +504,28 @@ nvfp4_status launch_gemm_pair(const GemmMaps& mp, const gemm::Args& g, cudaStrea
     return NVFP4_OK;
 }
 
+// Test-only: compare div6_rn(x) with the IEEE division x / 6 (__fdiv_rn) for
+// every float whose bit pattern lies in [lo, hi); counts the mismatches and
+// keeps the smallest mismatching pattern.
+__global__ void k_check_div6(uint32_t lo, uint32_t hi, unsigned long long* mismatches, uint32_t* first_bad) {
+    unsigned long long local = 0;
+    uint32_t first = 0xFFFFFFFFu;
+    const uint64_t n = (uint64_t)(hi - lo);
+    const uint64_t step = (uint64_t)gridDim.x * blockDim.x;
+    for (uint64_t i = (uint64_t)blockIdx.x * blockDim.x + threadIdx.x; i < n; i += step) {
+        const uint32_t bits = lo + (uint32_t)i;
+        const float x = __uint_as_float(bits);
+        if (__float_as_uint(div6_rn(x)) != __float_as_uint(__fdiv_rn(x, 6.0f))) {
+            ++local;
+            first = min(first, bits);
+        }
+    }
+    if (local) {
+        atomicAdd(mismatches, local);
+        atomicMin(first_bad, first);
+    }
+}
+
 // Host Philox4x32-10 (Salmon et al., SC'11), for the RHT sign mask.
 uint32_t host_philox_word0(uint64_t seed) {
     uint32_t c0 = 0, c1 = 0, c2 = 0, c3 = 0;
@@ -816,6 +838,19 @@ nvfp4_status nvfp4_get_status(cudaStream_t stream) {
 size_t nvfp4_scale_bytes(int64_t rows, int64_t k) {
     if (rows <= 0 || k <= 0) return 0;
     return (size_t)(cdiv(rows, 128) * cdiv(k / 16, 4) * 512);
+}
+
+nvfp4_status nvfp4_debug_check_div6(uint32_t lo_bits, uint32_t hi_bits, unsigned long long* mismatches_dev,
+                                    uint32_t* first_bad_dev, cudaStream_t stream) {
+    if (lo_bits > hi_bits || hi_bits > 0x7F800000u || mismatches_dev == nullptr || first_bad_dev == nullptr)
+        return NVFP4_ERR_INVALID_ARG;
+    if (!aligned(mismatches_dev, 8) || !aligned(first_bad_dev, 4)) return NVFP4_ERR_MISALIGNED;
+    if (cudaMemsetAsync(mismatches_dev, 0, sizeof(unsigned long long), stream) != cudaSuccess ||
+        cudaMemsetAsync(first_bad_dev, 0xFF, sizeof(uint32_t), stream) != cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (lo_bits == hi_bits) return NVFP4_OK;
+    k_check_div6<<<device_sm_count() * 8, 256, 0, stream>>>(lo_bits, hi_bits, mismatches_dev, first_bad_dev);
+    return launch_status();
 }
 
 nvfp4_status nvfp4_debug_inject(int mode) {

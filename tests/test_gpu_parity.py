@@ -125,6 +125,23 @@ def test_quantize_tiny_amax(nv):
     assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "tiny amax")
 
 
+def test_quantize_op_order_golden(nv, golden_dir):
+    """The golden rows that separate the two plausible operation orders of the
+    block scale and of the element encode: the kernels give the bytes derived
+    by hand from t = fp32(fp32(amax_b / 6) * S_enc) and v = fp32(x * r_b)."""
+    from conftest import read_golden
+    import os
+    for kind, a, b, x, expect, _ in read_golden(os.path.join(golden_dir, "op_order.txt")):
+        row = np.zeros((1, 32), np.uint16)
+        row[0, 0], row[0, 16], row[0, 17] = int(a, 16), int(b, 16), int(x, 16)
+        q, _, _ = gpu_quantize(nv, dev_bf16(row))
+        if kind == "scale":
+            plain = oracle.unswizzle_scales(q.scales.cpu().numpy()[:oracle.scale_bytes(1, 32)], 1, 32)
+            assert int(plain[0, 1]) == int(expect, 0), (a, b)
+        else:
+            assert (int(q.codes.cpu().numpy()[0, 8]) >> 4) & 0xF == int(expect, 0), (a, b, x)
+
+
 # ------------------------------------------------------ 16x16 quantisation --
 SHAPES_2D = [(16, 16), (32, 48), (48, 80), (128, 256), (144, 272), (256, 1040), (80, 192)]
 

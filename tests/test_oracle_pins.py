@@ -682,3 +682,62 @@ def test_mx_gemm_matches_numpy_on_dequantised_operands():
     ref = da @ db.T
     assert np.allclose(y, ref, rtol=0, atol=1e-12 * np.abs(da) @ np.abs(db).T + 1e-300)
     assert np.allclose(ab, np.abs(da) @ np.abs(db).T, rtol=1e-12)
+
+
+# ------------------------------------------------------ operation order ----
+def _op_order_cases(golden_dir):
+    from conftest import read_golden
+    return [(k, int(a, 16), int(b, 16), int(x, 16), int(e, 0), int(o, 0))
+            for k, a, b, x, e, o in read_golden(os.path.join(golden_dir, "op_order.txt"))]
+
+
+def _op_order_row(a_bits, b_bits, x_bits):
+    row = np.zeros((1, 32), np.uint16)
+    row[0, 0], row[0, 16], row[0, 17] = a_bits, b_bits, x_bits
+    return row
+
+
+def test_op_order_cases_discriminate(golden_dir):
+    """Each golden case separates the two operation orders: computed here with
+    numpy binary32 arithmetic and torch's float -> E4M3 cast (independent of
+    the oracle), the left-to-right order gives the stated byte and the other
+    order the stated other byte."""
+    import torch
+    f32 = np.float32
+    bf = lambda b: np.array([b << 16], np.uint32).view(np.float32)[0]
+    e4m3 = lambda t: int(torch.tensor([float(t)]).to(torch.float8_e4m3fn).view(torch.uint8)[0])
+    e4m3v = lambda c: float(torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn).float()[0])
+    grid = [0.0, 0.5, 1.0, 1.5, 2.0, 3.0, 4.0, 6.0]
+
+    def e2m1(v):                                   # nearest, ties to the even code (v >= 0)
+        d = [abs(float(v) - g) for g in grid]
+        best = min(d)
+        return min(i for i in range(8) if d[i] == best and (d.count(best) == 1 or i % 2 == 0))
+
+    cases = _op_order_cases(golden_dir)
+    assert {c[0] for c in cases} == {"scale", "code"}
+    for kind, a, b, x, expect, other in cases:
+        A, ab, xv = bf(a), bf(b), bf(x)
+        s = f32(f32(2688.0) / A)
+        t_lr = f32(f32(ab / f32(6.0)) * s)
+        t_alt = f32(f32(ab * s) / f32(6.0))
+        if kind == "scale":
+            assert (e4m3(t_lr), e4m3(t_alt)) == (expect, other)
+        else:
+            sb = f32(e4m3v(e4m3(t_lr)))
+            v_lr = f32(xv * f32(s / sb))
+            v_alt = f32(f32(xv * s) / sb)
+            assert (e2m1(v_lr), e2m1(v_alt)) == (expect, other)
+
+
+def test_oracle_takes_the_specified_op_order(golden_dir):
+    """The oracle's block scale and element code on the golden rows are the
+    left-to-right ones: t = fp32(fp32(amax_b / 6) * S_enc) and
+    v = fp32(x * fp32(S_enc / s_b))."""
+    for kind, a, b, x, expect, other in _op_order_cases(golden_dir):
+        q = oracle.quantize(_op_order_row(a, b, x))
+        if kind == "scale":
+            assert int(q.scales_plain[0, 1]) == expect, (kind, hex(a), hex(b))
+        else:
+            code = (int(q.codes[0, 8]) >> 4) & 0xF        # element 17: high nibble of byte 8
+            assert code == expect, (kind, hex(a), hex(b), hex(x))
