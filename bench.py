@@ -51,6 +51,11 @@ WORKLOAD = ("linear-layer training step, 12B-hybrid FFN up-projection: X[8192x51
 # 1/16 B of scales; the 16x16 quantise with W^T and the dual-axis quantise
 # read once and write two operands
 B_AMAX, B_Q1D, B_Q2D_T, B_QDUAL = 2.0, 2.5625, 3.125, 3.125
+# the dequantiser reads codes and scales (0.5625 B) and writes bf16 (2 B)
+B_DEQ_BF16 = 2.5625
+# dense FP4 tensor throughput of one B300 as NVIDIA lists it for HGX B300
+# (108 PFLOP/s dense FP4 for 8 GPUs)
+FP4_NOMINAL_TFLOPS = 13500.0
 
 
 def load_peaks():
@@ -362,10 +367,12 @@ def oracle_step_sample(threads: int | None = None, rows: int = 16, pts: int = 25
         oracle.gemm_points(ca, swa, 1.0, cb, swb, 1.0, 64, 64, K, ms, ns, threads=thr)
         t_gemm += (time.perf_counter() - t0) * (M * N) / pts
     t_step = t_quant + t_gemm
+    q_bytes = (TOKENS * HIDDEN * 2 + FFN * HIDDEN + TOKENS * FFN * 2) * (B_AMAX + B_Q1D)
     return {"value": STEP_FLOPS / t_step / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
             "sample": f"{rows} rows of each of the 5 quantised operands (amax over a {rows * 64}-row "
                       f"slice) and {pts} output points of each of the 3 GEMMs (full K), "
                       "extrapolated by element and output counts to one step",
+            "quantize_gbs": q_bytes / t_quant / 1e9, "gemm_tflops": 3 * GEMM_FLOPS / t_gemm / 1e12,
             "seconds_per_step_extrapolated": t_step}
 
 
@@ -380,17 +387,35 @@ def run_reference(args):
     vals = vals[args.warmup:]
     v = statistics.median([c["value"] for c in vals])
     sec = statistics.median([c["seconds_per_step_extrapolated"] for c in vals])
+    wall = time.perf_counter() - t0
     out = {"metric": METRIC, "value": v, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
            "warmup": args.warmup, "ms_per_step": sec * 1e3, "higher_is_better": True,
            "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)", "data": "synthetic",
            "impl": "reference",
-           "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN},
+           # the oracle cannot run a whole step in bench time: each timed step is a bounded
+           # sample, and ms_per_step is the sample's time scaled by element and output counts
+           "extrapolated": True,
+           "sample_seconds_per_step": wall / max(1, args.warmup + args.steps),
+           "config": main_config(args),
            "cpu_baseline": {"value": v, "unit": "TFLOP/s", "cores": vals[0]["cores"], "kind": "oracle",
-                            "sample": vals[0]["sample"]},
+                            "sample": vals[0]["sample"], "quantize_gbs": vals[0]["quantize_gbs"],
+                            "gemm_tflops": vals[0]["gemm_tflops"]},
            "e2e": {"value": v, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
-           "wall_s": time.perf_counter() - t0}
+           "wall_s": wall}
     print(json.dumps(out))
     return 0
+
+
+def main_config(args, side_stream: bool = False) -> dict:
+    """The `config` object of the JSON line (the same keys for both arms)."""
+    return {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
+            "path": args.path,
+            "streams": ("2: forward W chain on a second stream beside the X chain; phase_ms overlap"
+                        if side_stream else "1"),
+            "sr": ("NVFP4_SR_HW: random bits in the hardware SR conversion's layout" if args.sr == "hw"
+                   else "NVFP4_SR: 16 independent Philox4x32-10 bits per element"),
+            "l2": "flushed before each step (256 MiB device write, untimed)",
+            "parallelism": f"replicas x{args.gpus}"}
 
 
 # -------------------------------------------------------------------- main --
@@ -403,6 +428,7 @@ def main():
     ap.add_argument("--e2e-steps", type=int, default=3)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-mx", action="store_true", help="skip the MXFP4 comparison timing")
+    ap.add_argument("--no-sweep", action="store_true", help="skip the quantise-only sweep (2^20..2^30)")
     ap.add_argument("--path", default="dual", choices=["dual", "separate"],
                     help="dual: X and dY read once each for both operands; separate: one call per operand")
     ap.add_argument("--streams", type=int, default=1, choices=[1, 2],
@@ -524,18 +550,12 @@ def main():
         "dtype": "fp4-e2m1 x e4m3-scaled, fp32 accumulate (bf16 in/out)",
         "data": "synthetic (seeded N(0,1)+outliers, N(0,0.02^2), 1e-3*t3)",
         "inputs_sha256": digests,
-        "config": {"workload": WORKLOAD, "tokens": TOKENS, "hidden": HIDDEN, "ffn": FFN,
-                   "path": args.path,
-                   "streams": ("2: forward W chain on a second stream beside the X chain; phase_ms overlap"
-                               if step.side is not None else "1"),
-                   "sr": ("NVFP4_SR_HW: random bits in the hardware SR conversion's layout" if args.sr == "hw"
-                          else "NVFP4_SR: 16 independent Philox4x32-10 bits per element"),
-                   "l2": "flushed before each step (256 MiB device write, untimed)",
-                   "parallelism": f"replicas x{world}"},
+        "config": main_config(args, step.side is not None),
         "gemm_tflops": gemm_tflops,
         "quantize_gbs": quant_gbs,
         "roofline": {"bound": "tensor", "achieved": gemm_tflops, "peak": fp4_peak, "unit": "TFLOP/s",
                      "frac": gemm_tflops / fp4_peak, "traffic": traffic.get("gemm_fwd"),
+                     "peak_nominal": FP4_NOMINAL_TFLOPS, "frac_nominal": gemm_tflops / FP4_NOMINAL_TFLOPS,
                      "traffic_note": "forward-GEMM launch (8192x20480x5120); achieved is the mean of the 3 GEMMs",
                      "kernel": "k_gemm_nvfp4_2sm",
                      "peak_source": f"{peak_src} bf16 burst {bf16_peak} TFLOP/s x 6 (nominal dense FP4:BF16)"},
@@ -560,9 +580,17 @@ def main():
         out["autograd"] = time_autograd(torch, step)
         if args.path == "dual" and args.sr == "philox16":
             out["sr_hw"] = time_sr_hw(nv, torch, step, out["phase_ms"], ms_per_step)
+    if world == 1:
+        out["calls"] = time_calls(nv, torch, step, hbm_peak)
+        out["library_gemm"] = time_library_gemm(torch, step)
+        if not args.no_sweep:
+            out["sweep"] = time_sweep(nv, torch, step, hbm_peak)
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         out["cpu_baseline"] = oracle_step_sample(rows=96, pts=2048)
         out["cpu_baseline"].pop("seconds_per_step_extrapolated", None)
+        one = oracle_step_sample(threads=1, rows=16, pts=256)
+        out["cpu_baseline"]["single_thread"] = {k: one[k] for k in ("value", "quantize_gbs", "gemm_tflops",
+                                                                      "cores", "sample")}
     if rank == 0:
         print(json.dumps(out))
     if world > 1:
@@ -655,6 +683,131 @@ def time_mxfp4(nv, torch, step, reps: int = 10) -> dict:
             "gemm_tflops": GEMM_FLOPS / (st.mean(g_ms) * 1e-3) / 1e12,
             "quantize_ms": {n: round(v, 4) for n, v in q_ms.items()},
             "quantize_gbs": sum(qbytes[n] * (2 + 0.5 + 1 / 32) for n in q_ms) / (sum(q_ms.values()) * 1e-3) / 1e9}
+
+
+def _timed_median(torch, step, fn, reps: int = 5) -> float:
+    """Median CUDA-event time (ms) of fn() on the current stream, L2 flushed
+    before each repetition."""
+    fn()
+    ts = []
+    for _ in range(reps):
+        step.flush_l2()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(); fn(); e1.record()
+        torch.cuda.synchronize()
+        ts.append(e0.elapsed_time(e1))
+    return statistics.median(ts)
+
+
+def time_calls(nv, torch, step, hbm_peak: float, reps: int = 5) -> dict:
+    """Every call of the C ABI at the step's shapes, one at a time (L2
+    flushed, median of `reps`): the separate-call path of the step (one amax
+    and one quantiser per operand, the wgrad operands read transposed with
+    the RHT), the dual-axis calls, the dequantiser and the three GEMMs.
+    GB/s are algorithmic bytes over time; fractions are of the HBM peak."""
+    rows = {}
+    calls = step.phases("separate") + [p for p in step.phases("dual") if p[0].startswith(("amax_dual", "quant_dual"))]
+    deq = torch.empty((TOKENS, HIDDEN), dtype=torch.bfloat16, device="cuda")
+    calls.append(("dequantize_x", lambda: step.nv.nvfp4_dequantize(step.qx, deq), TOKENS * HIDDEN * B_DEQ_BF16,
+                  False))
+    for name, call, nbytes, is_gemm in calls:
+        ms = _timed_median(torch, step, call, reps)
+        if is_gemm:
+            t = GEMM_FLOPS / (ms * 1e-3) / 1e12
+            rows[name] = {"ms": round(ms, 4), "tflops": round(t, 1)}
+        else:
+            g = nbytes / (ms * 1e-3) / 1e9
+            rows[name] = {"ms": round(ms, 4), "gbs": round(g, 1), "frac_hbm": round(g / hbm_peak, 3)}
+    st = nv.nvfp4_get_status()
+    if st != nv.NVFP4_OK:
+        raise SystemExit(f"device status after the per-call timing: {nv.status_string(st)}")
+    return rows
+
+
+def time_library_gemm(torch, step, reps: int = 5) -> dict:
+    """cuBLASLt's NVFP4 GEMM (through torch.nn.functional.scaled_mm, 1x16
+    E4M3 block scales in the same swizzled layout) on the step's quantised
+    operands, as a library comparison beside nvfp4_gemm.  Block scales only:
+    the tensor scales (alpha) are left out, which does not change the work."""
+    import torch.nn.functional as F
+    out = {}
+    try:
+        for name, a, b, d in (("fwd", step.qx, step.qw, step.y), ("dgrad", step.qdy, step.qwt, step.dx),
+                              ("wgrad", step.qdyt, step.qxt, step.dw)):
+            A = a.codes.view(torch.float4_e2m1fn_x2)
+            B = b.codes.view(torch.float4_e2m1fn_x2).t()
+            sa, sb = a.scales.view(torch.float8_e4m3fn), b.scales.view(torch.float8_e4m3fn)
+            fn = lambda: F.scaled_mm(A, B, sa, F.ScalingType.BlockWise1x16, sb, F.ScalingType.BlockWise1x16,
+                                     F.SwizzleType.SWIZZLE_32_4_4, F.SwizzleType.SWIZZLE_32_4_4,
+                                     output_dtype=torch.bfloat16)
+            ms = _timed_median(torch, step, fn, reps)
+            out[name] = {"ms": round(ms, 4), "tflops": round(GEMM_FLOPS / (ms * 1e-3) / 1e12, 1)}
+        out["mean_tflops"] = round(statistics.mean(v["tflops"] for v in out.values()), 1)
+        out["library"] = "cuBLASLt NVFP4 block-scaled GEMM via torch.nn.functional.scaled_mm"
+    except Exception as e:                        # a torch without NVFP4 scaled_mm
+        out = {"unavailable": f"{type(e).__name__}: {str(e)[:200]}"}
+    return out
+
+
+def time_sweep(nv, torch, step, hbm_peak: float, reps: int = 5) -> dict:
+    """The quantise-only sweep: bf16 tensors of n = 2^20 .. 2^30 elements as
+    [n/8192 x 8192], Student-t(3) (unscaled) and N(0,1) with 0.05% of the
+    entries x100, quantised in every combination of {1x16, 16x16} x
+    {RNE, NVFP4_SR} x {no RHT, RHT-16}: amax GB/s (2 B/element) per (size,
+    RHT), quantise GB/s (amax given, 2.5625 B/element) per point, each the
+    median of `reps` L2-flushed launches.  Inputs are drawn on the device
+    (seeded) because the host generators take minutes at 2^30; the n-element
+    tensor is the first n/8192 rows of the 2^30-element one."""
+    import synth
+    K = 8192
+    rows_max = (1 << 30) // K
+    amax = torch.empty((2,), dtype=torch.float32, device="cuda")
+    cols = ["log2_n", "dist", "block", "round", "rht", "quant_ms", "quant_gbs", "quant_frac",
+            "amax_ms", "amax_gbs", "amax_quant_gbs"]
+    out_rows = []
+    for dist in ("t3", "normal_outliers"):
+        x = (synth.student_t_bf16_device((rows_max, K), 5, 1.0) if dist == "t3"
+             else synth.normal_bf16_device((rows_max, K), 105, 1.0, 0.0005, 100.0))
+        for e in range(20, 31):
+            n = 1 << e
+            v = x[: n // K]
+            t_amax = {}
+            for rht in (False, True):
+                m = step.mask if rht else 0
+                t_amax[rht] = _timed_median(torch, step, lambda: nv.nvfp4_amax(v, m, amax[0:1]), reps)
+            for block2d in (False, True):
+                q = nv.QTensor(n // K, K, block2d)
+                for sr in (False, True):
+                    rnd = nv.NVFP4_SR if sr else nv.NVFP4_RNE
+                    for rht in (False, True):
+                        m = step.mask if rht else 0
+                        nv.nvfp4_amax(v, m, amax[0:1])
+                        if rht:
+                            f = lambda: nv.nvfp4_rht_quantize(v, m, amax[0:1], rnd, SR_SEED, 1, q)
+                        elif block2d:
+                            f = lambda: nv.nvfp4_quantize_2d(v, amax[0:1], rnd, SR_SEED, 1, q)
+                        else:
+                            f = lambda: nv.nvfp4_quantize_1d(v, amax[0:1], rnd, SR_SEED, 1, q)
+                        tq = _timed_median(torch, step, f, reps)
+                        gq = n * B_Q1D / (tq * 1e-3) / 1e9
+                        ga = n * B_AMAX / (t_amax[rht] * 1e-3) / 1e9
+                        both = n * (B_AMAX + B_Q1D) / ((tq + t_amax[rht]) * 1e-3) / 1e9
+                        out_rows.append([e, dist, "16x16" if block2d else "1x16", "SR" if sr else "RNE",
+                                         int(rht), round(tq, 4), round(gq, 1), round(gq / hbm_peak, 3),
+                                         round(t_amax[rht], 4), round(ga, 1), round(both, 1)])
+                del q
+        del x
+        torch.cuda.empty_cache()
+    st = nv.nvfp4_get_status()
+    if st != nv.NVFP4_OK:
+        raise SystemExit(f"device status after the sweep: {nv.status_string(st)}")
+    big = [r for r in out_rows if r[0] == 30]
+    return {"columns": cols, "rows": out_rows, "unit": "GB/s", "hbm_peak_gbs": hbm_peak,
+            "at_2^30": {"quant_gbs_min": min(r[6] for r in big), "quant_gbs_max": max(r[6] for r in big),
+                        "quant_frac_median": statistics.median(r[7] for r in big),
+                        "amax_gbs_min": min(r[9] for r in big)},
+            "inputs": "seeded, drawn on the device (torch CUDA generator): t3 seed 5, normal seed 105",
+            "l2": "flushed before each launch"}
 
 
 def load_traffic():

@@ -91,3 +91,62 @@ def weights(seed: int, ffn: int = FFN, hidden: int = HIDDEN):
 def grad_output(seed: int, tokens: int = TOKENS, ffn: int = FFN):
     """dY [tokens x ffn] ~ 1e-3 * Student-t(3)."""
     return student_t_bf16((tokens, ffn), seed, 3, 1e-3)
+
+
+# --- device-side generators (for inputs too large to draw on the host) -----
+# Same distributions as above, drawn with torch's seeded CUDA generator
+# (Philox-based) instead of numpy's PCG64, so the values differ from the host
+# generators' but the recipe is the same:
+#   normal:    N(0, sigma^2), then round(frac * n) entries chosen uniformly
+#              without replacement (the first entries of a seeded random
+#              permutation) multiplied by outlier_mult;
+#   student_t: z / sqrt(chi2_3 / 3) with chi2_3 = z1^2 + z2^2 + z3^2 (the
+#              definition of a chi-square variable with 3 degrees of freedom),
+#              times scale;
+# then float32 -> bf16 round to nearest even.  Generation runs in row chunks
+# to bound the temporary memory.
+def _device_generator(seed: int, device: str):
+    import torch
+    g = torch.Generator(device=device)
+    g.manual_seed(seed)
+    return g
+
+
+def normal_bf16_device(shape, seed: int, sigma: float = 1.0, outlier_frac: float = 0.0,
+                       outlier_mult: float = 1.0, device: str = "cuda"):
+    import torch
+    rows, cols = shape
+    g = _device_generator(seed, device)
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
+    chunk = max(1, (1 << 26) // cols)
+    n = rows * cols
+    n_out = int(round(outlier_frac * n))
+    idx = torch.randperm(n, generator=g, device=device)[:n_out] if n_out else None
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        x = torch.randn((r1 - r0, cols), generator=g, dtype=torch.float32, device=device)
+        if sigma != 1.0:
+            x *= sigma
+        if idx is not None:
+            lo, hi = r0 * cols, r1 * cols
+            sel = idx[(idx >= lo) & (idx < hi)] - lo
+            x.view(-1)[sel] *= outlier_mult
+        out[r0:r1] = x.to(torch.bfloat16)
+    return out
+
+
+def student_t_bf16_device(shape, seed: int, scale: float = 1e-3, device: str = "cuda"):
+    import torch
+    rows, cols = shape
+    g = _device_generator(seed, device)
+    out = torch.empty((rows, cols), dtype=torch.bfloat16, device=device)
+    chunk = max(1, (1 << 25) // cols)
+    for r0 in range(0, rows, chunk):
+        r1 = min(rows, r0 + chunk)
+        z = torch.randn((4, r1 - r0, cols), generator=g, dtype=torch.float32, device=device)
+        chi2 = z[1] * z[1] + z[2] * z[2] + z[3] * z[3]
+        x = z[0] / torch.sqrt(chi2 / 3.0)
+        if scale != 1.0:
+            x *= scale
+        out[r0:r1] = x.to(torch.bfloat16)
+    return out

@@ -23,6 +23,15 @@ def test_reference_arm_json_line():
     assert d["cpu_baseline"]["cores"] >= 1 and d["cpu_baseline"]["sample"]
     assert d["e2e"] == {"value": d["value"], "unit": d["unit"], "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}
     assert d["config"]["workload"]
+    # the oracle's step time is a scaled-up sample, and says so
+    assert d["extrapolated"] is True and d["sample_seconds_per_step"] > 0
+    # the same config keys as the device arm's line
+    import argparse
+    sys.path.insert(0, ROOT)
+    import bench
+    ns = argparse.Namespace(gpus=1, path="dual", sr="philox16")
+    assert d["config"] == bench.main_config(ns)
+    assert d["cpu_baseline"]["quantize_gbs"] > 0 and d["cpu_baseline"]["gemm_tflops"] > 0
 
 
 def test_input_digests_are_stable():

@@ -1,11 +1,14 @@
-"""Quantise-only sweep: bf16 tensors of n = 2^20 ... 2^28 elements shaped
+"""Quantise-only sweep: bf16 tensors of n = 2^20 ... 2^30 elements shaped
 [n/8192 x 8192] (k = 8192), drawn as Student-t(3) (unscaled) and as N(0,1)
 with 0.05% of the entries x100, each quantised in every combination of
 {1x16, 16x16 blocks} x {RNE, stochastic (NVFP4_SR)} x {no RHT, RHT-16}.
 
 The amax is compared exactly.  The oracle cannot quantise 2^28 elements per
 case in test time, so codes and scales are compared bit for bit on sampled
-row ranges (aligned to 16), with the full tensor's amax.
+row ranges (aligned to 16), with the full tensor's amax.  Sizes up to 2^28
+are drawn on the host (numpy); 2^29 and 2^30 are drawn on the device by the
+seeded device generators (the host ones take minutes there) and copied to
+the host for the oracle.
 """
 import itertools
 
@@ -71,5 +74,28 @@ def test_sweep_point(nv, n, dist):
         assert amax == ref_amax[mask], what
         r = sample_ranges(rows, 3, 16, 16, n.bit_length() + int(block2d) + 2 * int(sr))
         ref = oracle.quantize(x, block2d=block2d, rht_mask=mask, amax_v=amax, sr=sr, seed=seed, stream_id=1,
+                              ranges=r, swizzle=False)
+        check_sampled(got, ref, r, rows, K, what)
+
+
+LARGE = [1 << 29, 1 << 30]
+
+
+@pytest.mark.parametrize("n", LARGE)
+@pytest.mark.parametrize("dist", ["t3", "normal_outliers"])
+def test_sweep_point_large(nv, n, dist):
+    rows, seed = n // K, n.bit_length()
+    d = (synth.student_t_bf16_device((rows, K), seed, 1.0) if dist == "t3"
+         else synth.normal_bf16_device((rows, K), seed + 100, 1.0, 0.0005, 100.0))
+    x = d.view(torch.int16).cpu().numpy().view(np.uint16)
+    ref_amax = {m: oracle.amax(x, rht_mask=m) for m in (0, MASK)}
+    for block2d, sr, mask in itertools.product((False, True), (False, True), (0, MASK)):
+        what = f"n=2^{n.bit_length() - 1} {dist} {'16x16' if block2d else '1x16'} {'SR' if sr else 'RNE'} " \
+               f"rht={mask:#x}"
+        qseed = 1000 + n.bit_length()
+        amax, got = quantise_point(nv, d, rows, block2d, sr, mask, qseed)
+        assert amax == ref_amax[mask], what
+        r = sample_ranges(rows, 3, 16, 16, n.bit_length() + int(block2d) + 2 * int(sr))
+        ref = oracle.quantize(x, block2d=block2d, rht_mask=mask, amax_v=amax, sr=sr, seed=qseed, stream_id=1,
                               ranges=r, swizzle=False)
         check_sampled(got, ref, r, rows, K, what)
