@@ -255,8 +255,11 @@ const char* nvfp4_status_string(nvfp4_status s);
  * first tile.  That tile's bounded wait expires after about 2 s, the kernel
  * drains its other copies and returns, and nvfp4_get_status then reports
  * NVFP4_ERR_TIMEOUT; the amax written by that call is undefined.  The
- * injection applies once and then clears.  mode 0 clears it.  Returns
- * NVFP4_ERR_INVALID_ARG for any other mode. */
+ * injection applies once and then clears.  mode 2: the next
+ * nvfp4_quantize_dual takes its general path for Philox block indices of 64
+ * bits (used only for operands of more than 2^35 elements) instead of the
+ * path with 32-bit indices; the outputs must not change.  mode 0 clears
+ * both.  Returns NVFP4_ERR_INVALID_ARG for any other mode. */
 nvfp4_status nvfp4_debug_inject(int mode);
 
 /* Test-only check of the block-scale arithmetic: the kernels compute

@@ -296,9 +296,10 @@ def nvfp4_get_status(stream=None) -> int:
 
 
 def nvfp4_debug_inject(mode: int) -> int:
-    """Test-only fault injection: mode 1 makes the next streamed amax launch
-    skip the copy of its first tile, so that its bounded wait expires and
-    nvfp4_get_status reports NVFP4_ERR_TIMEOUT (see include/nvfp4.h)."""
+    """Test-only: mode 1 makes the next streamed amax launch skip the copy of
+    its first tile, so that its bounded wait expires and nvfp4_get_status
+    reports NVFP4_ERR_TIMEOUT; mode 2 makes the next dual quantise take its
+    64-bit Philox block-index path; mode 0 clears both (see include/nvfp4.h)."""
     return _check(int(lib.nvfp4_debug_inject(mode)), "nvfp4_debug_inject")
 
 

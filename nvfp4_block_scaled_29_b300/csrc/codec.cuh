@@ -110,6 +110,31 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const uint32_t* key) {
     return c;
 }
 
+// Philox4x32-10 of the counter (g, 0, stream_lo, stream_hi) -- a block index
+// below 2^32 -- with the counter's constant words folded into rounds 0 and 1
+// on the host: pre = {A2, B1, B2, B3} where, with t = stream_lo * M1,
+// A0 = hi(t) ^ k0, A1 = lo(t), A2 = stream_hi ^ k1, B1 = A1 ^ k0', B2 =
+// hi(A0 * M0) ^ k1', B3 = lo(A0 * M0) (k, k' the round-0 and round-1 keys).
+// Round 0 then leaves (A0, A1, hi(g M0) ^ A2, lo(g M0)) and round 1 (hi(c2 M1)
+// ^ B1, lo(c2 M1), c3 ^ B2, B3); rounds 2-9 run as usual.  NOT: the outputs
+// complemented as in philox4x32_10_not (round-9 keys given complemented).
+template <bool NOT>
+__device__ __forceinline__ uint4 philox4x32_10_g32(uint32_t g, const uint32_t* key, const uint32_t* pre) {
+    const uint64_t p = (uint64_t)g * 0xD2511F53u;
+    const uint32_t c2 = (uint32_t)(p >> 32) ^ pre[0];
+    const uint64_t q = (uint64_t)c2 * 0xCD9E8D57u;
+    uint4 c = make_uint4((uint32_t)(q >> 32) ^ pre[1], (uint32_t)q, (uint32_t)p ^ pre[2], pre[3]);
+#pragma unroll
+    for (int round = 2; round < 10; ++round) {
+        const uint64_t p0 = (uint64_t)c.x * 0xD2511F53u;
+        const uint64_t p1 = (uint64_t)c.z * 0xCD9E8D57u;
+        const uint32_t lo1 = (uint32_t)p1, lo0 = (uint32_t)p0;
+        c = make_uint4((uint32_t)(p1 >> 32) ^ c.y ^ key[2 * round], (NOT && round == 9) ? ~lo1 : lo1,
+                       (uint32_t)(p0 >> 32) ^ c.w ^ key[2 * round + 1], (NOT && round == 9) ? ~lo0 : lo0);
+    }
+    return c;
+}
+
 // NVFP4_SR_HW: random words of the 16 elements idx = 16*g .. 16*g+15 of a
 // quantised operand: the Philox block of counter (g, stream_id); element idx
 // reads word (idx % 16) / 4.
@@ -173,14 +198,31 @@ __device__ __forceinline__ uint32_t e2m1_sr_rp_at(float v, uint32_t rp_word, boo
 }
 
 // Eight values -> eight NVFP4_SR codes (element 0 in the lowest nibble), rp =
-// the complemented Philox block of these 8 elements (sr_rp8).  Two conversion
-// results join into one word with codes c0..c3 in the low nibbles of bytes
-// 0..3; t | (t >> 4) then holds c0 | c1 << 4 in byte 0 and c2 | c3 << 4 in
-// byte 2, and one byte permutation gathers those bytes of the two halves.
+// the complemented Philox block of these 8 elements (sr_rp8).  Each
+// conversion rounds two values (e2m1x2_sr_rp, in one asm block with its
+// 16-bit results joined pairwise by mov.b32): the joined word t holds codes
+// c0..c3 in the low nibbles of bytes 0..3 with the high nibbles zero, so
+// t + (t >> 4) -- computed as t + umulhi(t, 2^28), an integer multiply-add
+// rather than a shift and an OR -- holds c0 | c1 << 4 in byte 0 and
+// c2 | c3 << 4 in byte 2, and one byte permutation gathers those bytes.
 __device__ __forceinline__ uint32_t e2m1x8_sr_cvt(const float* v, uint4 rp) {
-    const uint32_t t01 = __byte_perm(e2m1x2_sr_rp(v[0], v[1], rp.x), e2m1x2_sr_rp(v[2], v[3], rp.y), 0x5410u);
-    const uint32_t t23 = __byte_perm(e2m1x2_sr_rp(v[4], v[5], rp.z), e2m1x2_sr_rp(v[6], v[7], rp.w), 0x5410u);
-    return __byte_perm(t01 | (t01 >> 4), t23 | (t23 >> 4), 0x6420u);
+    uint32_t t01, t23;
+    asm("{\n\t.reg .b16 d0, d1, d2, d3;\n\t.reg .b32 r0, r1, r2, r3;\n\t.reg .f32 z;\n\t"
+        "mov.f32 z, 0f00000000;\n\t"
+        "prmt.b32 r0, %10, 0, 0x3120;\n\t"
+        "prmt.b32 r1, %11, 0, 0x3120;\n\t"
+        "prmt.b32 r2, %12, 0, 0x3120;\n\t"
+        "prmt.b32 r3, %13, 0, 0x3120;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 d0, {z, %3, z, %2}, r0;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 d1, {z, %5, z, %4}, r1;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 d2, {z, %7, z, %6}, r2;\n\t"
+        "cvt.rs.satfinite.e2m1x4.f32 d3, {z, %9, z, %8}, r3;\n\t"
+        "mov.b32 %0, {d0, d1};\n\t"
+        "mov.b32 %1, {d2, d3};\n\t}"
+        : "=r"(t01), "=r"(t23)
+        : "f"(v[0]), "f"(v[1]), "f"(v[2]), "f"(v[3]), "f"(v[4]), "f"(v[5]), "f"(v[6]), "f"(v[7]),
+          "r"(rp.x), "r"(rp.y), "r"(rp.z), "r"(rp.w));
+    return __byte_perm(t01 + __umulhi(t01, 0x10000000u), t23 + __umulhi(t23, 0x10000000u), 0x6420u);
 }
 
 // --------------------------- stochastic E2M1, hardware layout (NVFP4_SR_HW) --

@@ -18,6 +18,7 @@
 #pragma once
 #include <cuda.h>
 #include <cstdint>
+#include <type_traits>
 #include "codec.cuh"
 #include "ptx.cuh"
 #include "quantize.cuh"
@@ -50,18 +51,24 @@ __device__ __forceinline__ void block_max2_to_global(uint32_t m0, float* out0, u
 
 // ======================================================== dual quantise ====
 // Persistent CTAs walk 64-row x 256-column tiles of S through a ring of
-// kDqStages shared-memory slots, so that up to kDqStages - 1 tiles per CTA
-// are in flight while one is encoded.  A tile arrives as four 64 x 64 boxes
-// (one TMA copy each, 128-byte swizzle: 16-byte chunk c of row r of a box
-// sits at chunk c ^ (r & 7)); rows and columns beyond S read as zeros.
-// Row tiles cover S's 128-padded row count, so that the padding rows' scale
-// words are written too.
-//  * row-wise items (tile row r, group g of 4 blocks = box g): 16-byte reads;
+// kDqStages shared-memory slots.  A tile arrives as four 64 x 64 boxes (one
+// TMA copy each, 128-byte swizzle: 16-byte chunk c of row r of a box sits at
+// chunk c ^ (r & 7)); rows and columns beyond S read as zeros.  Row tiles
+// cover S's 128-padded row count, so that the padding rows' scale words are
+// written too.
+//  * warp 8 (one lane) feeds the ring: it refills slot s as soon as all eight
+//    encoding warps have arrived on empty[s];
+//  * warps 0-7 encode.  They wait for full[s] and release the slot each on
+//    its own, never for one another, so they drift apart in phase and the
+//    Philox (integer), Hadamard (FP32) and conversion work of different warps
+//    overlap on the SM's pipes.
+// Each encoding thread takes one item of each kind per tile:
+//  * row-wise item (tile row r, group g of 4 blocks = box g): 16-byte reads;
 //    the 8 lanes of a quarter warp read one chunk of 8 consecutive rows,
 //    which the swizzle spreads over all banks;
-//  * column-wise items (column pair, half h of the tile's rows = 2 blocks):
+//  * column-wise item (column pair, half h of the tile's rows = 2 blocks):
 //    4-byte reads, a warp reading the 128 bytes of one box row.
-// Both item kinds carry 64 elements, one of each per thread.
+// Both item kinds carry 64 elements.
 struct DualArgs {
     QuantArgs row;      // logical S [R x C]: x, rows = R, k = C, ld; codes/scales of out
     QuantArgs col;      // logical S^T [C x R]: rows = C, k = R; codes/scales of out_t; rht
@@ -71,7 +78,9 @@ constexpr int kDqRows = 64, kDqCols = 256, kDqBoxCols = 64;
 constexpr int kDqBoxBytes = kDqRows * kDqBoxCols * 2;            // 8 KB
 constexpr int kDqTileBytes = (kDqCols / kDqBoxCols) * kDqBoxBytes;  // 32 KB
 constexpr int kDqStages = 3;
-constexpr int kDqSmem = kDqStages * kDqTileBytes + 1024 + 64;      // + 1024-byte alignment slack, barriers
+constexpr int kDqConsumerWarps = 8;
+constexpr int kDqThreads = (kDqConsumerWarps + 1) * 32;
+constexpr int kDqSmem = kDqStages * kDqTileBytes + 1024 + 128;     // + 1024-byte alignment slack, barriers
 
 // Byte offset of 16-byte chunk c of row r of box b in a tile slot.
 __device__ __forceinline__ uint32_t dq_chunk(int b, int r, int c) {
@@ -80,11 +89,12 @@ __device__ __forceinline__ uint32_t dq_chunk(int b, int r, int c) {
 
 // SR1, SR2: rounding of each operand, 0 = RNE, 1 = NVFP4_SR, 2 = NVFP4_SR_HW.
 template <int SR1, int SR2, bool RHT2>
-__global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_constant__ CUtensorMap map,
-                                                                 const __grid_constant__ DualArgs d) {
+__global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_constant__ CUtensorMap map,
+                                                              const __grid_constant__ DualArgs d) {
     extern __shared__ uint8_t dq_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(dq_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + kDqStages * kDqTileBytes);
+    uint64_t* empty = full + kDqStages;
     __shared__ float rtab1[128], rtab2[128];
     __shared__ int abort_flag;
     const QuantArgs& a1 = d.row;
@@ -102,26 +112,45 @@ __global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_co
     const int64_t row_tiles = rows_pad / kDqRows;
     const int64_t col_tiles = (C + kDqCols - 1) / kDqCols;
     const int64_t ntiles = row_tiles * col_tiles;
+    const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kDqStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < kDqStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kDqConsumerWarps);
+        }
         abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map);
     }
     __syncthreads();
-    auto issue = [&](int64_t t, int s) {
-        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
-        mbar_arrive_expect_tx(&full[s], kDqTileBytes);
+
+    if (warp == kDqConsumerWarps) {
+        // ------------------------------------------------------ producer --
+        if ((threadIdx.x & 31) == 0) {
+            int i = 0;
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % kDqStages;
+                if (i >= kDqStages &&
+                    !mbar_wait_bounded(&empty[s], (uint32_t)(i / kDqStages - 1) & 1u, &abort_flag))
+                    break;
+                if (abort_flag) break;
+                const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+                mbar_arrive_expect_tx(&full[s], kDqTileBytes);
 #pragma unroll
-        for (int b = 0; b < kDqCols / kDqBoxCols; ++b)
-            tma_load_2d(ring + s * kDqTileBytes + b * kDqBoxBytes, &map, &full[s],
-                        (int32_t)(tc * kDqCols + b * kDqBoxCols), (int32_t)(tr * kDqRows));
-    };
-    if (threadIdx.x == 0)
-        for (int s = 0; s < kDqStages; ++s) {
-            const int64_t t = (int64_t)blockIdx.x + (int64_t)s * gridDim.x;
-            if (t < ntiles) issue(t, s);
+                for (int b = 0; b < kDqCols / kDqBoxCols; ++b)
+                    tma_load_2d(ring + s * kDqTileBytes + b * kDqBoxBytes, &map, &full[s],
+                                (int32_t)(tc * kDqCols + b * kDqBoxCols), (int32_t)(tr * kDqRows));
+            }
+            // every issued copy has landed before the CTA exits: copies before
+            // the last kDqStages were waited for by the encoding warps (their
+            // slots were released), the last kDqStages are waited for here
+            for (int k = 1; k <= kDqStages && i - k >= 0; ++k) {
+                const int ii = i - k;
+                mbar_wait_bounded(&full[ii % kDqStages], (uint32_t)(ii / kDqStages) & 1u, nullptr);
+            }
         }
+        return;
+    }
 
     // per-thread item coordinates (fixed over tiles)
     const int ri = threadIdx.x;
@@ -135,127 +164,124 @@ __global__ void __launch_bounds__(kQuantThreads, 2) k_quant_dual(const __grid_co
     const int64_t nkb_t = R >> 4, ngroups_t = (nkb_t + 3) >> 2;  // column-wise operand
     const int64_t rows_pad_t = (C + 127) & ~int64_t(127);
 
-    int i = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-        const int s = i % kDqStages;
-        const uint32_t ph = (uint32_t)(i / kDqStages) & 1u;
-        const bool ok = mbar_wait_bounded(&full[s], ph, &abort_flag);
-        __syncthreads();                                         // every thread saw the same outcome
-        if (abort_flag || !ok) break;
-        const uint8_t* tile = ring + s * kDqTileBytes;
-        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
-        const int64_t r0 = tr * kDqRows, c0 = tc * kDqCols;
+    // The encoding loop, instantiated twice: with G32 the Philox block
+    // indices are known to stay below 2^32 (the usual case, decided once per
+    // launch) and the counter's constant words come folded.
+    auto encode_tiles = [&](auto g32) {
+        constexpr bool G32 = decltype(g32)::value;
+        int i = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int s = i % kDqStages;
+            const uint32_t ph = (uint32_t)(i / kDqStages) & 1u;
+            // warp-uniform outcome: a lane that timed out stops its whole warp
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[s], ph, &abort_flag))) break;
+            const uint8_t* tile = ring + s * kDqTileBytes;
+            const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+            const int64_t r0 = tr * kDqRows, c0 = tc * kDqCols;
 
-        // ---- row-wise operand
-        if (ok1) {
-            const int64_t row = r0 + rr;
-            const int64_t G = c0 / 64 + rg;
-            if (G < ngroups) {
-                uint32_t* sdst = reinterpret_cast<uint32_t*>(a1.scales + scale_offset(row, G * 4, ngroups));
-                if (row >= R) {
-                    *sdst = 0u;
-                } else {
-                    const int nblk = (int)min64(4, nkb - G * 4);
-                    uint32_t sw = 0, cw[8];
-#pragma unroll
-                    for (int b = 0; b < 4; ++b) {
-                        cw[2 * b] = cw[2 * b + 1] = 0u;
-                        if (b < nblk) {
-                            const uint4 lo = *reinterpret_cast<const uint4*>(tile + dq_chunk(rg, rr, 2 * b));
-                            const uint4 hi = *reinterpret_cast<const uint4*>(tile + dq_chunk(rg, rr, 2 * b + 1));
-                            float v[16];
-                            unpack8(lo, v);
-                            unpack8(hi, v + 8);
-                            uint32_t sb;
-                            encode_block16<false, SR1 != 0, SR1 == 2>(v, s1, rtab1, (uint64_t)(row * C + G * 64 + b * 16), a1, &sb,
-                                                       &cw[2 * b], &cw[2 * b + 1], absmax_bits16_packed(lo, hi));
-                            sw |= sb << (8 * b);
-                        }
-                    }
-                    uint8_t* cdst = a1.codes + row * (C >> 1) + G * 32;
-                    if (nblk == 4 && (C & 31) == 0) {
-                        reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-                        reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
+            // ---- row-wise operand
+            if (ok1) {
+                const int64_t row = r0 + rr;
+                const int64_t G = c0 / 64 + rg;
+                if (G < ngroups) {
+                    uint32_t* sdst = reinterpret_cast<uint32_t*>(a1.scales + scale_offset(row, G * 4, ngroups));
+                    if (row >= R) {
+                        *sdst = 0u;
                     } else {
+                        const int nblk = (int)min64(4, nkb - G * 4);
+                        uint32_t sw = 0, cw[8];
 #pragma unroll
-                        for (int b = 0; b < 4; ++b)
-                            if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-                    }
-                    *sdst = sw;
-                }
-            }
-        }
-
-        // ---- column-wise operand: logical rows cc, cc + 1 of S^T, blocks kb0, kb0 + 1
-        if (ok2) {
-            const int64_t cc = c0 + 2 * pc;
-            const int64_t G = r0 / 64;
-            const int64_t kb0 = G * 4 + 2 * ch;
-            if (G < ngroups_t && cc < rows_pad_t) {
-                uint16_t* s0 = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc, kb0, ngroups_t));
-                uint16_t* s1p = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc + 1, kb0, ngroups_t));
-                const int nblk = (int)max64(0, min64(2, nkb_t - kb0));
-                if (cc >= C || nblk == 0) {                      // C is even: both rows are padding
-                    *s0 = 0;
-                    *s1p = 0;
-                } else {
-                    uint32_t sw0 = 0, sw1 = 0, c0w[4], c1w[4];
-#pragma unroll
-                    for (int b = 0; b < 2; ++b) {
-                        c0w[2 * b] = c0w[2 * b + 1] = c1w[2 * b] = c1w[2 * b + 1] = 0u;
-                        if (b < nblk) {
-                            uint32_t w[16];
-#pragma unroll
-                            for (int u = 0; u < 16; ++u) {
-                                const int r = ch * 32 + b * 16 + u;
-                                w[u] = *reinterpret_cast<const uint32_t*>(tile + dq_chunk(pb, r, pchunk) + pword * 4);
+                        for (int b = 0; b < 4; ++b) {
+                            cw[2 * b] = cw[2 * b + 1] = 0u;
+                            if (b < nblk) {
+                                const uint4 lo = *reinterpret_cast<const uint4*>(tile + dq_chunk(rg, rr, 2 * b));
+                                const uint4 hi = *reinterpret_cast<const uint4*>(tile + dq_chunk(rg, rr, 2 * b + 1));
+                                float v[16];
+                                unpack8(lo, v);
+                                unpack8(hi, v + 8);
+                                uint32_t sb;
+                                encode_block16<false, SR1 != 0, SR1 == 2, G32>(
+                                    v, s1, rtab1, (uint64_t)(row * C + G * 64 + b * 16), a1, &sb, &cw[2 * b],
+                                    &cw[2 * b + 1], absmax_bits16_packed(lo, hi));
+                                sw |= sb << (8 * b);
                             }
-                            const int64_t kc = (kb0 + b) * 16;
-                            float v[16];
-                            uint32_t sb;
-#pragma unroll
-                            for (int u = 0; u < 16; ++u) v[u] = bf16_lo(w[u]);
-                            encode_block16<RHT2, SR2 != 0, SR2 == 2>(v, s2, rtab2, (uint64_t)(cc * R + kc), a2, &sb, &c0w[2 * b],
-                                                      &c0w[2 * b + 1]);
-                            sw0 |= sb << (8 * b);
-#pragma unroll
-                            for (int u = 0; u < 16; ++u) v[u] = bf16_hi(w[u]);
-                            encode_block16<RHT2, SR2 != 0, SR2 == 2>(v, s2, rtab2, (uint64_t)((cc + 1) * R + kc), a2, &sb,
-                                                      &c1w[2 * b], &c1w[2 * b + 1]);
-                            sw1 |= sb << (8 * b);
                         }
-                    }
-#pragma unroll
-                    for (int q = 0; q < 2; ++q) {
-                        const uint32_t* cw = q ? c1w : c0w;
-                        uint8_t* cdst = a2.codes + (cc + q) * (R >> 1) + kb0 * 8;
-                        if (nblk == 2 && (R & 31) == 0) {
-                            *reinterpret_cast<uint4*>(cdst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                        uint8_t* cdst = a1.codes + row * (C >> 1) + G * 32;
+                        if (nblk == 4 && (C & 31) == 0) {
+                            reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                            reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
                         } else {
 #pragma unroll
-                            for (int b = 0; b < 2; ++b)
+                            for (int b = 0; b < 4; ++b)
                                 if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
                         }
+                        *sdst = sw;
                     }
-                    *s0 = (uint16_t)sw0;
-                    *s1p = (uint16_t)sw1;
                 }
             }
+
+            // ---- column-wise operand: logical rows cc, cc + 1 of S^T, blocks kb0, kb0 + 1
+            if (ok2) {
+                const int64_t cc = c0 + 2 * pc;
+                const int64_t G = r0 / 64;
+                const int64_t kb0 = G * 4 + 2 * ch;
+                if (G < ngroups_t && cc < rows_pad_t) {
+                    uint16_t* s0 = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc, kb0, ngroups_t));
+                    uint16_t* s1p = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc + 1, kb0, ngroups_t));
+                    const int nblk = (int)max64(0, min64(2, nkb_t - kb0));
+                    if (cc >= C || nblk == 0) {                  // C is even: both rows are padding
+                        *s0 = 0;
+                        *s1p = 0;
+                    } else {
+                        uint32_t sw0 = 0, sw1 = 0, c0w[4], c1w[4];
+#pragma unroll
+                        for (int b = 0; b < 2; ++b) {
+                            c0w[2 * b] = c0w[2 * b + 1] = c1w[2 * b] = c1w[2 * b + 1] = 0u;
+                            if (b < nblk) {
+                                uint32_t w[16];
+#pragma unroll
+                                for (int u = 0; u < 16; ++u) {
+                                    const int r = ch * 32 + b * 16 + u;
+                                    w[u] = *reinterpret_cast<const uint32_t*>(tile + dq_chunk(pb, r, pchunk) + pword * 4);
+                                }
+                                const int64_t kc = (kb0 + b) * 16;
+                                float v[16];
+                                uint32_t sb;
+#pragma unroll
+                                for (int u = 0; u < 16; ++u) v[u] = bf16_lo(w[u]);
+                                encode_block16<RHT2, SR2 != 0, SR2 == 2, G32>(v, s2, rtab2, (uint64_t)(cc * R + kc), a2,
+                                                                              &sb, &c0w[2 * b], &c0w[2 * b + 1]);
+                                sw0 |= sb << (8 * b);
+#pragma unroll
+                                for (int u = 0; u < 16; ++u) v[u] = bf16_hi(w[u]);
+                                encode_block16<RHT2, SR2 != 0, SR2 == 2, G32>(v, s2, rtab2, (uint64_t)((cc + 1) * R + kc),
+                                                                              a2, &sb, &c1w[2 * b], &c1w[2 * b + 1]);
+                                sw1 |= sb << (8 * b);
+                            }
+                        }
+#pragma unroll
+                        for (int q = 0; q < 2; ++q) {
+                            const uint32_t* cw = q ? c1w : c0w;
+                            uint8_t* cdst = a2.codes + (cc + q) * (R >> 1) + kb0 * 8;
+                            if (nblk == 2 && (R & 31) == 0) {
+                                *reinterpret_cast<uint4*>(cdst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
+                            } else {
+#pragma unroll
+                                for (int b = 0; b < 2; ++b)
+                                    if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
+                            }
+                        }
+                        *s0 = (uint16_t)sw0;
+                        *s1p = (uint16_t)sw1;
+                    }
+                }
+            }
+            __syncwarp();                                        // this warp is done with slot s
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
         }
-        __syncthreads();                                         // slot s fully read
-        if (threadIdx.x == 0) {
-            const int64_t tn = t + (int64_t)kDqStages * gridDim.x;
-            if (tn < ntiles) issue(tn, s);
-        }
-    }
-    // drain: no copy may still be writing into this CTA's shared memory
-    if (threadIdx.x == 0 && abort_flag) {
-        for (int k = 0; k < kDqStages; ++k) {
-            const int ii = i + k;
-            const int64_t t = (int64_t)blockIdx.x + (int64_t)ii * gridDim.x;
-            if (t < ntiles) mbar_wait_bounded(&full[ii % kDqStages], (uint32_t)(ii / kDqStages) & 1u, nullptr);
-        }
-    }
+    };
+    if (a1.sr_g32 && a2.sr_g32) encode_tiles(std::true_type{});
+    else encode_tiles(std::false_type{});
 }
 
 }  // namespace nvfp4

@@ -102,6 +102,9 @@ EncodeTiledFn encode_fn() {
 // Test-only fault injection (nvfp4_debug_inject): 1 = the next streamed amax
 // launch skips the copy of its first tile.
 std::atomic<int> g_fault_injection{0};
+// Test-only (nvfp4_debug_inject mode 2): the next dual quantise takes its
+// general 64-bit Philox block-index path even though the indices fit 32 bits.
+std::atomic<int> g_force_g64{0};
 
 // 2D map of a stored bf16 array [rows x cols] (leading dimension ld) with a
 // box of box_rows x box_cols elements.
@@ -189,7 +192,7 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
 // runs philox4x32_10_not (complemented words, so that each half-word is
 // 65535 - u16), whose round-9 pair is complemented; NVFP4_SR_HW runs the plain
 // philox4x32_10.
-void set_sr_keys(QuantArgs* a, uint64_t seed, nvfp4_round round) {
+void set_sr_keys(QuantArgs* a, uint64_t seed, uint64_t stream_id, nvfp4_round round, int64_t n_elems) {
     uint32_t k0 = (uint32_t)seed, k1 = (uint32_t)(seed >> 32);
     const bool hw = round == NVFP4_SR_HW;
     for (int r = 0; r < 10; ++r) {
@@ -199,6 +202,21 @@ void set_sr_keys(QuantArgs* a, uint64_t seed, nvfp4_round round) {
         k1 += 0xBB67AE85u;
     }
     a->sr_hw = hw ? 1 : 0;
+    a->stream_id = stream_id;
+    // rounds 0 and 1 of Philox on the counter (g, 0, stream_lo, stream_hi):
+    // everything but g is fixed per call (see philox4x32_10_g32)
+    const uint32_t s_lo = (uint32_t)stream_id, s_hi = (uint32_t)(stream_id >> 32);
+    const uint32_t k00 = (uint32_t)seed, k10 = (uint32_t)(seed >> 32);
+    const uint32_t k01 = k00 + 0x9E3779B9u, k11 = k10 + 0xBB67AE85u;
+    const uint64_t t = (uint64_t)s_lo * 0xCD9E8D57u;
+    const uint32_t a0 = (uint32_t)(t >> 32) ^ k00, a1 = (uint32_t)t;
+    const uint64_t p = (uint64_t)a0 * 0xD2511F53u;
+    a->sr_pre[0] = s_hi ^ k10;
+    a->sr_pre[1] = a1 ^ k01;
+    a->sr_pre[2] = (uint32_t)(p >> 32) ^ k11;
+    a->sr_pre[3] = (uint32_t)p;
+    // the block index g = idx / 8 (idx / 16 for NVFP4_SR_HW) stays below 2^32
+    a->sr_g32 = n_elems <= (int64_t(1) << 35) ? 1 : 0;
 }
 
 bool valid_round(nvfp4_round r) { return r == NVFP4_RNE || r == NVFP4_SR || r == NVFP4_SR_HW; }
@@ -291,8 +309,7 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.gs_out = out->global_scale;
     a.gs_out2 = out_t ? out_t->global_scale : nullptr;
     a.rht = rht_signs(mask);
-    set_sr_keys(&a, seed, round);
-    a.stream_id = stream_id;
+    set_sr_keys(&a, seed, stream_id, round, x.rows * x.cols);
     const bool sr = round != NVFP4_RNE;
 
     if (!block2d) {
@@ -348,7 +365,7 @@ nvfp4_status launch_dual_t(const CUtensorMap& map, const DualArgs& d, int grid, 
             return NVFP4_ERR_CUDA;
         ready[dev].store(1);
     }
-    k_quant_dual<SR1, SR2, RHT2><<<grid, kQuantThreads, kDqSmem, st>>>(map, d);
+    k_quant_dual<SR1, SR2, RHT2><<<grid, kDqThreads, kDqSmem, st>>>(map, d);
     return launch_status();
 }
 
@@ -630,7 +647,7 @@ nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4
     a1.scales = out->scales;
     a1.stream_id = stream_id;
     a1.write_primary = 1;
-    set_sr_keys(&a1, seed, round);
+    set_sr_keys(&a1, seed, stream_id, round, x.rows * x.cols);
     QuantArgs& a2 = d.col;
     a2.x = a1.x;
     a2.ld = x.ld;
@@ -643,7 +660,8 @@ nvfp4_status nvfp4_quantize_dual(nvfp4_bf16_view x, const float* amax_dev, nvfp4
     a2.rht = rht_signs(rht_mask_t);
     a2.stream_id = stream_id_t;
     a2.write_primary = 1;
-    set_sr_keys(&a2, seed_t, round_t);
+    set_sr_keys(&a2, seed_t, stream_id_t, round_t, x.rows * x.cols);
+    if (g_force_g64.exchange(0) == 1) a1.sr_g32 = a2.sr_g32 = 0;    // test-only, one call
     return launch_dual(d, (int)round, (int)round_t, rht_mask_t != 0, stream);
 }
 
@@ -854,8 +872,13 @@ nvfp4_status nvfp4_debug_check_div6(uint32_t lo_bits, uint32_t hi_bits, unsigned
 }
 
 nvfp4_status nvfp4_debug_inject(int mode) {
-    if (mode != 0 && mode != 1) return NVFP4_ERR_INVALID_ARG;
+    if (mode < 0 || mode > 2) return NVFP4_ERR_INVALID_ARG;
+    if (mode == 2) {
+        g_force_g64.store(1);
+        return NVFP4_OK;
+    }
     g_fault_injection.store(mode);
+    if (mode == 0) g_force_g64.store(0);
     return NVFP4_OK;
 }
 

@@ -296,6 +296,8 @@ struct QuantArgs {
     uint32_t sr_key[20];        // Philox round keys of the seed (philox4x32_10_not for
                                 // NVFP4_SR, philox4x32_10 for NVFP4_SR_HW)
     int sr_hw;                  // 1: NVFP4_SR_HW random-bit layout (hardware conversion)
+    int sr_g32;                 // 1: every Philox block index of the operand is below 2^32
+    uint32_t sr_pre[4];         // rounds 0-1 constants of philox4x32_10_g32 (seed, stream_id)
     // 2D transposed emit (optional)
     uint8_t* codes_t;           // [k x rows/2]
     uint8_t* scales_t;
@@ -328,8 +330,10 @@ __device__ __forceinline__ void init_rtab(float* rtab, float s_enc) {
 // Encode one 16-element block.  amax_bits: the block's max |value| as float
 // bits when already known (raw bf16 input), or ~0u to compute it here.
 // HW: the stochastic rounding's random-bit layout, 1 = NVFP4_SR_HW, 0 =
-// NVFP4_SR, -1 = taken from a.sr_hw at run time.
-template <bool RHT, bool SR, int HW = -1>
+// NVFP4_SR, -1 = taken from a.sr_hw at run time.  G32: the caller knows that
+// a.sr_g32 holds (Philox block indices below 2^32), so the counter's constant
+// words come folded (philox4x32_10_g32).
+template <bool RHT, bool SR, int HW = -1, bool G32 = false>
 __device__ __forceinline__ void encode_block16(float* v, float s_enc, const float* rtab, uint64_t idx0,
                                                const QuantArgs& a, uint32_t* sb_out,
                                                uint32_t* code_lo, uint32_t* code_hi,
@@ -350,7 +354,13 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
     scale16(v, r_b);
     if (SR) {
         if (HW == 1 || (HW < 0 && a.sr_hw)) {
-            e2m1x16_sr(v, sr_words16(idx0 >> 4, a.stream_id, a.sr_key), code_lo, code_hi);
+            const uint4 w = G32 ? philox4x32_10_g32<false>((uint32_t)(idx0 >> 4), a.sr_key, a.sr_pre)
+                                : sr_words16(idx0 >> 4, a.stream_id, a.sr_key);
+            e2m1x16_sr(v, w, code_lo, code_hi);
+        } else if (G32) {
+            const uint32_t g = (uint32_t)(idx0 >> 3);
+            *code_lo = e2m1x8_sr_cvt(v, philox4x32_10_g32<true>(g, a.sr_key, a.sr_pre));
+            *code_hi = e2m1x8_sr_cvt(v + 8, philox4x32_10_g32<true>(g + 1, a.sr_key, a.sr_pre));
         } else {
             *code_lo = e2m1x8_sr_cvt(v, sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
             *code_hi = e2m1x8_sr_cvt(v + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));

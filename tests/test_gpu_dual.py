@@ -159,3 +159,49 @@ def test_quantize_dual_many_tiles_per_cta(nv):
     assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "dual rows, many tiles")
     ref_t = oracle.quantize(s, transposed=True, rht_mask=MASK, sr=True, seed=17, stream_id=2)
     assert_q_equal(qt, ref_t.codes, ref_t.scales, ref_t.s_enc, "dual cols, many tiles")
+
+
+@pytest.mark.parametrize("hw", [False, True])
+def test_quantize_dual_wide_seed_and_stream(nv, hw):
+    """Seeds and Philox stream ids with both 32-bit words set: the kernels fold
+    the counter's stream words and the first keys into constants made on the
+    host, so every word of the key and of the counter must reach the draws."""
+    rows, cols = 256, 528
+    s = _data(rows, cols, 41, "t")
+    d = dev_bf16(s)
+    seed, sid, seed_t, sid_t = 0xDEADBEEF12345678, 0x123456789ABCDEF0, 0x0F1E2D3C4B5A6978, 0xFEDCBA9876543210
+    a, at = nv.nvfp4_amax_dual(d, MASK)
+    q, qt = nv.QTensor(rows, cols), nv.QTensor(cols, rows)
+    rnd = nv.NVFP4_SR_HW if hw else nv.NVFP4_SR
+    nv.nvfp4_quantize_dual(d, a, rnd, seed, sid, q, MASK, at, rnd, seed_t, sid_t, qt)
+    torch.cuda.synchronize()
+    assert nv.nvfp4_get_status() == nv.NVFP4_OK
+    ref = oracle.quantize(s, sr=True, seed=seed, stream_id=sid, sr_hw=hw)
+    assert_q_equal(q, ref.codes, ref.scales, ref.s_enc, "wide seed rows")
+    ref_t = oracle.quantize(s, transposed=True, rht_mask=MASK, sr=True, seed=seed_t, stream_id=sid_t, sr_hw=hw)
+    assert_q_equal(qt, ref_t.codes, ref_t.scales, ref_t.s_enc, "wide seed cols")
+
+
+@pytest.mark.parametrize("rnd_name", ["NVFP4_SR", "NVFP4_SR_HW", "NVFP4_RNE"])
+def test_quantize_dual_general_index_path(nv, rnd_name):
+    """The path for Philox block indices of 64 bits (taken only for operands of
+    more than 2^35 elements) writes the same bytes as the 32-bit-index path;
+    the test-only injection mode 2 makes one call take it on a small tensor."""
+    rows, cols = 384, 1280
+    s = _data(rows, cols, 43, "t")
+    d = dev_bf16(s)
+    rnd = getattr(nv, rnd_name)
+    a, at = nv.nvfp4_amax_dual(d, MASK)
+    outs = []
+    for force in (False, True):
+        q, qt = nv.QTensor(rows, cols), nv.QTensor(cols, rows)
+        if force:
+            nv.nvfp4_debug_inject(2)
+        nv.nvfp4_quantize_dual(d, a, rnd, 7, 3, q, MASK, at, rnd, 8, 4, qt)
+        torch.cuda.synchronize()
+        assert nv.nvfp4_get_status() == nv.NVFP4_OK
+        outs.append((q, qt))
+    for x, y in zip(outs[0], outs[1]):
+        assert torch.equal(x.codes, y.codes) and torch.equal(x.scales, y.scales)
+    ref = oracle.quantize(s, sr=rnd != nv.NVFP4_RNE, seed=7, stream_id=3, sr_hw=rnd == nv.NVFP4_SR_HW)
+    assert_q_equal(outs[1][0], ref.codes, ref.scales, ref.s_enc, "general path rows")

@@ -46,5 +46,5 @@ def test_dropped_copy_reports_timeout_and_context_survives(nv):
 
 def test_debug_inject_rejects_unknown_modes(nv):
     with pytest.raises(nv.Nvfp4Error):
-        nv.nvfp4_debug_inject(2)
+        nv.nvfp4_debug_inject(3)
     nv.nvfp4_debug_inject(0)
