@@ -105,6 +105,13 @@ __host__ __device__ constexpr uint32_t make_idesc() {
 struct Alpha {
     float m, p;
     __device__ __forceinline__ float apply(float acc) const { return __fmul_rn(__fmul_rn(acc, m), p); }
+    // two accumulators at once on packed two-lane FP32 (per lane the same
+    // IEEE products as apply); the second product only when p != 1
+    __device__ __forceinline__ float2 apply2(float a0, float a1) const {
+        float2 r = __fmul2_rn(make_float2(a0, a1), make_float2(m, m));
+        if (p != 1.0f) r = __fmul2_rn(r, make_float2(p, p));
+        return r;
+    }
 };
 
 __device__ __forceinline__ Alpha make_alpha(float s_a, float s_b) {
@@ -161,8 +168,8 @@ __device__ __forceinline__ void stage_bf16_chunk(uint32_t stg, int c, int lane, 
     uint32_t p[16];
 #pragma unroll
     for (int j = 0; j < 16; ++j) {
-        __nv_bfloat162 h = __floats2bfloat162_rn(alpha.apply(__uint_as_float(acc[2 * j])),
-                                                 alpha.apply(__uint_as_float(acc[2 * j + 1])));
+        const float2 r = alpha.apply2(__uint_as_float(acc[2 * j]), __uint_as_float(acc[2 * j + 1]));
+        __nv_bfloat162 h = __floats2bfloat162_rn(r.x, r.y);
         p[j] = *reinterpret_cast<uint32_t*>(&h);
     }
     const uint32_t blk = stg + (uint32_t)(c >> 1) * (32 * 128) + (uint32_t)lane * 128;

@@ -352,9 +352,9 @@ k_gemm_nvfp4_2sm(const __grid_constant__ CUtensorMap tma_a, const __grid_constan
                     if (c + 1 < BN / 32) tmem_ld_32x32b_x16(t_row + (c + 1) * 16, acc[(c + 1) & 1]);
 #pragma unroll
                     for (int j = 0; j < 8; ++j) {
-                        __nv_bfloat162 hv = __floats2bfloat162_rn(
-                            alpha.apply(__uint_as_float(acc[c & 1][2 * j])),
-                            alpha.apply(__uint_as_float(acc[c & 1][2 * j + 1])));
+                        const float2 r = alpha.apply2(__uint_as_float(acc[c & 1][2 * j]),
+                                                      __uint_as_float(acc[c & 1][2 * j + 1]));
+                        __nv_bfloat162 hv = __floats2bfloat162_rn(r.x, r.y);
                         packed[(c & 3) * 8 + j] = *reinterpret_cast<uint32_t*>(&hv);
                     }
                     if (c == 3 || c == BN / 32 - 1) {
