@@ -88,7 +88,11 @@ __device__ __forceinline__ uint32_t dq_chunk(int b, int r, int c) {
 }
 
 // SR1, SR2: rounding of each operand, 0 = RNE, 1 = NVFP4_SR, 2 = NVFP4_SR_HW.
-template <int SR1, int SR2, bool RHT2>
+// PATHS: bit 0 = the row-wise operand, bit 1 = the column-wise operand; a
+// single path makes the kernel the TMA-fed 1x16 quantiser of one view (rows:
+// a non-transposed view, with RHT1 for the transform along its k; columns: a
+// transposed view, whose stored array is S).
+template <int SR1, int SR2, bool RHT2, int PATHS = 3, bool RHT1 = false>
 __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_constant__ CUtensorMap map,
                                                               const __grid_constant__ DualArgs d) {
     extern __shared__ uint8_t dq_raw[];
@@ -100,8 +104,9 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
     const QuantArgs& a1 = d.row;
     const QuantArgs& a2 = d.col;
     float s1, s2;
-    const bool ok1 = resolve_scale(a1.scale_src, 0, a1.gs_out, nullptr, &s1);
-    const bool ok2 = resolve_scale(a2.scale_src, 0, a2.gs_out, nullptr, &s2);
+    constexpr bool ROWS = (PATHS & 1) != 0, COLS = (PATHS & 2) != 0;
+    const bool ok1 = ROWS && resolve_scale(a1.scale_src, a1.src_is_senc, a1.gs_out, a1.gs_out2, &s1);
+    const bool ok2 = COLS && resolve_scale(a2.scale_src, a2.src_is_senc, a2.gs_out, a2.gs_out2, &s2);
     if (!ok1 && !ok2) return;                                    // uniform over the grid
     for (int c = threadIdx.x; c < 128; c += blockDim.x) {
         rtab1[c] = ok1 ? encode_factor(s1, (uint32_t)c) : 0.0f;
@@ -180,7 +185,7 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
             const int64_t r0 = tr * kDqRows, c0 = tc * kDqCols;
 
             // ---- row-wise operand
-            if (ok1) {
+            if (ROWS && ok1) {
                 const int64_t row = r0 + rr;
                 const int64_t G = c0 / 64 + rg;
                 if (G < ngroups) {
@@ -200,9 +205,9 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                                 unpack8(lo, v);
                                 unpack8(hi, v + 8);
                                 uint32_t sb;
-                                encode_block16<false, SR1 != 0, SR1 == 2, G32>(
+                                encode_block16<RHT1, SR1 != 0, SR1 == 2, G32>(
                                     v, s1, rtab1, (uint64_t)(row * C + G * 64 + b * 16), a1, &sb, &cw[2 * b],
-                                    &cw[2 * b + 1], absmax_bits16_packed(lo, hi));
+                                    &cw[2 * b + 1], RHT1 ? ~0u : absmax_bits16_packed(lo, hi));
                                 sw |= sb << (8 * b);
                             }
                         }
@@ -221,7 +226,7 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
             }
 
             // ---- column-wise operand: logical rows cc, cc + 1 of S^T, blocks kb0, kb0 + 1
-            if (ok2) {
+            if (COLS && ok2) {
                 const int64_t cc = c0 + 2 * pc;
                 const int64_t G = r0 / 64;
                 const int64_t kb0 = G * 4 + 2 * ch;
@@ -280,7 +285,7 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
             if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
         }
     };
-    if (a1.sr_g32 && a2.sr_g32) encode_tiles(std::true_type{});
+    if ((!ROWS || a1.sr_g32) && (!COLS || a2.sr_g32)) encode_tiles(std::true_type{});
     else encode_tiles(std::false_type{});
 }
 

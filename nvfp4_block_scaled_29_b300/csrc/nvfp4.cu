@@ -263,6 +263,9 @@ nvfp4_status launch_q2d(const QuantArgs& a, bool emit_t, cudaStream_t st) {
     return launch_q2d_t<RHT, SR, false>(map, a, grid, st);
 }
 
+template <int PATHS, bool RHT>
+nvfp4_status launch_dual_single_sr(const DualArgs& d, int sr, cudaStream_t st);
+
 nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float* amax_dev,
                            nvfp4_round round, uint64_t seed, uint64_t stream_id, nvfp4_q* out,
                            nvfp4_q* out_t, bool block2d, cudaStream_t st) {
@@ -318,6 +321,23 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
         a.codes = out->codes;
         a.scales = out->scales;
         a.write_primary = 1;
+        // TMA-fed persistent path (one path of the dual kernel): a stored
+        // array read in swizzled tiles; a transposed view needs an even
+        // number of logical rows (its items are row pairs)
+        if (!x.transposed || (x.rows % 2) == 0) {
+            DualArgs d{};
+            const int r = (int)round;
+            if (!x.transposed) {
+                d.row = a;
+                return mask ? launch_dual_single_sr<1, true>(d, r, st) : launch_dual_single_sr<1, false>(d, r, st);
+            }
+            d.col = a;                              // the logical operand [x.rows x x.cols]
+            d.row.x = a.x;                          // the stored array S = [x.cols x x.rows]
+            d.row.rows = x.cols;
+            d.row.k = x.rows;
+            d.row.ld = x.ld;
+            return mask ? launch_dual_single_sr<2, true>(d, r, st) : launch_dual_single_sr<2, false>(d, r, st);
+        }
         if (mask) {
             if (sr) launch_q1d<true, true>(a, x.transposed, st);
             else launch_q1d<true, false>(a, x.transposed, st);
@@ -384,15 +404,52 @@ nvfp4_status launch_dual_sr2(const CUtensorMap& map, const DualArgs& d, int sr2,
     }
 }
 
+// The TMA map and grid of the dual kernel: tiles of the stored array S, whose
+// dimensions d.row carries (rows = S's rows, k = S's columns) for every path.
+bool dual_map_grid(const DualArgs& d, CUtensorMap* map, int* grid) {
+    if (!make_bf16_map(map, d.row.x, d.row.rows, d.row.k, d.row.ld, kDqBoxCols, kDqRows, CU_TENSOR_MAP_SWIZZLE_128B))
+        return false;
+    const int64_t rows_pad = cdiv(d.row.rows, 128) * 128;
+    const int64_t tiles = (rows_pad / kDqRows) * cdiv(d.row.k, kDqCols);
+    *grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
+    return true;
+}
+
+// One path of the dual kernel as a 1x16 quantiser (PATHS 1: the row-wise
+// operand, rounding SR and RHT along its k; PATHS 2: the column-wise one).
+template <int PATHS, int SR, bool RHT>
+nvfp4_status launch_dual_single(const DualArgs& d, cudaStream_t st) {
+    constexpr int SR1 = PATHS == 1 ? SR : 0, SR2 = PATHS == 2 ? SR : 0;
+    auto kern = k_quant_dual<SR1, SR2, PATHS == 2 && RHT, PATHS, PATHS == 1 && RHT>;
+    static std::atomic<int> ready[kMaxDevices];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
+    if (!ready[dev].load()) {
+        if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kDqSmem) != cudaSuccess)
+            return NVFP4_ERR_CUDA;
+        ready[dev].store(1);
+    }
+    CUtensorMap map;
+    int grid = 0;
+    if (!dual_map_grid(d, &map, &grid)) return NVFP4_ERR_CUDA;
+    kern<<<grid, kDqThreads, kDqSmem, st>>>(map, d);
+    return launch_status();
+}
+
+template <int PATHS, bool RHT>
+nvfp4_status launch_dual_single_sr(const DualArgs& d, int sr, cudaStream_t st) {
+    switch (sr) {
+        case 0: return launch_dual_single<PATHS, 0, RHT>(d, st);
+        case 1: return launch_dual_single<PATHS, 1, RHT>(d, st);
+        default: return launch_dual_single<PATHS, 2, RHT>(d, st);
+    }
+}
+
 // sr1, sr2: 0 = RNE, 1 = NVFP4_SR, 2 = NVFP4_SR_HW
 nvfp4_status launch_dual(const DualArgs& d, int sr1, int sr2, bool rht2, cudaStream_t st) {
     CUtensorMap map;
-    if (!make_bf16_map(&map, d.row.x, d.row.rows, d.row.k, d.row.ld, kDqBoxCols, kDqRows,
-                       CU_TENSOR_MAP_SWIZZLE_128B))
-        return NVFP4_ERR_CUDA;
-    const int64_t rows_pad = cdiv(d.row.rows, 128) * 128;
-    const int64_t tiles = (rows_pad / kDqRows) * cdiv(d.row.k, kDqCols);
-    const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
+    int grid = 0;
+    if (!dual_map_grid(d, &map, &grid)) return NVFP4_ERR_CUDA;
     switch (sr1) {
         case 0: return launch_dual_sr2<0>(map, d, sr2, rht2, grid, st);
         case 1: return launch_dual_sr2<1>(map, d, sr2, rht2, grid, st);
