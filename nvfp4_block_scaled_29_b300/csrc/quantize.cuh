@@ -569,8 +569,14 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
     __shared__ __align__(16) uint32_t tile_codes[64 * 16];
     __shared__ uint8_t tile_sb[4][8];          // [row block][k block]
     __shared__ int abort_flag;
+    // encode factors r_b from a per-CTA table of the 128 E4M3 codes where the
+    // kernel is bound by instructions (stochastic rounding, RHT, transposed
+    // emit); the plain RNE kernel, bound by HBM, divides per block
+    constexpr bool kTable = SR || RHT || EMIT_T;
+    __shared__ float rtab[kTable ? 128 : 1];
     float s_enc;
     if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
+    if constexpr (kTable) init_rtab(rtab, s_enc);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int64_t nkb = a.k >> 4;
     const int64_t ngroups = (nkb + 3) >> 2;
@@ -647,7 +653,7 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
     #pragma unroll
         for (int b = 0; b < 4; ++b) {
             const uint32_t sb = (b < nblk) ? block_scale_code(__uint_as_float(lmax[b]), s_enc) : 0u;
-            const float r_b = (b < nblk) ? encode_factor(s_enc, sb) : 0.0f;
+            const float r_b = (b < nblk) ? (kTable ? rtab[sb] : encode_factor(s_enc, sb)) : 0.0f;
             sw |= sb << (8 * b);
             scale16(v[b], r_b);
             if (SR) {
