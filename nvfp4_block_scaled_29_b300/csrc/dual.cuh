@@ -27,9 +27,9 @@
 namespace nvfp4 {
 
 // Block-wide maxima of two non-negative float bit patterns, merged into two
-// outputs with one atomic each per CTA.
+// outputs with one atomic each per CTA (at most 32 warps per CTA).
 __device__ __forceinline__ void block_max2_to_global(uint32_t m0, float* out0, uint32_t m1, float* out1) {
-    __shared__ uint32_t red[2][kQuantThreads / 32];
+    __shared__ uint32_t red[2][32];
     m0 = __reduce_max_sync(0xFFFFFFFFu, m0);
     m1 = __reduce_max_sync(0xFFFFFFFFu, m1);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -297,91 +297,103 @@ namespace nvfp4 {
 // max |S| and (RHT_COLS) max |RHT16 down the columns of S| for a stored bf16
 // array S [srows x scols], streamed through shared memory: persistent CTAs
 // walk 64-row x 256-column tiles (32 KB, loaded by one 2D TMA copy; zeros
-// beyond the array) through a ring of kAmaxStages slots, so that up to
-// kAmaxStages - 1 tiles per CTA are in flight while one is reduced.
-// A tile is 128 column pairs x 4 blocks of 16 rows; each thread reduces two
-// (pair, block) items with conflict-free 4-byte reads (a warp reads 128
-// contiguous bytes of a tile row).
+// beyond the array) through a ring of kAmaxStages slots.  Warp 8 (one lane)
+// feeds the ring and refills a slot as soon as the 8 reducing warps have
+// arrived on its empty barrier; the reducing warps never wait for one
+// another.  A tile is 128 column pairs x 4 blocks of 16 rows; each thread
+// reduces two (pair, block) items with conflict-free 4-byte reads (a warp
+// reads 128 contiguous bytes of a tile row).
 constexpr int kAmaxTileRows = 64, kAmaxTileCols = 256;
 constexpr int kAmaxTileBytes = kAmaxTileRows * kAmaxTileCols * 2;
 constexpr int kAmaxStages = 3;
-constexpr int kAmaxSmem = kAmaxStages * kAmaxTileBytes + 64;
+constexpr int kAmaxConsumerWarps = 8;
+constexpr int kAmaxThreads = (kAmaxConsumerWarps + 1) * 32;
+constexpr int kAmaxSmem = kAmaxStages * kAmaxTileBytes + 128;
 
 // fi_skip_tile >= 0 (test-only fault injection): that tile's copy is never
 // issued, so its consumers' bounded wait expires and the kernel reports
 // NVFP4_DEV_TIMEOUT instead of hanging.
 template <bool RHT_COLS>
-__global__ void __launch_bounds__(kQuantThreads, 2) k_amax_stream(const __grid_constant__ CUtensorMap map,
-                                                                  int64_t srows, int64_t scols, const RhtSigns sg,
-                                                                  float* out_plain, float* out_t,
-                                                                  int64_t fi_skip_tile) {
+__global__ void __launch_bounds__(kAmaxThreads, 2) k_amax_stream(const __grid_constant__ CUtensorMap map,
+                                                                 int64_t srows, int64_t scols, const RhtSigns sg,
+                                                                 float* out_plain, float* out_t,
+                                                                 int64_t fi_skip_tile) {
     extern __shared__ __align__(128) uint8_t amax_smem[];
     uint64_t* full = reinterpret_cast<uint64_t*>(amax_smem + kAmaxStages * kAmaxTileBytes);
+    uint64_t* empty = full + kAmaxStages;
     __shared__ int abort_flag;
     const int64_t row_tiles = (srows + kAmaxTileRows - 1) / kAmaxTileRows;
     const int64_t col_tiles = (scols + kAmaxTileCols - 1) / kAmaxTileCols;
     const int64_t ntiles = row_tiles * col_tiles;
+    const int warp = threadIdx.x >> 5;
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kAmaxStages; ++s) mbar_init(&full[s], 1);
+        for (int s = 0; s < kAmaxStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kAmaxConsumerWarps);
+        }
         abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&map);
     }
     __syncthreads();
-    auto issue = [&](int64_t t, int s) {
-        if (t == fi_skip_tile) return;
-        const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
-        mbar_arrive_expect_tx(&full[s], kAmaxTileBytes);
-        tma_load_2d(amax_smem + s * kAmaxTileBytes, &map, &full[s], (int32_t)(tc * kAmaxTileCols),
-                    (int32_t)(tr * kAmaxTileRows));
-    };
-    if (threadIdx.x == 0)
-        for (int s = 0; s < kAmaxStages; ++s) {
-            const int64_t t = (int64_t)blockIdx.x + (int64_t)s * gridDim.x;
-            if (t < ntiles) issue(t, s);
-        }
     constexpr uint32_t M = 0x7FFF7FFFu;
     uint32_t m2 = 0, m = 0;
-    const int pr = threadIdx.x & 127;                 // column pair of the tile
-    const int kb0 = threadIdx.x >> 7;                 // blocks kb0 and kb0 + 2
-    int i = 0;
-    for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
-        const int s = i % kAmaxStages;
-        const uint32_t ph = (uint32_t)(i / kAmaxStages) & 1u;
-        const bool ok = mbar_wait_bounded(&full[s], ph, &abort_flag);
-        __syncthreads();                              // every thread saw the same outcome
-        if (abort_flag || !ok) break;
-        const uint32_t* words = reinterpret_cast<const uint32_t*>(amax_smem + s * kAmaxTileBytes);
-#pragma unroll
-        for (int j = 0; j < 2; ++j) {
-            const int kb = kb0 + 2 * j;
-            uint32_t w[16];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) w[r] = words[(kb * 16 + r) * (kAmaxTileCols / 2) + pr];
-#pragma unroll
-            for (int r = 0; r < 16; ++r) m2 = __vmaxu2(m2, w[r] & M);
-            if (RHT_COLS) {
-                float v[16];
-#pragma unroll
-                for (int r = 0; r < 16; ++r) v[r] = bf16_lo(w[r]);
-                m = max(m, rht16_absmax_bits_nan(v, sg));
-#pragma unroll
-                for (int r = 0; r < 16; ++r) v[r] = bf16_hi(w[r]);
-                m = max(m, rht16_absmax_bits_nan(v, sg));
+    if (warp == kAmaxConsumerWarps) {
+        // ------------------------------------------------------ producer --
+        if ((threadIdx.x & 31) == 0) {
+            int i = 0;
+            bool issued[kAmaxStages] = {};
+            for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+                const int s = i % kAmaxStages;
+                if (i >= kAmaxStages &&
+                    !mbar_wait_bounded(&empty[s], (uint32_t)(i / kAmaxStages - 1) & 1u, &abort_flag))
+                    break;
+                if (abort_flag) break;
+                issued[s] = t != fi_skip_tile;
+                if (!issued[s]) continue;              // test-only: this tile is never copied
+                const int64_t tr = t / col_tiles, tc = t - tr * col_tiles;
+                mbar_arrive_expect_tx(&full[s], kAmaxTileBytes);
+                tma_load_2d(amax_smem + s * kAmaxTileBytes, &map, &full[s], (int32_t)(tc * kAmaxTileCols),
+                            (int32_t)(tr * kAmaxTileRows));
+            }
+            // every issued copy lands before the CTA exits: the last kAmaxStages
+            // issues (earlier ones were waited for by the reducing warps)
+            for (int k = 1; k <= kAmaxStages && i - k >= 0; ++k) {
+                const int ii = i - k;
+                if (issued[ii % kAmaxStages])
+                    mbar_wait_bounded(&full[ii % kAmaxStages], (uint32_t)(ii / kAmaxStages) & 1u, nullptr);
             }
         }
-        __syncthreads();                              // slot s fully read
-        if (threadIdx.x == 0) {
-            const int64_t tn = t + (int64_t)kAmaxStages * gridDim.x;
-            if (tn < ntiles) issue(tn, s);
-        }
-    }
-    // drain: no copy may still be writing into this CTA's shared memory
-    if (threadIdx.x == 0 && abort_flag) {
-        for (int k = 0; k < kAmaxStages; ++k) {
-            const int ii = i + k;
-            const int64_t t = (int64_t)blockIdx.x + (int64_t)ii * gridDim.x;
-            if (t < ntiles && ii < i + kAmaxStages) mbar_wait_bounded(&full[ii % kAmaxStages], (uint32_t)(ii / kAmaxStages) & 1u, nullptr);
+    } else {
+        const int pr = threadIdx.x & 127;             // column pair of the tile
+        const int kb0 = threadIdx.x >> 7;             // blocks kb0 and kb0 + 2
+        int i = 0;
+        for (int64_t t = blockIdx.x; t < ntiles; t += gridDim.x, ++i) {
+            const int s = i % kAmaxStages;
+            const uint32_t ph = (uint32_t)(i / kAmaxStages) & 1u;
+            // warp-uniform outcome: a lane that timed out stops its whole warp
+            if (!__all_sync(0xFFFFFFFFu, mbar_wait_bounded(&full[s], ph, &abort_flag))) break;
+            const uint32_t* words = reinterpret_cast<const uint32_t*>(amax_smem + s * kAmaxTileBytes);
+#pragma unroll
+            for (int j = 0; j < 2; ++j) {
+                const int kb = kb0 + 2 * j;
+                uint32_t w[16];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) w[r] = words[(kb * 16 + r) * (kAmaxTileCols / 2) + pr];
+#pragma unroll
+                for (int r = 0; r < 16; ++r) m2 = __vmaxu2(m2, w[r] & M);
+                if (RHT_COLS) {
+                    float v[16];
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) v[r] = bf16_lo(w[r]);
+                    m = max(m, rht16_absmax_bits_nan(v, sg));
+#pragma unroll
+                    for (int r = 0; r < 16; ++r) v[r] = bf16_hi(w[r]);
+                    m = max(m, rht16_absmax_bits_nan(v, sg));
+                }
+            }
+            __syncwarp();                             // this warp is done with slot s
+            if ((threadIdx.x & 31) == 0) mbar_arrive(&empty[s]);
         }
     }
     const uint32_t plain = max(m2 & 0xFFFFu, m2 >> 16) << 16;

@@ -157,8 +157,8 @@ nvfp4_status launch_amax_stream(const void* ptr, int64_t srows, int64_t scols, i
     const int g = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * 2));
     const RhtSigns sg = rht_signs(mask);
     const int64_t skip = g_fault_injection.exchange(0) == 1 ? 0 : -1;   // test-only, one launch
-    if (mask) k_amax_stream<true><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t, skip);
-    else k_amax_stream<false><<<g, kQuantThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t, skip);
+    if (mask) k_amax_stream<true><<<g, kAmaxThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t, skip);
+    else k_amax_stream<false><<<g, kAmaxThreads, kAmaxSmem, st>>>(map, srows, scols, sg, out_plain, out_t, skip);
     return launch_status();
 }
 
