@@ -93,8 +93,10 @@ typedef enum {
     NVFP4_ERR_NONFINITE = 4,        /* amax was NaN or Inf (device-side, via get_status) */
     NVFP4_ERR_TIMEOUT = 5,          /* a bounded device wait expired (device-side)       */
     NVFP4_ERR_CUDA = 6,             /* a CUDA runtime call failed                        */
-    NVFP4_ERR_LAUNCH = 7            /* a kernel got less dynamic shared memory than it   */
+    NVFP4_ERR_LAUNCH = 7,           /* a kernel got less dynamic shared memory than it   */
                                     /* needs and returned early (device-side)            */
+    NVFP4_ERR_GUARD = 8             /* debug build only: an index guard refused a global */
+                                    /* access outside its buffer (device-side)           */
 } nvfp4_status;
 
 typedef enum { NVFP4_RNE = 0, NVFP4_SR = 1, NVFP4_SR_HW = 2 } nvfp4_round;
@@ -238,7 +240,7 @@ nvfp4_status nvfp4_mx_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is
 uint32_t nvfp4_rht_mask_from_seed(uint64_t seed);
 
 /* Synchronises `stream`, returns the device-side status recorded since the
- * last call (NVFP4_ERR_LAUNCH before NVFP4_ERR_TIMEOUT before
+ * last call (NVFP4_ERR_GUARD before NVFP4_ERR_LAUNCH before NVFP4_ERR_TIMEOUT before
  * NVFP4_ERR_NONFINITE before NVFP4_OK, NVFP4_ERR_CUDA if the stream reports
  * a CUDA error) and clears it.                                              */
 nvfp4_status nvfp4_get_status(cudaStream_t stream);
@@ -274,6 +276,36 @@ nvfp4_status nvfp4_debug_inject(int mode);
 nvfp4_status nvfp4_debug_check_div6(uint32_t lo_bits, uint32_t hi_bits,
                                     unsigned long long* mismatches_dev, uint32_t* first_bad_dev,
                                     cudaStream_t stream);
+
+/* Index guards (debug build).  The library built with NVFP4_DEBUG_GUARDS
+ * defined (libnvfp4_guarded.so; same entry points, same results) checks
+ * every plain global load and store of its kernels against the extent that
+ * the layouts above give the buffer it addresses: codes rows * k/2 bytes,
+ * scales nvfp4_scale_bytes (nvfp4_mx_scale_bytes for MXFP4), a bf16 or fp32
+ * array ((outer - 1) * ld + inner) elements.  TMA copies are bounded by
+ * their tensor maps and need no guard.  An access outside its extent is
+ * skipped (a refused load reads zeros), nvfp4_get_status reports
+ * NVFP4_ERR_GUARD, and the first refused access is recorded.  No access is
+ * made outside the buffers in either build; the guards turn an indexing
+ * error into a status instead of a memory fault.
+ *
+ * nvfp4_debug_guards_enabled: 1 in the guarded build, 0 otherwise.
+ *
+ * nvfp4_debug_guard_record: synchronises `stream`, writes the site of the
+ * first refused access since the last call (0: none; 1..20 name the kernel
+ * and buffer, listed in csrc/guard.cuh) and the low 48 bits of its byte
+ * offset from the buffer's start to the host pointers, and clears the
+ * record.  In the normal build it writes 0 and 0.  NVFP4_ERR_INVALID_ARG for
+ * a null pointer.
+ *
+ * nvfp4_debug_guard_shrink (test-only): every guard checks against its extent
+ * minus `bytes` (0 restores the extents), so that a test can make the guards
+ * refuse in-bounds accesses near the end of a buffer and see them reported
+ * and skipped, without any access leaving the buffer.  Synchronous.
+ * NVFP4_ERR_INVALID_ARG in the normal build.                                */
+int nvfp4_debug_guards_enabled(void);
+nvfp4_status nvfp4_debug_guard_record(uint32_t* site, uint64_t* byte_offset, cudaStream_t stream);
+nvfp4_status nvfp4_debug_guard_shrink(uint64_t bytes);
 
 #ifdef __cplusplus
 }

@@ -26,7 +26,11 @@ import os
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libnvfp4.so")
+# NVFP4_DEBUG_GUARDS=1 in the environment loads the debug build, whose kernels
+# check every plain global access against its buffer's extent (same entry
+# points, same results; see include/nvfp4.h, "Index guards").
+GUARDED = os.environ.get("NVFP4_DEBUG_GUARDS", "0") not in ("", "0")
+LIB_PATH = os.path.join(_HERE, "libnvfp4_guarded.so" if GUARDED else "libnvfp4.so")
 
 NVFP4_OK = 0
 NVFP4_ERR_INVALID_ARG = 1
@@ -36,6 +40,7 @@ NVFP4_ERR_NONFINITE = 4
 NVFP4_ERR_TIMEOUT = 5
 NVFP4_ERR_CUDA = 6
 NVFP4_ERR_LAUNCH = 7
+NVFP4_ERR_GUARD = 8
 NVFP4_RNE = 0
 NVFP4_SR = 1
 NVFP4_SR_HW = 2              # the same rule, random bits in the hardware conversion's layout
@@ -60,7 +65,7 @@ class QStruct(ctypes.Structure):
 
 def _load():
     if not os.path.exists(LIB_PATH):
-        raise ImportError(f"libnvfp4.so is not built ({LIB_PATH}); run "
+        raise ImportError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
                           "`python -m nvfp4_block_scaled_29_b300.build` (needs nvcc)")
     L = ctypes.CDLL(LIB_PATH)
     st = ctypes.c_int
@@ -107,6 +112,12 @@ def _load():
     L.nvfp4_debug_inject.restype = st
     L.nvfp4_debug_check_div6.argtypes = [ctypes.c_uint32, ctypes.c_uint32, vp, vp, vp]
     L.nvfp4_debug_check_div6.restype = st
+    L.nvfp4_debug_guards_enabled.argtypes = []
+    L.nvfp4_debug_guards_enabled.restype = ctypes.c_int
+    L.nvfp4_debug_guard_record.argtypes = [ctypes.POINTER(ctypes.c_uint32), ctypes.POINTER(ctypes.c_uint64), vp]
+    L.nvfp4_debug_guard_record.restype = st
+    L.nvfp4_debug_guard_shrink.argtypes = [u64]
+    L.nvfp4_debug_guard_shrink.restype = st
     return L
 
 
@@ -301,6 +312,28 @@ def nvfp4_debug_inject(mode: int) -> int:
     reports NVFP4_ERR_TIMEOUT; mode 2 makes the next dual quantise take its
     64-bit Philox block-index path; mode 0 clears both (see include/nvfp4.h)."""
     return _check(int(lib.nvfp4_debug_inject(mode)), "nvfp4_debug_inject")
+
+
+def nvfp4_debug_guards_enabled() -> bool:
+    """True when the loaded library is the guarded debug build."""
+    return bool(lib.nvfp4_debug_guards_enabled())
+
+
+def nvfp4_debug_guard_record(stream=None):
+    """(site, byte offset) of the first access an index guard refused since
+    the last call, or None; clears the record (debug build; None otherwise)."""
+    site = ctypes.c_uint32(0)
+    off = ctypes.c_uint64(0)
+    _check(lib.nvfp4_debug_guard_record(ctypes.byref(site), ctypes.byref(off), _stream(stream)),
+           "nvfp4_debug_guard_record")
+    return None if site.value == 0 else (int(site.value), int(off.value))
+
+
+def nvfp4_debug_guard_shrink(nbytes: int) -> int:
+    """Test-only (debug build): every guard checks against its extent minus
+    nbytes, so in-bounds accesses near a buffer's end are refused and
+    reported; 0 restores the extents."""
+    return _check(int(lib.nvfp4_debug_guard_shrink(nbytes)), "nvfp4_debug_guard_shrink")
 
 
 def nvfp4_debug_check_div6(lo_bits: int, hi_bits: int, *, stream=None):

@@ -20,6 +20,7 @@
 #include <cstdint>
 #include <type_traits>
 #include "codec.cuh"
+#include "guard.cuh"
 #include "ptx.cuh"
 #include "quantize.cuh"
 #include "status.cuh"
@@ -190,8 +191,10 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                 const int64_t G = c0 / 64 + rg;
                 if (G < ngroups) {
                     uint32_t* sdst = reinterpret_cast<uint32_t*>(a1.scales + scale_offset(row, G * 4, ngroups));
+                    const bool s_ok =
+                        NVFP4_GUARD(a1.scales, scales_extent(a1.rows, a1.k), sdst, 4, kGuardDualScales);
                     if (row >= R) {
-                        *sdst = 0u;
+                        if (s_ok) *sdst = 0u;
                     } else {
                         const int nblk = (int)min64(4, nkb - G * 4);
                         uint32_t sw = 0, cw[8];
@@ -212,7 +215,8 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                             }
                         }
                         uint8_t* cdst = a1.codes + row * (C >> 1) + G * 32;
-                        if (nblk == 4 && (C & 31) == 0) {
+                        if (!NVFP4_GUARD(a1.codes, codes_extent(a1.rows, a1.k), cdst, 8 * nblk, kGuardDualCodes)) {
+                        } else if (nblk == 4 && (C & 31) == 0) {
                             reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
                             reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
                         } else {
@@ -220,7 +224,7 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                             for (int b = 0; b < 4; ++b)
                                 if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
                         }
-                        *sdst = sw;
+                        if (s_ok) *sdst = sw;
                     }
                 }
             }
@@ -234,9 +238,11 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                     uint16_t* s0 = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc, kb0, ngroups_t));
                     uint16_t* s1p = reinterpret_cast<uint16_t*>(a2.scales + scale_offset(cc + 1, kb0, ngroups_t));
                     const int nblk = (int)max64(0, min64(2, nkb_t - kb0));
+                    const bool s0_ok = NVFP4_GUARD(a2.scales, scales_extent(a2.rows, a2.k), s0, 2, kGuardDualScalesT);
+                    const bool s1_ok = NVFP4_GUARD(a2.scales, scales_extent(a2.rows, a2.k), s1p, 2, kGuardDualScalesT);
                     if (cc >= C || nblk == 0) {                  // C is even: both rows are padding
-                        *s0 = 0;
-                        *s1p = 0;
+                        if (s0_ok) *s0 = 0;
+                        if (s1_ok) *s1p = 0;
                     } else {
                         uint32_t sw0 = 0, sw1 = 0, c0w[4], c1w[4];
 #pragma unroll
@@ -268,7 +274,8 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                         for (int q = 0; q < 2; ++q) {
                             const uint32_t* cw = q ? c1w : c0w;
                             uint8_t* cdst = a2.codes + (cc + q) * (R >> 1) + kb0 * 8;
-                            if (nblk == 2 && (R & 31) == 0) {
+                            if (!NVFP4_GUARD(a2.codes, codes_extent(a2.rows, a2.k), cdst, 8 * nblk, kGuardDualCodesT)) {
+                            } else if (nblk == 2 && (R & 31) == 0) {
                                 *reinterpret_cast<uint4*>(cdst) = make_uint4(cw[0], cw[1], cw[2], cw[3]);
                             } else {
 #pragma unroll
@@ -276,8 +283,8 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                                     if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
                             }
                         }
-                        *s0 = (uint16_t)sw0;
-                        *s1p = (uint16_t)sw1;
+                        if (s0_ok) *s0 = (uint16_t)sw0;
+                        if (s1_ok) *s1p = (uint16_t)sw1;
                     }
                 }
             }

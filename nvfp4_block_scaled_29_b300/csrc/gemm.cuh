@@ -37,6 +37,7 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_bf16.h>
+#include "guard.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
 
@@ -130,7 +131,9 @@ __device__ __forceinline__ void store_chunk(const Args& a, int64_t row, int64_t 
     const bool full = col0 + 32 <= a.N;
     if (a.d_bf16) {
         uint16_t* dst = reinterpret_cast<uint16_t*>(a.d) + row * a.ldd + col0;
-        if (full) {
+        if (!NVFP4_GUARD(a.d, stored_extent(a.M, a.N, a.ldd, 2), dst, 2 * (uint32_t)min64(32, a.N - col0),
+                         kGuardGemmD)) {
+        } else if (full) {
             uint32_t p[16];
 #pragma unroll
             for (int j = 0; j < 16; ++j) {
@@ -149,7 +152,9 @@ __device__ __forceinline__ void store_chunk(const Args& a, int64_t row, int64_t 
         }
     } else {
         float* dst = reinterpret_cast<float*>(a.d) + row * a.ldd + col0;
-        if (full) {
+        if (!NVFP4_GUARD(a.d, stored_extent(a.M, a.N, a.ldd, 4), dst, 4 * (uint32_t)min64(32, a.N - col0),
+                         kGuardGemmD)) {
+        } else if (full) {
             float4* d4 = reinterpret_cast<float4*>(dst);
 #pragma unroll
             for (int j = 0; j < 8; ++j) d4[j] = make_float4(v[4 * j], v[4 * j + 1], v[4 * j + 2], v[4 * j + 3]);

@@ -19,6 +19,7 @@
 #pragma once
 #include <cstdint>
 #include "codec.cuh"
+#include "guard.cuh"
 #include "quantize.cuh"
 #include "status.cuh"
 
@@ -62,17 +63,20 @@ __global__ void __launch_bounds__(kQuantThreads, RHT ? 2 : 3) k_mx_quant_rows(co
         const int64_t g = w.minor;
         uint16_t* sdst = reinterpret_cast<uint16_t*>(a.scales + scale_offset(r, g * 2, col_tiles));
         const int nblk = (int)min64(2, nb - g * 2);
+        const bool s_ok = NVFP4_GUARD(a.scales, mx_scales_extent(a.rows, a.k), sdst, 2, kGuardMxScales);
         if (r >= a.rows || nblk <= 0) {
-            *sdst = 0;
+            if (s_ok) *sdst = 0;
             continue;
         }
         const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64);
+        const bool x_ok = NVFP4_GUARD(a.x, stored_extent(a.rows, a.k, a.ld, 2), src, 64 * nblk, kGuardMxX);
         uint4 raw[8];
 #pragma unroll
         for (int b = 0; b < 2; ++b)
             if (b < nblk) {
 #pragma unroll
-                for (int q = 0; q < 4; ++q) raw[4 * b + q] = ldg_stream(src + 4 * b + q);
+                for (int q = 0; q < 4; ++q)
+                    raw[4 * b + q] = x_ok ? ldg_stream(src + 4 * b + q) : make_uint4(0, 0, 0, 0);
             }
         uint32_t sw = 0, cw[8];
 #pragma unroll
@@ -121,7 +125,8 @@ __global__ void __launch_bounds__(kQuantThreads, RHT ? 2 : 3) k_mx_quant_rows(co
             }
         }
         uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
-        if (nblk == 2 && (a.k & 31) == 0 && ((r * (a.k >> 1)) & 15) == 0) {
+        if (!NVFP4_GUARD(a.codes, codes_extent(a.rows, a.k), cdst, 16 * nblk, kGuardMxCodes)) {
+        } else if (nblk == 2 && (a.k & 31) == 0 && ((r * (a.k >> 1)) & 15) == 0) {
             reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
             reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
         } else {
@@ -132,7 +137,7 @@ __global__ void __launch_bounds__(kQuantThreads, RHT ? 2 : 3) k_mx_quant_rows(co
                     reinterpret_cast<uint2*>(cdst)[2 * b + 1] = make_uint2(cw[4 * b + 2], cw[4 * b + 3]);
                 }
         }
-        *sdst = (uint16_t)sw;
+        if (s_ok) *sdst = (uint16_t)sw;
     }
     if (bad) record_device_error(NVFP4_DEV_NONFINITE);
 }
@@ -148,8 +153,11 @@ __global__ void __launch_bounds__(kQuantThreads) k_mx_dequant(const uint8_t* __r
     for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
          it += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = it / (k >> 4), kb = it - r * (k >> 4);          // 16-element chunk
-        const uint2 c = *reinterpret_cast<const uint2*>(codes + r * (k >> 1) + kb * 8);
-        const uint32_t sc = scales[scale_offset(r, kb >> 1, col_tiles)];
+        const uint8_t* csrc = codes + r * (k >> 1) + kb * 8;
+        const uint8_t* ssrc = scales + scale_offset(r, kb >> 1, col_tiles);
+        const uint2 c = NVFP4_GUARD(codes, codes_extent(rows, k), csrc, 8, kGuardMxDeqIn)
+                            ? *reinterpret_cast<const uint2*>(csrc) : make_uint2(0, 0);
+        const uint32_t sc = NVFP4_GUARD(scales, mx_scales_extent(rows, k), ssrc, 1, kGuardMxDeqIn) ? *ssrc : 0u;
         const float s = sc == 0xFFu ? __int_as_float(0x7FC00000) : __uint_as_float(sc << 23);  // 2^(sc-127)
         const float s_small = sc == 0 ? 0x1p-127f : s;                    // code 0 is 2^-127 (subnormal)
         float o[16];
@@ -169,12 +177,17 @@ __global__ void __launch_bounds__(kQuantThreads) k_mx_dequant(const uint8_t* __r
                 p[j] = *reinterpret_cast<const uint32_t*>(&h);
             }
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + r * ld + kb * 16);
-            dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-            dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 2), dst, 32, kGuardMxDeqOut)) {
+                dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+            }
         } else {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ld + kb * 16);
+            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 4), dst, 64, kGuardMxDeqOut)) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
         }
     }
 }

@@ -221,18 +221,14 @@ void set_sr_keys(QuantArgs* a, uint64_t seed, uint64_t stream_id, nvfp4_round ro
 
 bool valid_round(nvfp4_round r) { return r == NVFP4_RNE || r == NVFP4_SR || r == NVFP4_SR_HW; }
 
+// 1x16 quantisation of a transposed view with an odd number of logical rows
+// (the TMA-fed kernel takes row pairs): register-streaming kernel.
 template <bool RHT, bool SR>
-void launch_q1d(const QuantArgs& a, bool transposed, cudaStream_t st) {
-    const int64_t nkb = a.k / 16;
-    const int64_t ngroups = cdiv(nkb, 4);
+void launch_q1d_cols(const QuantArgs& a, cudaStream_t st) {
+    const int64_t ngroups = cdiv(a.k / 16, 4);
     const int64_t rows_pad = cdiv(a.rows, 128) * 128;
-    if (!transposed) {
-        k_quant1d_rows<RHT, SR><<<grid_for(rows_pad * ngroups, kQuantThreads, 8), kQuantThreads, 0,
-                                  st>>>(a);
-    } else {
-        k_quant1d_cols<RHT, SR><<<grid_for((rows_pad / 2) * ngroups, kQuantThreads, 1 << 20),
-                                  kQuantThreads, 0, st>>>(a);
-    }
+    k_quant1d_cols<RHT, SR><<<grid_for((rows_pad / 2) * ngroups, kQuantThreads, 1 << 20), kQuantThreads, 0,
+                              st>>>(a);
 }
 
 template <bool RHT, bool SR, bool EMIT_T>
@@ -339,11 +335,11 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
             return mask ? launch_dual_single_sr<2, true>(d, r, st) : launch_dual_single_sr<2, false>(d, r, st);
         }
         if (mask) {
-            if (sr) launch_q1d<true, true>(a, x.transposed, st);
-            else launch_q1d<true, false>(a, x.transposed, st);
+            if (sr) launch_q1d_cols<true, true>(a, st);
+            else launch_q1d_cols<true, false>(a, st);
         } else {
-            if (sr) launch_q1d<false, true>(a, x.transposed, st);
-            else launch_q1d<false, false>(a, x.transposed, st);
+            if (sr) launch_q1d_cols<false, true>(a, st);
+            else launch_q1d_cols<false, false>(a, st);
         }
         return launch_status();
     }
@@ -904,6 +900,7 @@ nvfp4_status nvfp4_get_status(cudaStream_t stream) {
                                 stream) != cudaSuccess)
         return NVFP4_ERR_CUDA;
     if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    if (word & NVFP4_DEV_GUARD) return NVFP4_ERR_GUARD;
     if (word & NVFP4_DEV_LAUNCH) return NVFP4_ERR_LAUNCH;
     if (word & NVFP4_DEV_TIMEOUT) return NVFP4_ERR_TIMEOUT;
     if (word & NVFP4_DEV_NONFINITE) return NVFP4_ERR_NONFINITE;
@@ -939,6 +936,48 @@ nvfp4_status nvfp4_debug_inject(int mode) {
     return NVFP4_OK;
 }
 
+int nvfp4_debug_guards_enabled(void) {
+#ifdef NVFP4_DEBUG_GUARDS
+    return 1;
+#else
+    return 0;
+#endif
+}
+
+nvfp4_status nvfp4_debug_guard_record(uint32_t* site, uint64_t* byte_offset, cudaStream_t stream) {
+    if (site == nullptr || byte_offset == nullptr) return NVFP4_ERR_INVALID_ARG;
+    *site = 0;
+    *byte_offset = 0;
+#ifdef NVFP4_DEBUG_GUARDS
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    unsigned long long rec = 0;
+    if (cudaMemcpyFromSymbolAsync(&rec, g_guard_record, sizeof(rec), 0, cudaMemcpyDeviceToHost, stream) !=
+        cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    const unsigned long long zero = 0;
+    if (cudaMemcpyToSymbolAsync(g_guard_record, &zero, sizeof(zero), 0, cudaMemcpyHostToDevice, stream) !=
+        cudaSuccess)
+        return NVFP4_ERR_CUDA;
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return NVFP4_ERR_CUDA;
+    *site = (uint32_t)(rec >> 48);
+    *byte_offset = rec & 0xFFFFFFFFFFFFull;
+#else
+    (void)stream;
+#endif
+    return NVFP4_OK;
+}
+
+nvfp4_status nvfp4_debug_guard_shrink(uint64_t bytes) {
+#ifdef NVFP4_DEBUG_GUARDS
+    const unsigned long long v = bytes;
+    if (cudaMemcpyToSymbol(g_guard_shrink, &v, sizeof(v)) != cudaSuccess) return NVFP4_ERR_CUDA;
+    return NVFP4_OK;
+#else
+    (void)bytes;
+    return NVFP4_ERR_INVALID_ARG;
+#endif
+}
+
 const char* nvfp4_status_string(nvfp4_status s) {
     switch (s) {
         case NVFP4_OK: return "ok";
@@ -949,6 +988,7 @@ const char* nvfp4_status_string(nvfp4_status s) {
         case NVFP4_ERR_TIMEOUT: return "device wait timed out";
         case NVFP4_ERR_CUDA: return "CUDA error";
         case NVFP4_ERR_LAUNCH: return "kernel launched with too little dynamic shared memory";
+        case NVFP4_ERR_GUARD: return "an index guard refused a global access (debug build)";
     }
     return "unknown status";
 }

@@ -9,21 +9,21 @@
 // scale), "Training stability and protection of sensitive layers" (16x16
 // weight blocks), "Techniques against outliers and rounding error" (RHT, SR).
 //
-// Work decomposition (all kernels are grid-stride, 256 threads per CTA):
-//  * rows variant: one thread owns 4 consecutive 16-element blocks (64
-//    elements) of one logical row: 8 x 16-byte loads, 32 bytes of codes and
-//    one 32-bit word of scales out (the 4 scales of a row are adjacent in the
-//    GEMM layout).
-//  * cols variant (transpose-on-load): one thread owns 2 adjacent logical
-//    rows x 64 logical columns; a warp reads 128 contiguous bytes of a stored
-//    row per load, so the stored tensor is read coalesced.
-//  * 2D variant: a 16-lane half-warp holds one 16x64 strip (one row per
-//    lane); the 16x16 block amax is a 4-step shuffle reduction.  The
-//    transposed operand is emitted from a shared-memory nibble tile.
+// Work decomposition (the 1x16 quantiser of stored arrays read by TMA is the
+// row-wise or column-wise path of the dual kernel, dual.cuh):
+//  * cols variant (transpose-on-load of a view with an odd number of logical
+//    rows; grid-stride, 256 threads per CTA): one thread owns 2 adjacent
+//    logical rows x 64 logical columns; a warp reads 128 contiguous bytes of
+//    a stored row per load, so the stored tensor is read coalesced.
+//  * 2D variant (persistent, TMA-fed): a 16-lane half-warp holds one 16x64
+//    strip (one row per lane); the 16x16 block amax is a 4-step shuffle
+//    reduction.  The transposed operand is emitted from a shared-memory
+//    nibble tile.
 #pragma once
 #include <cuda.h>
 #include <cstdint>
 #include "codec.cuh"
+#include "guard.cuh"
 #include "ptx.cuh"
 #include "status.cuh"
 
@@ -179,7 +179,7 @@ __global__ void k_publish_senc(const float* src, int src_is_senc, float* gs_out,
 // half-word SIMD maxima of the magnitude bit patterns (order-free and
 // NaN-propagating: a NaN pattern exceeds every finite one).
 __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t len, int64_t tid,
-                                                int64_t nt) {
+                                                int64_t nt, const uint16_t* gbase, uint64_t gext) {
     constexpr uint32_t M = 0x7FFF7FFFu;
     constexpr int U = 16;
     uint32_t m2 = 0, m1 = 0;
@@ -189,16 +189,20 @@ __device__ __forceinline__ uint32_t span_absmax(const uint16_t* base, int64_t le
     for (; i + (U - 1) * nt < nch; i += U * nt) {
         uint4 c[U];
 #pragma unroll
-        for (int u = 0; u < U; ++u) c[u] = ldg_stream_na(v + i + u * nt);
+        for (int u = 0; u < U; ++u)
+            c[u] = NVFP4_GUARD(gbase, gext, v + i + u * nt, 16, kGuardAmaxX) ? ldg_stream_na(v + i + u * nt)
+                                                                              : make_uint4(0, 0, 0, 0);
 #pragma unroll
         for (int u = 0; u < U; ++u)
             m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(c[u].x & M, c[u].y & M), __vmaxu2(c[u].z & M, c[u].w & M)));
     }
     for (; i < nch; i += nt) {
-        const uint4 a = ldg_stream_na(v + i);
+        const uint4 a = NVFP4_GUARD(gbase, gext, v + i, 16, kGuardAmaxX) ? ldg_stream_na(v + i)
+                                                                         : make_uint4(0, 0, 0, 0);
         m2 = __vmaxu2(m2, __vmaxu2(__vmaxu2(a.x & M, a.y & M), __vmaxu2(a.z & M, a.w & M)));
     }
-    for (int64_t j = (nch << 3) + tid; j < len; j += nt) m1 = max(m1, (uint32_t)(base[j] & 0x7FFFu));
+    for (int64_t j = (nch << 3) + tid; j < len; j += nt)
+        if (NVFP4_GUARD(gbase, gext, base + j, 2, kGuardAmaxX)) m1 = max(m1, (uint32_t)(base[j] & 0x7FFFu));
     return max(max(m2 & 0xFFFFu, m2 >> 16), m1);
 }
 
@@ -211,10 +215,10 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_amax_plain(const uint16_t*
     uint32_t m = 0;
     if (nrows == 1) {
         m = span_absmax(p, len, (int64_t)blockIdx.x * blockDim.x + threadIdx.x,
-                        (int64_t)gridDim.x * blockDim.x);
+                        (int64_t)gridDim.x * blockDim.x, p, stored_extent(1, len, len, 2));
     } else {
         for (int64_t r = blockIdx.x; r < nrows; r += gridDim.x)
-            m = max(m, span_absmax(p + r * ld, len, threadIdx.x, blockDim.x));
+            m = max(m, span_absmax(p + r * ld, len, threadIdx.x, blockDim.x, p, stored_extent(nrows, len, ld, 2)));
     }
     block_max_to_global(m << 16, out);
 }
@@ -232,6 +236,7 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
         const int64_t r = b / nkb, kb = b - r * nkb;
         const uint4* src = reinterpret_cast<const uint4*>(p + r * ld + kb * 16);
         float v[16];
+        if (!NVFP4_GUARD(p, stored_extent(rows, k, ld, 2), src, 32, kGuardAmaxX)) continue;
         unpack8(ldg_stream(src), v);
         unpack8(ldg_stream(src + 1), v + 8);
         m = max(m, rht16_absmax_bits_nan(v, sg));
@@ -253,6 +258,10 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_amax_rht_cols(const uint16
         const int64_t c0 = (int64_t)it.minor * 2;
         const uint16_t* base = p + it.major * 16 * ld + c0;
         uint32_t w[16];
+        if (!NVFP4_GUARD(p, stored_extent(srows, scols, ld, 2), base, c0 + 2 <= scols ? 4 : 2, kGuardAmaxX) ||
+            !NVFP4_GUARD(p, stored_extent(srows, scols, ld, 2), base + 15 * ld, c0 + 2 <= scols ? 4 : 2,
+                         kGuardAmaxX))
+            continue;
         if (c0 + 2 <= scols) {
 #pragma unroll
             for (int t = 0; t < 16; ++t) w[t] = ldg_u32(base + t * ld);
@@ -371,62 +380,6 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
     }
 }
 
-// Non-transposed view: thread item = (row, group of 4 blocks).
-template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads, SR ? 2 : 3) k_quant1d_rows(const QuantArgs a) {
-    __shared__ float rtab[128];
-    float s_enc;
-    if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
-    init_rtab(rtab, s_enc);
-    const int64_t nkb = a.k >> 4;
-    const uint32_t ngroups = (uint32_t)((nkb + 3) >> 2);
-    const int64_t rows_pad = (a.rows + 127) & ~int64_t(127);
-    const bool vec16 = (a.k & 31) == 0;
-    for (ItemWalk w(ngroups); w.major < rows_pad; w.next()) {
-        const int64_t r = w.major;
-        const uint32_t g = w.minor;
-        uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
-        if (r >= a.rows) {
-            *sdst = 0u;
-            continue;
-        }
-        const int nblk = (int)min64(4, nkb - (int64_t)g * 4);
-        const uint4* src = reinterpret_cast<const uint4*>(a.x + r * a.ld + g * 64);
-        uint4 raw[8];
-#pragma unroll
-        for (int b = 0; b < 4; ++b)
-            if (b < nblk) {
-                raw[2 * b] = ldg_stream(src + 2 * b);
-                raw[2 * b + 1] = ldg_stream(src + 2 * b + 1);
-            }
-        uint32_t sw = 0, cw[8];
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            cw[2 * b] = cw[2 * b + 1] = 0u;
-            if (b < nblk) {
-                float v[16];
-                unpack8(raw[2 * b], v);
-                unpack8(raw[2 * b + 1], v + 8);
-                uint32_t sb;
-                encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)(r * a.k + g * 64 + b * 16), a, &sb,
-                                        &cw[2 * b], &cw[2 * b + 1],
-                                        RHT ? ~0u : absmax_bits16_packed(raw[2 * b], raw[2 * b + 1]));
-                sw |= sb << (8 * b);
-            }
-        }
-        uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
-        if (nblk == 4 && vec16) {
-            reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
-            reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
-        } else {
-#pragma unroll
-            for (int b = 0; b < 4; ++b)
-                if (b < nblk) reinterpret_cast<uint2*>(cdst)[b] = make_uint2(cw[2 * b], cw[2 * b + 1]);
-        }
-        *sdst = sw;
-    }
-}
-
 // 16 stored rows x 2 stored columns starting at src (one 16-element block of
 // two logical rows of the transposed view), one 32-bit word per stored row.
 __device__ __forceinline__ void load_col_pair(const uint16_t* src, int64_t ld, bool has2, uint32_t* w) {
@@ -459,9 +412,11 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(const QuantAr
         const int64_t r0 = (int64_t)it.minor * 2;
         uint32_t* s0 = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0, g * 4, ngroups));
         uint32_t* s1 = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups));
+        const bool s0_ok = NVFP4_GUARD(a.scales, scales_extent(a.rows, a.k), s0, 4, kGuardQ1dScales);
+        const bool s1_ok = NVFP4_GUARD(a.scales, scales_extent(a.rows, a.k), s1, 4, kGuardQ1dScales);
         if (r0 >= a.rows) {
-            *s0 = 0u;
-            *s1 = 0u;
+            if (s0_ok) *s0 = 0u;
+            if (s1_ok) *s1 = 0u;
             continue;
         }
         const bool has2 = r0 + 1 < a.rows;
@@ -470,27 +425,46 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(const QuantAr
         uint8_t* c0 = a.codes + r0 * (a.k >> 1) + g * 32;
         uint8_t* c1 = c0 + (a.k >> 1);
         uint32_t sw0 = 0, sw1 = 0;
+        // the loads of block b: stored rows g*64 + 16b .. +15, 2 (or 1) columns
+        auto x_ok = [&](int b) {
+            const uint64_t ext = stored_extent(a.k, a.rows, a.ld, 2);
+            const uint16_t* p0 = src + b * 16 * a.ld;
+            return NVFP4_GUARD(a.x, ext, p0, has2 ? 4 : 2, kGuardQ1dX) &&
+                   NVFP4_GUARD(a.x, ext, p0 + 15 * a.ld, has2 ? 4 : 2, kGuardQ1dX);
+        };
         uint32_t w[16];
-        load_col_pair(src, a.ld, has2, w);
+        if (x_ok(0)) load_col_pair(src, a.ld, has2, w);
+        else {
+#pragma unroll
+            for (int t = 0; t < 16; ++t) w[t] = 0u;
+        }
 #pragma unroll
         for (int b = 0; b < 4; ++b) {
             if (b < nblk) {
                 uint32_t wn[16];
-                if (b + 1 < nblk) load_col_pair(src + (b + 1) * 16 * a.ld, a.ld, has2, wn);
+                if (b + 1 < nblk) {
+                    if (x_ok(b + 1)) load_col_pair(src + (b + 1) * 16 * a.ld, a.ld, has2, wn);
+                    else {
+#pragma unroll
+                        for (int t = 0; t < 16; ++t) wn[t] = 0u;
+                    }
+                }
                 const int64_t kc = g * 64 + b * 16;
                 float v[16];
                 uint32_t sb, lo, hi;
 #pragma unroll
                 for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
                 encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)(r0 * a.k + kc), a, &sb, &lo, &hi);
-                reinterpret_cast<uint2*>(c0)[b] = make_uint2(lo, hi);
+                if (NVFP4_GUARD(a.codes, codes_extent(a.rows, a.k), c0 + 8 * b, 8, kGuardQ1dCodes))
+                    reinterpret_cast<uint2*>(c0)[b] = make_uint2(lo, hi);
                 sw0 |= sb << (8 * b);
                 if (has2) {
 #pragma unroll
                     for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
                     encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)((r0 + 1) * a.k + kc), a, &sb, &lo,
                                             &hi);
-                    reinterpret_cast<uint2*>(c1)[b] = make_uint2(lo, hi);
+                    if (NVFP4_GUARD(a.codes, codes_extent(a.rows, a.k), c1 + 8 * b, 8, kGuardQ1dCodes))
+                        reinterpret_cast<uint2*>(c1)[b] = make_uint2(lo, hi);
                     sw1 |= sb << (8 * b);
                 }
                 if (b + 1 < nblk) {
@@ -499,8 +473,8 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(const QuantAr
                 }
             }
         }
-        *s0 = sw0;
-        *s1 = sw1;
+        if (s0_ok) *s0 = sw0;
+        if (s1_ok) *s1 = sw1;
     }
 }
 
@@ -707,10 +681,13 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
         // primary operand
         if (a.write_primary && grp_ok) {
             uint32_t* sdst = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r, g * 4, ngroups));
-            if (r < ((a.rows + 127) & ~int64_t(127))) *sdst = row_ok ? sw : 0u;
+            if (r < ((a.rows + 127) & ~int64_t(127)) &&
+                NVFP4_GUARD(a.scales, scales_extent(a.rows, a.k), sdst, 4, kGuardQ2dScales))
+                *sdst = row_ok ? sw : 0u;
             if (row_ok) {
                 uint8_t* cdst = a.codes + r * (a.k >> 1) + g * 32;
-                if (nblk == 4 && (a.k & 31) == 0) {
+                if (!NVFP4_GUARD(a.codes, codes_extent(a.rows, a.k), cdst, 8 * nblk, kGuardQ2dCodes)) {
+                } else if (nblk == 4 && (a.k & 31) == 0) {
                     reinterpret_cast<uint4*>(cdst)[0] = make_uint4(cw[0], cw[1], cw[2], cw[3]);
                     reinterpret_cast<uint4*>(cdst)[1] = make_uint4(cw[4], cw[5], cw[6], cw[7]);
                 } else {
@@ -748,7 +725,8 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                     uint32_t* sdst_t =
                         reinterpret_cast<uint32_t*>(a.scales_t + scale_offset(ct, gt * 4, ngroups_t));
                     const int kb_local = threadIdx.x >> 4;
-                    *sdst_t = ct >= a.k ? 0u
+                    if (NVFP4_GUARD(a.scales_t, scales_extent(a.k, kt), sdst_t, 4, kGuardQ2dScalesT))
+                        *sdst_t = ct >= a.k ? 0u
                                         : (uint32_t)tile_sb[0][kb_local] | ((uint32_t)tile_sb[1][kb_local] << 8) |
                                               ((uint32_t)tile_sb[2][kb_local] << 16) |
                                               ((uint32_t)tile_sb[3][kb_local] << 24);
@@ -767,7 +745,9 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                     uint8_t* cdst = a.codes_t + c0 * (kt >> 1) + (row0 >> 1) + rb * 4;
 #pragma unroll
                     for (int n = 0; n < 8; ++n)
-                        if (c0 + n < a.k) *reinterpret_cast<uint32_t*>(cdst + n * (kt >> 1)) = x[n];
+                        if (c0 + n < a.k &&
+                            NVFP4_GUARD(a.codes_t, codes_extent(a.k, kt), cdst + n * (kt >> 1), 4, kGuardQ2dCodesT))
+                            *reinterpret_cast<uint32_t*>(cdst + n * (kt >> 1)) = x[n];
                 }
             }
         }
@@ -796,8 +776,12 @@ __global__ void __launch_bounds__(kQuantThreads) k_dequant(const uint8_t* __rest
     for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
          it += (int64_t)gridDim.x * blockDim.x) {
         const int64_t r = it / nkb, kb = it - r * nkb;
-        const uint2 c = *reinterpret_cast<const uint2*>(codes + r * (k >> 1) + kb * 8);
-        const float sb = e4m3_value(scales[scale_offset(r, kb, ngroups)]);
+        const uint8_t* csrc = codes + r * (k >> 1) + kb * 8;
+        const uint8_t* ssrc = scales + scale_offset(r, kb, ngroups);
+        const uint2 c = NVFP4_GUARD(codes, codes_extent(rows, k), csrc, 8, kGuardDeqIn)
+                            ? *reinterpret_cast<const uint2*>(csrc) : make_uint2(0, 0);
+        const float sb = e4m3_value(NVFP4_GUARD(scales, scales_extent(rows, k), ssrc, 1, kGuardDeqIn) ? *ssrc
+                                                                                                   : (uint8_t)0);
         float o[16];
 #pragma unroll
         for (int j = 0; j < 16; ++j) {
@@ -816,12 +800,17 @@ __global__ void __launch_bounds__(kQuantThreads) k_dequant(const uint8_t* __rest
                 p[j] = *reinterpret_cast<const uint32_t*>(&h);
             }
             uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + r * ld + kb * 16);
-            dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-            dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 2), dst, 32, kGuardDeqOut)) {
+                dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
+                dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
+            }
         } else {
             float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ld + kb * 16);
+            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 4), dst, 64, kGuardDeqOut)) {
 #pragma unroll
-            for (int j = 0; j < 4; ++j) dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+                for (int j = 0; j < 4; ++j)
+                    dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
+            }
         }
     }
 }

@@ -53,8 +53,51 @@ def test_scale_bytes_matches_oracle(nv):
 
 
 def test_status_strings(nv):
-    for s in range(7):
+    for s in range(9):
         assert nv.status_string(s) and "unknown" not in nv.status_string(s)
+    assert "unknown" in nv.status_string(9)
+
+
+@pytest.fixture(scope="module")
+def guarded():
+    """The index-guarded debug build (libnvfp4_guarded.so)."""
+    from nvfp4_block_scaled_29_b300 import build
+    lib = ctypes.CDLL(build.build(guards=True))
+    lib.nvfp4_debug_guard_record.restype = ctypes.c_int
+    lib.nvfp4_debug_guard_shrink.restype = ctypes.c_int
+    return lib
+
+
+def test_guarded_library_exports_every_declared_symbol(guarded):
+    for name in _declared_functions():
+        assert hasattr(guarded, name), name
+
+
+def test_guard_entry_points(nv, guarded):
+    """Which build is which, and the calls that need no GPU in either."""
+    from nvfp4_block_scaled_29_b300 import build
+    normal = ctypes.CDLL(build.LIB)
+    normal.nvfp4_debug_guard_record.restype = ctypes.c_int
+    normal.nvfp4_debug_guard_shrink.restype = ctypes.c_int
+    assert normal.nvfp4_debug_guards_enabled() == 0
+    assert guarded.nvfp4_debug_guards_enabled() == 1
+    site, off = ctypes.c_uint32(7), ctypes.c_uint64(9)
+    assert normal.nvfp4_debug_guard_record(ctypes.byref(site), ctypes.byref(off), None) == nv.NVFP4_OK
+    assert site.value == 0 and off.value == 0
+    assert normal.nvfp4_debug_guard_shrink(ctypes.c_uint64(8)) == nv.NVFP4_ERR_INVALID_ARG
+    assert guarded.nvfp4_debug_guard_record(None, None, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert normal.nvfp4_debug_guard_record(None, None, None) == nv.NVFP4_ERR_INVALID_ARG
+    assert nv.NVFP4_ERR_GUARD == 8 and "guard" in nv.status_string(nv.NVFP4_ERR_GUARD)
+
+
+def test_guard_sites_are_documented():
+    """The public header names the range of guard sites that csrc/guard.cuh
+    defines."""
+    text = open(os.path.join(ROOT, "nvfp4_block_scaled_29_b300", "csrc", "guard.cuh")).read()
+    sites = [int(v) for v in re.findall(r"kGuard\w+ = (\d+),", text)]
+    assert sites == list(range(1, len(sites) + 1))
+    hdr = open(os.path.join(ROOT, "include", "nvfp4.h")).read()
+    assert f"1..{len(sites)}" in hdr
 
 
 def _view(nv, ptr, rows, cols, ld, tr=0):
