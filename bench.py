@@ -723,6 +723,17 @@ def time_calls(nv, torch, step, hbm_peak: float, reps: int = 5) -> dict:
         else:
             g = nbytes / (ms * 1e-3) / 1e9
             rows[name] = {"ms": round(ms, 4), "gbs": round(g, 1), "frac_hbm": round(g / hbm_peak, 3)}
+    # reference for the write-dominated dequantiser: torch's fill kernel
+    # writing the same 84 MB output (a write-only stream runs well below the
+    # copy bandwidth on this part)
+    wbytes = TOKENS * HIDDEN * 2
+    ms = _timed_median(torch, step, lambda: deq.fill_(1.0), reps)
+    g = wbytes / (ms * 1e-3) / 1e9
+    rows["write_ref_x"] = {"ms": round(ms, 4), "gbs": round(g, 1), "frac_hbm": round(g / hbm_peak, 3),
+                           "kernel": "torch fill_ (library), 84 MB bf16 write"}
+    d = rows["dequantize_x"]
+    d["write_gbs"] = round(wbytes / (d["ms"] * 1e-3) / 1e9, 1)
+    d["frac_of_write_ref"] = round(d["write_gbs"] / g, 3)
     st = nv.nvfp4_get_status()
     if st != nv.NVFP4_OK:
         raise SystemExit(f"device status after the per-call timing: {nv.status_string(st)}")

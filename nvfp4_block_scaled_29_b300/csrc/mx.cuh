@@ -142,54 +142,22 @@ __global__ void __launch_bounds__(kQuantThreads, RHT ? 2 : 3) k_mx_quant_rows(co
     if (bad) record_device_error(NVFP4_DEV_NONFINITE);
 }
 
-// x_hat = q * 2^X (exact) as fp32 or bf16 (RNE).
+// x_hat = q * 2^X (exact) as fp32 or bf16 (RNE); the codes are decoded
+// exactly (times an f16 one) and scaled in fp32.
 template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads) k_mx_dequant(const uint8_t* __restrict__ codes,
                                                               const uint8_t* __restrict__ scales,
                                                               int64_t rows, int64_t k, void* out, int64_t ld) {
-    const int64_t nb = k >> 5;
-    const int64_t col_tiles = (nb + 3) >> 2;
-    const int64_t total = rows * (k >> 4);
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = it / (k >> 4), kb = it - r * (k >> 4);          // 16-element chunk
-        const uint8_t* csrc = codes + r * (k >> 1) + kb * 8;
-        const uint8_t* ssrc = scales + scale_offset(r, kb >> 1, col_tiles);
-        const uint2 c = NVFP4_GUARD(codes, codes_extent(rows, k), csrc, 8, kGuardMxDeqIn)
-                            ? *reinterpret_cast<const uint2*>(csrc) : make_uint2(0, 0);
-        const uint32_t sc = NVFP4_GUARD(scales, mx_scales_extent(rows, k), ssrc, 1, kGuardMxDeqIn) ? *ssrc : 0u;
-        const float s = sc == 0xFFu ? __int_as_float(0x7FC00000) : __uint_as_float(sc << 23);  // 2^(sc-127)
-        const float s_small = sc == 0 ? 0x1p-127f : s;                    // code 0 is 2^-127 (subnormal)
-        float o[16];
+    dequant_walk<BF16, 32>(codes, scales, mx_scales_extent(rows, k), rows, k, out, ld, kGuardMxDeqIn,
+                           kGuardMxDeqOut, [](uint32_t cw, uint32_t sc, float* o) {
+                               e2m1x8_times_scale(cw, 0x3C003C00u, o);                 // f16x2 (1, 1)
+                               // 2^(sc - 127); code 0 is 2^-127 (subnormal), 0xFF NaN
+                               const float s = sc == 0xFFu ? __int_as_float(0x7FC00000)
+                                               : sc == 0u  ? 0x1p-127f
+                                                           : __uint_as_float(sc << 23);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint32_t q = ((j < 8 ? c.x : c.y) >> (4 * (j & 7))) & 0xFu;
-            const float mag = (q & 7u) < 4u ? __fmul_rn((float)(q & 7u), 0.5f)
-                              : (q & 7u) < 6u ? (float)((q & 7u) - 2u)
-                              : (q & 7u) == 6u ? 4.0f : 6.0f;
-            o[j] = __fmul_rn((q & 8u) ? -mag : mag, s_small);
-        }
-        if (BF16) {
-            uint32_t p[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-                p[j] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + r * ld + kb * 16);
-            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 2), dst, 32, kGuardMxDeqOut)) {
-                dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
-            }
-        } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ld + kb * 16);
-            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 4), dst, 64, kGuardMxDeqOut)) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            }
-        }
-    }
+                               for (int j = 0; j < 8; ++j) o[j] = __fmul_rn(o[j], s);
+                           });
 }
 
 }  // namespace nvfp4

@@ -729,7 +729,8 @@ nvfp4_status nvfp4_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, int6
     if (out == nullptr || ld < q->k) return NVFP4_ERR_INVALID_ARG;
     const int64_t esz = out_is_bf16 ? 2 : 4;
     if (!aligned(out, 16) || (ld * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
-    const int g = grid_for(q->rows * (q->k / 16), kQuantThreads, 8);
+    // one warp per 256-element chunk of a row, kDeqUnroll chunks per pass
+    const int g = grid_for(q->rows * cdiv(q->k, 256) * 32 / kDeqUnroll, kQuantThreads, 5);
     if (out_is_bf16)
         k_dequant<true><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->global_scale,
                                                           q->rows, q->k, out, ld);
@@ -835,7 +836,7 @@ nvfp4_status nvfp4_mx_dequantize(const nvfp4_q* q, void* out, int out_is_bf16, i
     if (q->codes == nullptr || q->scales == nullptr || out == nullptr || ld < q->k) return NVFP4_ERR_INVALID_ARG;
     const int64_t esz = out_is_bf16 ? 2 : 4;
     if (!aligned(q->codes, 16) || !aligned(out, 16) || (ld * esz) % 16 != 0) return NVFP4_ERR_MISALIGNED;
-    const int g = grid_for(q->rows * (q->k / 16), kQuantThreads, 8);
+    const int g = grid_for(q->rows * cdiv(q->k, 256) * 32 / kDeqUnroll, kQuantThreads, 4);
     if (out_is_bf16) k_mx_dequant<true><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->rows, q->k, out, ld);
     else k_mx_dequant<false><<<g, kQuantThreads, 0, stream>>>(q->codes, q->scales, q->rows, q->k, out, ld);
     return launch_status();

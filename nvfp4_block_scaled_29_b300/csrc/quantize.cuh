@@ -763,6 +763,115 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
 }
 
 // ======================================================== dequantise ======
+// Two copies of the scale value as f16x2 (exact: a block scale is an E4M3
+// value, at most 480 in magnitude with 4 significant bits).
+__device__ __forceinline__ uint32_t f16x2_splat(float s) {
+    uint32_t d;
+    asm("cvt.rn.f16x2.f32 %0, %1, %1;" : "=r"(d) : "f"(s));
+    return d;
+}
+
+// q * s_b for the 8 E2M1 codes of a word (element j in nibble j), exactly,
+// as 8 floats: the hardware conversion decodes the codes in pairs to f16x2
+// (exact), one f16x2 multiply per pair forms q * s_b (exact: |q s_b| <= 6 *
+// 480 with at most 6 significant bits, and never below 2^-10, the f16
+// normal range), and the products are widened to fp32 (exact).
+__device__ __forceinline__ void e2m1x8_times_scale(uint32_t codes, uint32_t sb2, float* p) {
+    uint32_t h[4];
+    asm("{\n\t.reg .b8 c0, c1, c2, c3;\n\t"
+        "mov.b32 {c0, c1, c2, c3}, %4;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %0, c0;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %1, c1;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %2, c2;\n\t"
+        "cvt.rn.f16x2.e2m1x2 %3, c3;\n\t}"
+        : "=r"(h[0]), "=r"(h[1]), "=r"(h[2]), "=r"(h[3])
+        : "r"(codes));
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        asm("{\n\t.reg .f16 lo, hi;\n\t"
+            "mul.rn.f16x2 %2, %2, %3;\n\t"
+            "mov.b32 {lo, hi}, %2;\n\t"
+            "cvt.f32.f16 %0, lo;\n\t"
+            "cvt.f32.f16 %1, hi;\n\t}"
+            : "=f"(p[2 * j]), "=f"(p[2 * j + 1]), "+r"(h[j])
+            : "r"(sb2));
+    }
+}
+
+// The walk of the dequantisers.  A warp takes 256 consecutive elements of a
+// row at a time, 8 per lane, so that its code loads (4 bytes a lane) and its
+// output stores (16 or 32 bytes a lane) each cover one contiguous span; the
+// (row, chunk) walk is warp-uniform and free of 64-bit divides, and a warp
+// gathers the loads of kDeqUnroll chunks before it converts and stores
+// them.  decode(codes, scale byte, o) turns a lane's 8 codes and the scale
+// byte of their block (BLOCK elements, swizzled layout) into 8 floats.
+constexpr int kDeqUnroll = 4;
+
+template <bool BF16, int BLOCK, class Decode>
+__device__ __forceinline__ void dequant_walk(const uint8_t* __restrict__ codes, const uint8_t* __restrict__ scales,
+                                             uint64_t scales_ext, int64_t rows, int64_t k, void* out, int64_t ld,
+                                             uint32_t site_in, uint32_t site_out, Decode decode) {
+    const int lane = threadIdx.x & 31;
+    const int64_t col_tiles = ((k / BLOCK) + 3) >> 2;
+    const uint32_t nchunks = (uint32_t)((k + 255) >> 8);
+    const int64_t w0 = ((int64_t)blockIdx.x * blockDim.x + threadIdx.x) >> 5;
+    const int64_t nw = ((int64_t)gridDim.x * blockDim.x) >> 5;
+    int64_t r = w0 / nchunks;
+    uint32_t ch = (uint32_t)(w0 - r * nchunks);
+    const int64_t dr = nw / nchunks;
+    const uint32_t dch = (uint32_t)(nw - dr * nchunks);
+    while (r < rows) {
+        uint32_t cw[kDeqUnroll], sc[kDeqUnroll];
+        int64_t e0[kDeqUnroll];
+        bool ok[kDeqUnroll];
+#pragma unroll
+        for (int u = 0; u < kDeqUnroll; ++u) {
+            const int64_t c = (int64_t)ch * 256 + lane * 8;            // c < k implies c + 8 <= k
+            ok[u] = r < rows && c < k;
+            cw[u] = 0u;
+            sc[u] = 0u;
+            e0[u] = r * ld + c;
+            if (ok[u]) {
+                const uint8_t* csrc = codes + r * (k >> 1) + (c >> 1);
+                const uint8_t* ssrc = scales + scale_offset(r, c / BLOCK, col_tiles);
+                if (NVFP4_GUARD(codes, codes_extent(rows, k), csrc, 4, site_in))
+                    cw[u] = __ldg(reinterpret_cast<const uint32_t*>(csrc));
+                if (NVFP4_GUARD(scales, scales_ext, ssrc, 1, site_in)) sc[u] = __ldg(ssrc);
+            }
+            ch += dch;
+            r += dr;
+            if (ch >= nchunks) {
+                ch -= nchunks;
+                ++r;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kDeqUnroll; ++u) {
+            if (!ok[u]) continue;
+            float o[8];
+            decode(cw[u], sc[u], o);
+            if (BF16) {
+                uint32_t p[4];
+#pragma unroll
+                for (int j = 0; j < 4; ++j) {
+                    const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
+                    p[j] = *reinterpret_cast<const uint32_t*>(&h);
+                }
+                uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + e0[u]);
+                if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 2), dst, 16, site_out))
+                    *dst = make_uint4(p[0], p[1], p[2], p[3]);
+            } else {
+                float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + e0[u]);
+                if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 4), dst, 32, site_out)) {
+                    dst[0] = make_float4(o[0], o[1], o[2], o[3]);
+                    dst[1] = make_float4(o[4], o[5], o[6], o[7]);
+                }
+            }
+        }
+    }
+}
+
+// x_hat = fp32(fp32(q * s_b) * fp32(1 / S_enc)), as fp32 or bf16 (RNE).
 template <bool BF16>
 __global__ void __launch_bounds__(kQuantThreads) k_dequant(const uint8_t* __restrict__ codes,
                                                            const uint8_t* __restrict__ scales,
@@ -770,49 +879,12 @@ __global__ void __launch_bounds__(kQuantThreads) k_dequant(const uint8_t* __rest
                                                            int64_t rows, int64_t k, void* out,
                                                            int64_t ld) {
     const float inv = __frcp_rn(*gs);
-    const int64_t nkb = k >> 4;
-    const int64_t ngroups = (nkb + 3) >> 2;
-    const int64_t total = rows * nkb;
-    for (int64_t it = (int64_t)blockIdx.x * blockDim.x + threadIdx.x; it < total;
-         it += (int64_t)gridDim.x * blockDim.x) {
-        const int64_t r = it / nkb, kb = it - r * nkb;
-        const uint8_t* csrc = codes + r * (k >> 1) + kb * 8;
-        const uint8_t* ssrc = scales + scale_offset(r, kb, ngroups);
-        const uint2 c = NVFP4_GUARD(codes, codes_extent(rows, k), csrc, 8, kGuardDeqIn)
-                            ? *reinterpret_cast<const uint2*>(csrc) : make_uint2(0, 0);
-        const float sb = e4m3_value(NVFP4_GUARD(scales, scales_extent(rows, k), ssrc, 1, kGuardDeqIn) ? *ssrc
-                                                                                                   : (uint8_t)0);
-        float o[16];
+    dequant_walk<BF16, 16>(codes, scales, scales_extent(rows, k), rows, k, out, ld, kGuardDeqIn, kGuardDeqOut,
+                           [inv](uint32_t cw, uint32_t sc, float* o) {
+                               e2m1x8_times_scale(cw, f16x2_splat(e4m3_value(sc)), o);
 #pragma unroll
-        for (int j = 0; j < 16; ++j) {
-            const uint32_t q = ((j < 8 ? c.x : c.y) >> (4 * (j & 7))) & 0xFu;
-            const float mag = (q & 7u) < 4u ? __fmul_rn((float)(q & 7u), 0.5f)
-                              : (q & 7u) < 6u ? (float)((q & 7u) - 2u)
-                              : (q & 7u) == 6u ? 4.0f : 6.0f;
-            const float qv = (q & 8u) ? -mag : mag;
-            o[j] = __fmul_rn(__fmul_rn(qv, sb), inv);
-        }
-        if (BF16) {
-            uint32_t p[8];
-#pragma unroll
-            for (int j = 0; j < 8; ++j) {
-                const __nv_bfloat162 h = __floats2bfloat162_rn(o[2 * j], o[2 * j + 1]);
-                p[j] = *reinterpret_cast<const uint32_t*>(&h);
-            }
-            uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(out) + r * ld + kb * 16);
-            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 2), dst, 32, kGuardDeqOut)) {
-                dst[0] = make_uint4(p[0], p[1], p[2], p[3]);
-                dst[1] = make_uint4(p[4], p[5], p[6], p[7]);
-            }
-        } else {
-            float4* dst = reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + r * ld + kb * 16);
-            if (NVFP4_GUARD(out, stored_extent(rows, k, ld, 4), dst, 64, kGuardDeqOut)) {
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    dst[j] = make_float4(o[4 * j], o[4 * j + 1], o[4 * j + 2], o[4 * j + 3]);
-            }
-        }
-    }
+                               for (int j = 0; j < 8; ++j) o[j] = __fmul_rn(o[j], inv);
+                           });
 }
 
 }  // namespace nvfp4

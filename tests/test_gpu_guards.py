@@ -378,20 +378,23 @@ def test_guard_shrink_dual(nv, shrink):
 
 
 def test_guard_shrink_dequantize(nv, shrink):
-    # rows 200: the scale buffer's last 8 bytes are padding rows, never read;
-    # the last block's code load and its 64-byte store are refused
+    # rows 200: the scale buffer's last 8 bytes are padding rows, never read.
+    # The last two 4-byte code loads (row 199, elements 496..511) are refused
+    # and read zeros; of the two 32-byte stores of those elements, the last
+    # one reaches into the last 8 bytes and is refused.
     d = dev_bf16(_x(200, 512, 59))
     q = nv.QTensor(200, 512)
     nv.nvfp4_quantize_1d(d, nv.nvfp4_amax(d), nv.NVFP4_RNE, 0, 0, q)
     ref = torch.empty((200, 512), dtype=torch.float32, device="cuda")
     nv.nvfp4_dequantize(q, ref)
     _ok(nv)
+    ref.view(-1)[-16:-8] = 0.0
     out = torch.empty_like(ref)
     out.view(torch.uint8).fill_(CANARY)
     shrink(8)
     nv.nvfp4_dequantize(q, out)
     _refused(nv, DEQ)
-    _tail_check(out, ref, 64)
+    _tail_check(out, ref, 32)
 
 
 def test_guard_shrink_gemm(nv, shrink):
