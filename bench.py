@@ -308,7 +308,24 @@ PROFILE_CASES = {
                                                            s.mask, s.amax[3:4], s.nv.NVFP4_SR_HW, SR_SEED, 2, s.qdyt),
     "quant_dual_x": lambda s: s.nv.nvfp4_quantize_dual(s.x, s.amax[0:1], s.nv.NVFP4_RNE, 0, 0, s.qx, s.mask,
                                                        s.amax[4:5], s.nv.NVFP4_RNE, 0, 0, s.qxt),
+    # the library GEMM of the comparison (cuBLASLt through torch) on the forward operands
+    "gemm_fwd_library": lambda s: library_gemm_call(s, s.qx, s.qw)(),
 }
+
+
+def library_gemm_call(step, a, b):
+    """cuBLASLt's NVFP4 GEMM (torch.nn.functional.scaled_mm, 1x16 E4M3 block
+    scales in the same swizzled layout) of two quantised operands, bf16 out,
+    as a callable.  Block scales only: the tensor scales (alpha) are left
+    out, which does not change the work."""
+    import torch
+    import torch.nn.functional as F
+    A = a.codes.view(torch.float4_e2m1fn_x2)
+    B = b.codes.view(torch.float4_e2m1fn_x2).t()
+    sa, sb = a.scales.view(torch.float8_e4m3fn), b.scales.view(torch.float8_e4m3fn)
+    return lambda: F.scaled_mm(A, B, sa, F.ScalingType.BlockWise1x16, sb, F.ScalingType.BlockWise1x16,
+                               F.SwizzleType.SWIZZLE_32_4_4, F.SwizzleType.SWIZZLE_32_4_4,
+                               output_dtype=torch.bfloat16)
 
 
 def torch_int16(torch):
@@ -745,18 +762,10 @@ def time_library_gemm(torch, step, reps: int = 5) -> dict:
     E4M3 block scales in the same swizzled layout) on the step's quantised
     operands, as a library comparison beside nvfp4_gemm.  Block scales only:
     the tensor scales (alpha) are left out, which does not change the work."""
-    import torch.nn.functional as F
     out = {}
     try:
-        for name, a, b, d in (("fwd", step.qx, step.qw, step.y), ("dgrad", step.qdy, step.qwt, step.dx),
-                              ("wgrad", step.qdyt, step.qxt, step.dw)):
-            A = a.codes.view(torch.float4_e2m1fn_x2)
-            B = b.codes.view(torch.float4_e2m1fn_x2).t()
-            sa, sb = a.scales.view(torch.float8_e4m3fn), b.scales.view(torch.float8_e4m3fn)
-            fn = lambda: F.scaled_mm(A, B, sa, F.ScalingType.BlockWise1x16, sb, F.ScalingType.BlockWise1x16,
-                                     F.SwizzleType.SWIZZLE_32_4_4, F.SwizzleType.SWIZZLE_32_4_4,
-                                     output_dtype=torch.bfloat16)
-            ms = _timed_median(torch, step, fn, reps)
+        for name, a, b in (("fwd", step.qx, step.qw), ("dgrad", step.qdy, step.qwt), ("wgrad", step.qdyt, step.qxt)):
+            ms = _timed_median(torch, step, library_gemm_call(step, a, b), reps)
             out[name] = {"ms": round(ms, 4), "tflops": round(GEMM_FLOPS / (ms * 1e-3) / 1e12, 1)}
         out["mean_tflops"] = round(statistics.mean(v["tflops"] for v in out.values()), 1)
         out["library"] = "cuBLASLt NVFP4 block-scaled GEMM via torch.nn.functional.scaled_mm"

@@ -427,10 +427,10 @@ __global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(const QuantAr
         uint32_t sw0 = 0, sw1 = 0;
         // the loads of block b: stored rows g*64 + 16b .. +15, 2 (or 1) columns
         auto x_ok = [&](int b) {
-            const uint64_t ext = stored_extent(a.k, a.rows, a.ld, 2);
-            const uint16_t* p0 = src + b * 16 * a.ld;
-            return NVFP4_GUARD(a.x, ext, p0, has2 ? 4 : 2, kGuardQ1dX) &&
-                   NVFP4_GUARD(a.x, ext, p0 + 15 * a.ld, has2 ? 4 : 2, kGuardQ1dX);
+            return NVFP4_GUARD(a.x, stored_extent(a.k, a.rows, a.ld, 2), src + b * 16 * a.ld, has2 ? 4 : 2,
+                               kGuardQ1dX) &&
+                   NVFP4_GUARD(a.x, stored_extent(a.k, a.rows, a.ld, 2), src + (b * 16 + 15) * a.ld,
+                               has2 ? 4 : 2, kGuardQ1dX);
         };
         uint32_t w[16];
         if (x_ok(0)) load_col_pair(src, a.ld, has2, w);
