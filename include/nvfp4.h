@@ -292,7 +292,7 @@ nvfp4_status nvfp4_debug_check_div6(uint32_t lo_bits, uint32_t hi_bits,
  * nvfp4_debug_guards_enabled: 1 in the guarded build, 0 otherwise.
  *
  * nvfp4_debug_guard_record: synchronises `stream`, writes the site of the
- * first refused access since the last call (0: none; 1..20 name the kernel
+ * first refused access since the last call (0: none; 1..17 name the kernel
  * and buffer, listed in csrc/guard.cuh) and the low 48 bits of its byte
  * offset from the buffer's start to the host pointers, and clears the
  * record.  In the normal build it writes 0 and 0.  NVFP4_ERR_INVALID_ARG for

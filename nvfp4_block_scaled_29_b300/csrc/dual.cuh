@@ -240,7 +240,9 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                     const int nblk = (int)max64(0, min64(2, nkb_t - kb0));
                     const bool s0_ok = NVFP4_GUARD(a2.scales, scales_extent(a2.rows, a2.k), s0, 2, kGuardDualScalesT);
                     const bool s1_ok = NVFP4_GUARD(a2.scales, scales_extent(a2.rows, a2.k), s1p, 2, kGuardDualScalesT);
-                    if (cc >= C || nblk == 0) {                  // C is even: both rows are padding
+                    // cc is even: cc >= C makes both rows padding; with an odd C the
+                    // last pair's second row (column C, read as zeros) is padding too
+                    if (cc >= C || nblk == 0) {
                         if (s0_ok) *s0 = 0;
                         if (s1_ok) *s1p = 0;
                     } else {
@@ -272,6 +274,7 @@ __global__ void __launch_bounds__(kDqThreads, 2) k_quant_dual(const __grid_const
                         }
 #pragma unroll
                         for (int q = 0; q < 2; ++q) {
+                            if (cc + q >= C) break;              // no codes for a padding row
                             const uint32_t* cw = q ? c1w : c0w;
                             uint8_t* cdst = a2.codes + (cc + q) * (R >> 1) + kb0 * 8;
                             if (!NVFP4_GUARD(a2.codes, codes_extent(a2.rows, a2.k), cdst, 8 * nblk, kGuardDualCodesT)) {

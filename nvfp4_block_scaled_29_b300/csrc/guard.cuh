@@ -22,25 +22,22 @@ namespace nvfp4 {
 // The access a guard protects: the site field of the guard record.
 enum GuardSite : uint32_t {
     kGuardAmaxX = 1,       // amax kernels: loads of x
-    kGuardQ1dX = 2,        // 1x16 quantise of a transposed view with an odd row count: loads of x
-    kGuardQ1dCodes = 3,
-    kGuardQ1dScales = 4,
-    kGuardQ2dCodes = 5,    // 16x16 quantise
-    kGuardQ2dScales = 6,
-    kGuardQ2dCodesT = 7,   // 16x16 quantise: the transposed operand
-    kGuardQ2dScalesT = 8,
-    kGuardDualCodes = 9,   // TMA-fed quantiser: the row-wise operand
-    kGuardDualScales = 10,
-    kGuardDualCodesT = 11, // TMA-fed quantiser: the column-wise operand
-    kGuardDualScalesT = 12,
-    kGuardDeqIn = 13,      // dequantise: loads of codes and scales
-    kGuardDeqOut = 14,
-    kGuardMxX = 15,        // MXFP4 quantise
-    kGuardMxCodes = 16,
-    kGuardMxScales = 17,
-    kGuardMxDeqIn = 18,    // MXFP4 dequantise
-    kGuardMxDeqOut = 19,
-    kGuardGemmD = 20,      // GEMM epilogue: plain stores of D
+    kGuardQ2dCodes = 2,    // 16x16 quantise
+    kGuardQ2dScales = 3,
+    kGuardQ2dCodesT = 4,   // 16x16 quantise: the transposed operand
+    kGuardQ2dScalesT = 5,
+    kGuardDualCodes = 6,   // TMA-fed quantiser (dual and 1x16): the row-wise operand
+    kGuardDualScales = 7,
+    kGuardDualCodesT = 8,  // TMA-fed quantiser (dual and 1x16 of a transposed view): the column-wise operand
+    kGuardDualScalesT = 9,
+    kGuardDeqIn = 10,      // dequantise: loads of codes and scales
+    kGuardDeqOut = 11,
+    kGuardMxX = 12,        // MXFP4 quantise
+    kGuardMxCodes = 13,
+    kGuardMxScales = 14,
+    kGuardMxDeqIn = 15,    // MXFP4 dequantise
+    kGuardMxDeqOut = 16,
+    kGuardGemmD = 17,      // GEMM epilogue: plain stores of D
 };
 
 // Byte extents of the public layouts.

@@ -221,16 +221,6 @@ void set_sr_keys(QuantArgs* a, uint64_t seed, uint64_t stream_id, nvfp4_round ro
 
 bool valid_round(nvfp4_round r) { return r == NVFP4_RNE || r == NVFP4_SR || r == NVFP4_SR_HW; }
 
-// 1x16 quantisation of a transposed view with an odd number of logical rows
-// (the TMA-fed kernel takes row pairs): register-streaming kernel.
-template <bool RHT, bool SR>
-void launch_q1d_cols(const QuantArgs& a, cudaStream_t st) {
-    const int64_t ngroups = cdiv(a.k / 16, 4);
-    const int64_t rows_pad = cdiv(a.rows, 128) * 128;
-    k_quant1d_cols<RHT, SR><<<grid_for((rows_pad / 2) * ngroups, kQuantThreads, 1 << 20), kQuantThreads, 0,
-                              st>>>(a);
-}
-
 template <bool RHT, bool SR, bool EMIT_T>
 nvfp4_status launch_q2d_t(const CUtensorMap& map, const QuantArgs& a, int grid, cudaStream_t st) {
     static std::atomic<int> ready[kMaxDevices];
@@ -317,31 +307,22 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
         a.codes = out->codes;
         a.scales = out->scales;
         a.write_primary = 1;
-        // TMA-fed persistent path (one path of the dual kernel): a stored
-        // array read in swizzled tiles; a transposed view needs an even
-        // number of logical rows (its items are row pairs)
-        if (!x.transposed || (x.rows % 2) == 0) {
-            DualArgs d{};
-            const int r = (int)round;
-            if (!x.transposed) {
-                d.row = a;
-                return mask ? launch_dual_single_sr<1, true>(d, r, st) : launch_dual_single_sr<1, false>(d, r, st);
-            }
-            d.col = a;                              // the logical operand [x.rows x x.cols]
-            d.row.x = a.x;                          // the stored array S = [x.cols x x.rows]
-            d.row.rows = x.cols;
-            d.row.k = x.rows;
-            d.row.ld = x.ld;
-            return mask ? launch_dual_single_sr<2, true>(d, r, st) : launch_dual_single_sr<2, false>(d, r, st);
+        // TMA-fed persistent path (one path of the dual kernel): the stored
+        // array is read in swizzled tiles; a transposed view is the
+        // column-wise path over the stored array (logical rows in pairs, an
+        // odd last row paired with a padding row)
+        DualArgs d{};
+        const int r = (int)round;
+        if (!x.transposed) {
+            d.row = a;
+            return mask ? launch_dual_single_sr<1, true>(d, r, st) : launch_dual_single_sr<1, false>(d, r, st);
         }
-        if (mask) {
-            if (sr) launch_q1d_cols<true, true>(a, st);
-            else launch_q1d_cols<true, false>(a, st);
-        } else {
-            if (sr) launch_q1d_cols<false, true>(a, st);
-            else launch_q1d_cols<false, false>(a, st);
-        }
-        return launch_status();
+        d.col = a;                              // the logical operand [x.rows x x.cols]
+        d.row.x = a.x;                          // the stored array S = [x.cols x x.rows]
+        d.row.rows = x.cols;
+        d.row.k = x.rows;
+        d.row.ld = x.ld;
+        return mask ? launch_dual_single_sr<2, true>(d, r, st) : launch_dual_single_sr<2, false>(d, r, st);
     }
     if (!x.transposed) {
         a.rows = x.rows;

@@ -9,12 +9,8 @@
 // scale), "Training stability and protection of sensitive layers" (16x16
 // weight blocks), "Techniques against outliers and rounding error" (RHT, SR).
 //
-// Work decomposition (the 1x16 quantiser of stored arrays read by TMA is the
-// row-wise or column-wise path of the dual kernel, dual.cuh):
-//  * cols variant (transpose-on-load of a view with an odd number of logical
-//    rows; grid-stride, 256 threads per CTA): one thread owns 2 adjacent
-//    logical rows x 64 logical columns; a warp reads 128 contiguous bytes of
-//    a stored row per load, so the stored tensor is read coalesced.
+// Work decomposition (the 1x16 quantiser, of a view or of its transpose, is
+// the row-wise or the column-wise path of the dual kernel, dual.cuh):
 //  * 2D variant (persistent, TMA-fed): a 16-lane half-warp holds one 16x64
 //    strip (one row per lane); the 16x16 block amax is a 4-step shuffle
 //    reduction.  The transposed operand is emitted from a shared-memory
@@ -377,104 +373,6 @@ __device__ __forceinline__ void encode_block16(float* v, float s_enc, const floa
     } else {
         *code_lo = e2m1x8_rne(v);
         *code_hi = e2m1x8_rne(v + 8);
-    }
-}
-
-// 16 stored rows x 2 stored columns starting at src (one 16-element block of
-// two logical rows of the transposed view), one 32-bit word per stored row.
-__device__ __forceinline__ void load_col_pair(const uint16_t* src, int64_t ld, bool has2, uint32_t* w) {
-    if (has2) {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) w[t] = ldg_u32(src + t * ld);
-    } else {
-#pragma unroll
-        for (int t = 0; t < 16; ++t) w[t] = (uint32_t)src[t * ld];
-    }
-}
-
-// Transposed view (stored [k x rows]): thread item = (group of 4 blocks along
-// the logical k = the stored rows, pair of logical rows), pairs fastest so a
-// warp reads 128 contiguous bytes of each stored row.  The next block's 16
-// words are loaded while the current block is encoded; each block's codes are
-// stored as soon as they are made.
-template <bool RHT, bool SR>
-__global__ void __launch_bounds__(kQuantThreads, 3) k_quant1d_cols(const QuantArgs a) {
-    __shared__ float rtab[128];
-    float s_enc;
-    if (!resolve_scale(a.scale_src, a.src_is_senc, a.gs_out, a.gs_out2, &s_enc)) return;
-    init_rtab(rtab, s_enc);
-    const int64_t nkb = a.k >> 4;
-    const int64_t ngroups = (nkb + 3) >> 2;
-    const int64_t rows_pad = (a.rows + 127) & ~int64_t(127);
-    const uint32_t npairs = (uint32_t)(rows_pad >> 1);
-    for (ItemWalk it(npairs); it.major < ngroups; it.next()) {
-        const int64_t g = it.major;
-        const int64_t r0 = (int64_t)it.minor * 2;
-        uint32_t* s0 = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0, g * 4, ngroups));
-        uint32_t* s1 = reinterpret_cast<uint32_t*>(a.scales + scale_offset(r0 + 1, g * 4, ngroups));
-        const bool s0_ok = NVFP4_GUARD(a.scales, scales_extent(a.rows, a.k), s0, 4, kGuardQ1dScales);
-        const bool s1_ok = NVFP4_GUARD(a.scales, scales_extent(a.rows, a.k), s1, 4, kGuardQ1dScales);
-        if (r0 >= a.rows) {
-            if (s0_ok) *s0 = 0u;
-            if (s1_ok) *s1 = 0u;
-            continue;
-        }
-        const bool has2 = r0 + 1 < a.rows;
-        const int nblk = (int)min64(4, nkb - g * 4);
-        const uint16_t* src = a.x + g * 64 * a.ld + r0;
-        uint8_t* c0 = a.codes + r0 * (a.k >> 1) + g * 32;
-        uint8_t* c1 = c0 + (a.k >> 1);
-        uint32_t sw0 = 0, sw1 = 0;
-        // the loads of block b: stored rows g*64 + 16b .. +15, 2 (or 1) columns
-        auto x_ok = [&](int b) {
-            return NVFP4_GUARD(a.x, stored_extent(a.k, a.rows, a.ld, 2), src + b * 16 * a.ld, has2 ? 4 : 2,
-                               kGuardQ1dX) &&
-                   NVFP4_GUARD(a.x, stored_extent(a.k, a.rows, a.ld, 2), src + (b * 16 + 15) * a.ld,
-                               has2 ? 4 : 2, kGuardQ1dX);
-        };
-        uint32_t w[16];
-        if (x_ok(0)) load_col_pair(src, a.ld, has2, w);
-        else {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = 0u;
-        }
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            if (b < nblk) {
-                uint32_t wn[16];
-                if (b + 1 < nblk) {
-                    if (x_ok(b + 1)) load_col_pair(src + (b + 1) * 16 * a.ld, a.ld, has2, wn);
-                    else {
-#pragma unroll
-                        for (int t = 0; t < 16; ++t) wn[t] = 0u;
-                    }
-                }
-                const int64_t kc = g * 64 + b * 16;
-                float v[16];
-                uint32_t sb, lo, hi;
-#pragma unroll
-                for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
-                encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)(r0 * a.k + kc), a, &sb, &lo, &hi);
-                if (NVFP4_GUARD(a.codes, codes_extent(a.rows, a.k), c0 + 8 * b, 8, kGuardQ1dCodes))
-                    reinterpret_cast<uint2*>(c0)[b] = make_uint2(lo, hi);
-                sw0 |= sb << (8 * b);
-                if (has2) {
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
-                    encode_block16<RHT, SR>(v, s_enc, rtab, (uint64_t)((r0 + 1) * a.k + kc), a, &sb, &lo,
-                                            &hi);
-                    if (NVFP4_GUARD(a.codes, codes_extent(a.rows, a.k), c1 + 8 * b, 8, kGuardQ1dCodes))
-                        reinterpret_cast<uint2*>(c1)[b] = make_uint2(lo, hi);
-                    sw1 |= sb << (8 * b);
-                }
-                if (b + 1 < nblk) {
-#pragma unroll
-                    for (int t = 0; t < 16; ++t) w[t] = wn[t];
-                }
-            }
-        }
-        if (s0_ok) *s0 = sw0;
-        if (s1_ok) *s1 = sw1;
     }
 }
 

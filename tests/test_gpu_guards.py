@@ -34,12 +34,11 @@ MASK = 0x9D2B
 
 # guard sites (the site field of nvfp4_debug_guard_record)
 AMAX_X = 1
-Q1D = {2, 3, 4}
-Q2D = {5, 6, 7, 8}
-DUAL = {9, 10, 11, 12}
-DEQ = {13, 14}
-MX_Q = {15, 16, 17}
-GEMM_D = 20
+Q2D = {2, 3, 4, 5}
+DUAL = {6, 7, 8, 9}
+DEQ = {10, 11}
+MX_Q = {12, 13, 14}
+GEMM_D = 17
 
 
 @pytest.fixture(scope="module")
@@ -265,7 +264,7 @@ def test_guarded_build_runs_the_parity_modules(nv):
     assert r.returncode == 0, report[-8000:] + r.stderr[-2000:]
     for name in ("test_guard_shrink_quantize_1d", "test_guard_shrink_quantize_2d", "test_guard_shrink_dual",
                  "test_guard_shrink_dequantize", "test_guard_shrink_gemm", "test_guard_shrink_amax",
-                 "test_guard_shrink_quantize_1d_cols", "test_guard_shrink_mx"):
+                 "test_guard_shrink_quantize_1d_transposed_odd", "test_guard_shrink_mx"):
         assert f"PASSED tests/test_gpu_guards.py::{name}" in r.stdout, name
 
 
@@ -321,27 +320,23 @@ def test_guard_shrink_quantize_1d(nv, shrink):
     _tail_check(q.scales, ref.scales, 8)
 
 
-def test_guard_shrink_quantize_1d_cols(nv, shrink):
-    # transposed view with an odd row count (plain-load kernel): logical
-    # [199 x 512], stored S [512 x 199] with ld 200.  The loads that reach
-    # into the stored array's last 8 bytes (stored row 511, columns 195..198)
-    # are refused, so the last block (stored rows 496..511) of logical rows
-    # 194..198 reads zeros; row 198's last 8-byte code store and the padding
-    # scale words of rows 223 and 255 are refused.
+def test_guard_shrink_quantize_1d_transposed_odd(nv, shrink):
+    # transposed view with an odd row count (the column-wise path of the
+    # TMA-fed kernel, the last logical row paired with a padding row):
+    # logical [199 x 512], stored [512 x 199] with ld 200.  The last 16-byte
+    # code store (row 198, blocks 30-31) and the padding scale halves of rows
+    # 223 and 255 reach into the last 8 bytes and are refused.
     x = _x(199, 512, 43)
-    s = x.T.copy()
-    d = dev_bf16(s, 200)
+    d = dev_bf16(x.T.copy(), 200)
     amax = nv.nvfp4_amax(d, transposed=True)
-    s_mod = s.copy()
-    s_mod[496:512, 194:199] = 0
     ref = nv.QTensor(199, 512)
-    nv.nvfp4_quantize_1d(dev_bf16(s_mod, 200), amax, nv.NVFP4_RNE, 0, 0, ref, transposed=True)
+    nv.nvfp4_quantize_1d(d, amax, nv.NVFP4_SR, 3, 4, ref, transposed=True)
     _ok(nv)
     q = _canary_q(nv, 199, 512)
     shrink(8)
-    nv.nvfp4_quantize_1d(d, amax, nv.NVFP4_RNE, 0, 0, q, transposed=True)
-    _refused(nv, Q1D)
-    _tail_check(q.codes, ref.codes, 8)
+    nv.nvfp4_quantize_1d(d, amax, nv.NVFP4_SR, 3, 4, q, transposed=True)
+    _refused(nv, DUAL)
+    _tail_check(q.codes, ref.codes, 16)
     _tail_check(q.scales, ref.scales, 8)
 
 
