@@ -253,7 +253,8 @@ const char* nvfp4_status_string(nvfp4_status s);
 
 /* Test-only fault injection for failure detection (no GPU fault, trap or
  * hang).  mode 1: the next streamed amax launch (nvfp4_amax_dual, or
- * nvfp4_amax on a strided view without RHT) does not issue the copy of its
+ * nvfp4_amax on a strided view without RHT or on a transposed view with RHT)
+ * does not issue the copy of its
  * first tile.  That tile's bounded wait expires after about 2 s, the kernel
  * drains its other copies and returns, and nvfp4_get_status then reports
  * NVFP4_ERR_TIMEOUT; the amax written by that call is undefined.  The

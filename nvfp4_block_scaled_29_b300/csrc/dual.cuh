@@ -44,8 +44,8 @@ __device__ __forceinline__ void block_max2_to_global(uint32_t m0, float* out0, u
         m0 = __reduce_max_sync(0xFFFFFFFFu, in ? red[0][lane] : 0u);
         m1 = __reduce_max_sync(0xFFFFFFFFu, in ? red[1][lane] : 0u);
         if (lane == 0) {
-            if (m0) atomicMax(reinterpret_cast<uint32_t*>(out0), m0);
-            if (m1) atomicMax(reinterpret_cast<uint32_t*>(out1), m1);
+            if (m0 && out0 != nullptr) atomicMax(reinterpret_cast<uint32_t*>(out0), m0);
+            if (m1 && out1 != nullptr) atomicMax(reinterpret_cast<uint32_t*>(out1), m1);
         }
     }
 }

@@ -181,8 +181,9 @@ nvfp4_status launch_amax(const nvfp4_bf16_view& x, uint32_t mask, float* out, cu
         k_amax_rht_rows<<<grid_for(x.rows * (x.cols / 16), kQuantThreads, 8), kQuantThreads, 0, st>>>(
             p, x.rows, x.cols, x.ld, rht_signs(mask), out);
     } else {
-        k_amax_rht_cols<<<grid_for(cdiv(x.rows, 2) * (x.cols / 16), kQuantThreads, 3), kQuantThreads,
-                          0, st>>>(p, x.cols, x.rows, x.ld, rht_signs(mask), out);
+        // transposed view: the RHT runs down the stored columns, the
+        // column-wise half of the streamed dual amax (its plain half unused)
+        return launch_amax_stream(p, x.cols, x.rows, x.ld, mask, nullptr, out, st);
     }
     return launch_status();
 }

@@ -240,42 +240,6 @@ __global__ void __launch_bounds__(kQuantThreads) k_amax_rht_rows(const uint16_t*
     block_max_to_global(m, out);
 }
 
-// max |RHT16(x)| over 16-chunks down the stored columns (transposed view:
-// the logical k runs along the stored rows).  One thread: 16 stored rows x
-// 2 stored columns (4-byte loads; a warp covers 128 contiguous bytes of a
-// row), transformed one column at a time.
-__global__ void __launch_bounds__(kQuantThreads, 3) k_amax_rht_cols(const uint16_t* __restrict__ p,
-                                                                    int64_t srows, int64_t scols,
-                                                                    int64_t ld, const RhtSigns sg,
-                                                                    float* out) {
-    uint32_t m = 0;
-    const int64_t ncp = (scols + 1) >> 1, nkb = srows >> 4;
-    for (ItemWalk it((uint32_t)ncp); it.major < nkb; it.next()) {
-        const int64_t c0 = (int64_t)it.minor * 2;
-        const uint16_t* base = p + it.major * 16 * ld + c0;
-        uint32_t w[16];
-        if (!NVFP4_GUARD(p, stored_extent(srows, scols, ld, 2), base, c0 + 2 <= scols ? 4 : 2, kGuardAmaxX) ||
-            !NVFP4_GUARD(p, stored_extent(srows, scols, ld, 2), base + 15 * ld, c0 + 2 <= scols ? 4 : 2,
-                         kGuardAmaxX))
-            continue;
-        if (c0 + 2 <= scols) {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = ldg_u32(base + t * ld);
-        } else {
-#pragma unroll
-            for (int t = 0; t < 16; ++t) w[t] = (uint32_t)base[t * ld];
-        }
-        float v[16];
-#pragma unroll
-        for (int t = 0; t < 16; ++t) v[t] = bf16_lo(w[t]);
-        m = max(m, rht16_absmax_bits_nan(v, sg));
-#pragma unroll
-        for (int t = 0; t < 16; ++t) v[t] = bf16_hi(w[t]);
-        m = max(m, rht16_absmax_bits_nan(v, sg));
-    }
-    block_max_to_global(m, out);
-}
-
 // In-place amax -> S_enc (used when a quantiser computes its own amax).
 __global__ void k_amax_to_senc(float* gs) {
     float s;
