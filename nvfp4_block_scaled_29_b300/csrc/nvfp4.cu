@@ -479,23 +479,12 @@ bool make_scale_map(CUtensorMap* m, const uint8_t* scales, int64_t rows, int64_t
              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-int gemm_smem_request(bool tma_epi) {
-    return tma_epi ? gemm::SMEM_LIMIT : gemm::smem_bytes_for(false);
-}
-
-template <bool TMA>
-bool set_gemm_attrs() {
-    return cudaFuncSetAttribute(gemm::k_gemm_nvfp4<TMA>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                gemm_smem_request(TMA)) == cudaSuccess;
-}
-
 bool gemm_smem_ready() {
     static std::atomic<int> done[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return false;
     if (done[dev].load()) return true;
-    if (!set_gemm_attrs<true>() || !set_gemm_attrs<false>() ||
-        cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+    if (cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<true, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gemm2::smem_bytes_for(true)) != cudaSuccess ||
         cudaFuncSetAttribute(gemm2::k_gemm_nvfp4_2sm<false, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                              gemm2::smem_bytes_for(false)) != cudaSuccess ||
@@ -511,16 +500,6 @@ bool gemm_smem_ready() {
 struct GemmMaps {
     CUtensorMap a, b, d, sfa, sfb;
 };
-
-// Launch the single-CTA GEMM: persistent, one CTA per SM.
-template <bool TMA>
-nvfp4_status launch_gemm(const GemmMaps& mp, const gemm::Args& g, cudaStream_t stream) {
-    const int64_t tiles = (int64_t)g.m_tiles * g.n_tiles;
-    const int grid = (int)std::min<int64_t>(tiles, device_sm_count());
-    gemm::k_gemm_nvfp4<TMA><<<grid, gemm::THREADS, gemm_smem_request(TMA), stream>>>(mp.a, mp.b, mp.d,
-                                                                                   mp.sfa, mp.sfb, g);
-    return NVFP4_OK;
-}
 
 // Launch the CTA-pair GEMM (clusters of 2 along M); MX selects the MXFP4
 // (E8M0, 32-element blocks) scale format.
@@ -741,21 +720,15 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
         return cudaMemset2DAsync(d, ldd * esz, 0, N * esz, M, stream) == cudaSuccess ? NVFP4_OK
                                                                                       : NVFP4_ERR_CUDA;
     }
-    // when the M tiles pair up, CTA pairs run 256-row MMAs (each CTA holds
-    // half of every B tile); otherwise one CTA per 128 x 256 tile
-    const int64_t m_tiles = cdiv(M, gemm::BM);
-    const int cm = (m_tiles % 2 == 0) ? 2 : 1;
+    // CTA pairs run 256-row MMAs, each CTA holding half of every B tile
     GemmMaps mp;
     std::memset(&mp, 0, sizeof(mp));
-    if (!make_code_map(&mp.a, a->codes, M, K, gemm::BM) ||
-        !make_code_map(&mp.b, b->codes, N, K, cm == 2 ? gemm::BN / 2 : gemm::BN) ||
+    if (!make_code_map(&mp.a, a->codes, M, K, gemm::BM) || !make_code_map(&mp.b, b->codes, N, K, gemm::BN / 2) ||
         !make_scale_map(&mp.sfa, a->scales, M, K, 1) || !make_scale_map(&mp.sfb, b->scales, N, K, 2))
         return NVFP4_ERR_CUDA;
     if (d_is_bf16 && !make_out_map(&mp.d, d, M, N, ldd)) return NVFP4_ERR_CUDA;
     if (!gemm_smem_ready()) return NVFP4_ERR_CUDA;
     gemm::Args g{};
-    g.sfa = a->scales;
-    g.sfb = b->scales;
     g.gs_a = a->global_scale;
     g.gs_b = b->global_scale;
     g.d = d;
@@ -764,18 +737,14 @@ nvfp4_status nvfp4_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is_bf
     g.M = (int)M;
     g.N = (int)N;
     g.K = (int)K;
-    g.m_tiles = (int)cdiv(M, gemm::BM);
+    // CTA pairs always: an odd last 128-row tile pairs with an empty one,
+    // whose loads read zeros and whose rows are never stored
+    g.m_tiles = (int)(cdiv(cdiv(M, gemm::BM), 2) * 2);
     g.n_tiles = (int)cdiv(N, gemm::BN);
     g.n_fastest = M > N ? 1 : 0;               // keep the smaller operand resident in L2
     g.k_blocks = (int)cdiv(K, gemm::BK);
     g.k_steps = (int)cdiv(K, 64);
-    g.sf_col_tiles = (int)cdiv(K, 64);
-    g.b_row_tiles = (int)cdiv(N, 128);
-    nvfp4_status st;
-    if (cm == 2)
-        st = d_is_bf16 ? launch_gemm_pair<true>(mp, g, stream) : launch_gemm_pair<false>(mp, g, stream);
-    else
-        st = d_is_bf16 ? launch_gemm<true>(mp, g, stream) : launch_gemm<false>(mp, g, stream);
+    const nvfp4_status st = d_is_bf16 ? launch_gemm_pair<true>(mp, g, stream) : launch_gemm_pair<false>(mp, g, stream);
     if (st != NVFP4_OK) return st;
     return launch_status();
 }
@@ -863,8 +832,6 @@ nvfp4_status nvfp4_mx_gemm(const nvfp4_q* a, const nvfp4_q* b, void* d, int d_is
     g.n_fastest = M > N ? 1 : 0;
     g.k_blocks = (int)cdiv(K, gemm::BK);
     g.k_steps = (int)cdiv(K, 64);
-    g.sf_col_tiles = (int)cdiv(K / 32, 4);
-    g.b_row_tiles = (int)cdiv(N, 128);
     nvfp4_status st = d_is_bf16 ? launch_gemm_pair<true, true>(mp, g, stream) : launch_gemm_pair<false, true>(mp, g, stream);
     if (st != NVFP4_OK) return st;
     return launch_status();

@@ -326,8 +326,8 @@ def test_gemm_full_e4m3_scale_range(nv, M, N, K, bf16):
     the subnormal codes 0x01-0x07 (2^-9 .. 7 * 2^-9) and 0x7E: the tensor
     core's UE4M3 scale decoding must match the format's value set ([NVB]
     recipe bullet 2: E4M3 block scales; [SAI] "Core architectural changes of
-    the MVFP4 format").  (128, 256, 320) and (384, 200, 4096) run the
-    single-CTA kernel (odd 128-row tile count)."""
+    the MVFP4 format").  (128, 256, 320) and (384, 200, 4096) have an odd
+    128-row tile count: their last CTA pair holds one empty tile."""
     rng = np.random.default_rng(M * 3 + N + K)
     ca = rng.integers(0, 256, size=(M, K // 2), dtype=np.uint8)
     cb = rng.integers(0, 256, size=(N, K // 2), dtype=np.uint8)
