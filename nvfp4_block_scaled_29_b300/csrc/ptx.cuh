@@ -91,33 +91,11 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* desc, uint64_
         : "memory");
 }
 
-// Prefetch a 2D tensor tile into L2 (no shared-memory destination).
-__device__ __forceinline__ void tma_prefetch_2d(const void* desc, int32_t x, int32_t y) {
-    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];" ::"l"(
-                     reinterpret_cast<uint64_t>(desc)),
-                 "r"(x), "r"(y)
-                 : "memory");
-}
-
-// 2D tiled tensor store from shared memory (bulk-group completion).
-__device__ __forceinline__ void tma_store_2d(const void* desc, const void* src, int32_t x, int32_t y) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.global.shared::cta.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
-            reinterpret_cast<uint64_t>(desc)),
-        "r"(smem_addr(src)), "r"(x), "r"(y)
-        : "memory");
-}
-
 // L2 cache policies (createpolicy): evict-first for data streamed out once,
 // evict-last for operands re-read by many CTAs.
 __device__ __forceinline__ uint64_t l2_policy_evict_first() {
     uint64_t p;
     asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
-    return p;
-}
-__device__ __forceinline__ uint64_t l2_policy_evict_last() {
-    uint64_t p;
-    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
     return p;
 }
 
@@ -131,16 +109,6 @@ __device__ __forceinline__ void tma_store_2d_hint(const void* desc, const void* 
         : "memory");
 }
 
-// Tiled 2D TMA load with an L2 cache policy.
-__device__ __forceinline__ void tma_load_2d_hint(void* dst, const void* desc, uint64_t* bar, int32_t x,
-                                                 int32_t y, uint64_t policy) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.L2::cache_hint"
-        " [%0], [%1, {%2, %3}], [%4], %5;" ::"r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(desc)), "r"(x), "r"(y), "r"(smem_addr(bar)), "l"(policy)
-        : "memory");
-}
-
 __device__ __forceinline__ void bulk_commit_group() {
     asm volatile("cp.async.bulk.commit_group;" ::: "memory");
 }
@@ -148,11 +116,6 @@ __device__ __forceinline__ void bulk_commit_group() {
 // Wait until all committed bulk stores have finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read_all() {
     asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
-}
-
-// Wait until at most one committed bulk-store group is still reading shared memory.
-__device__ __forceinline__ void bulk_wait_read_le1() {
-    asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory");
 }
 
 // Wait until all committed bulk stores have completed.
@@ -207,92 +170,13 @@ __device__ __forceinline__ void tma_load_3d(void* dst, const void* desc, uint64_
         : "memory");
 }
 
-// 1D bulk copy global -> shared (16-byte aligned, size a multiple of 16).
-__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes,
-                                          uint64_t* bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
-            "r"(smem_addr(dst)),
-        "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(smem_addr(bar))
-        : "memory");
-}
-
 // -------------------------------------------------------------- tcgen05 ----
-__device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
-    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
-                     smem_addr(dst_smem)),
-                 "r"(ncols)
-                 : "memory");
-}
-
-__device__ __forceinline__ void tmem_relinquish() {
-    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
-}
-
-__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
-                 : "memory");
-}
-
 __device__ __forceinline__ void tc_fence_before() {
     asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
 }
 
 __device__ __forceinline__ void tc_fence_after() {
     asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
-}
-
-// Arrive on `bar` once all tcgen05 operations issued so far by this thread
-// have completed.
-__device__ __forceinline__ void tc_commit(uint64_t* bar) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
-            smem_addr(bar))
-        : "memory");
-}
-
-// Copy a 32-row x 16-byte shared-memory block to TMEM, replicated into the
-// four 32-lane quarters (the layout the block-scale factors are read from).
-__device__ __forceinline__ void tc_cp_32x128b_warpx4(uint32_t taddr, uint64_t sdesc) {
-    asm volatile("tcgen05.cp.cta_group::1.32x128b.warpx4 [%0], %1;" ::"r"(taddr), "l"(sdesc)
-                 : "memory");
-}
-
-// Predicated forms: executed by the lanes whose `pred` is non-zero, so a
-// converged warp can issue a single-thread tcgen05 operation without a
-// divergent branch.
-__device__ __forceinline__ void tc_commit_if(uint32_t pred, uint64_t* bar) {
-    asm volatile(
-        "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
-        "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];\n\t}" ::"r"(
-            smem_addr(bar)),
-        "r"(pred)
-        : "memory");
-}
-
-__device__ __forceinline__ void tc_mma_nvf4_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
-                                               uint64_t b_desc, uint32_t idesc, uint32_t sfa_tmem,
-                                               uint32_t sfb_tmem, uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p, q;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "setp.ne.b32 q, %7, 0;\n\t"
-        "@q tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate),
-        "r"(pred)
-        : "memory");
-}
-
-// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
-// tcgen05 operations issued so far by this thread have completed.
-__device__ __forceinline__ void tc_commit_mc_if(uint32_t pred, uint64_t* bar, uint16_t mask) {
-    asm volatile(
-        "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
-        "@P tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-        " [%0], %2;\n\t}" ::"r"(smem_addr(bar)),
-        "r"(pred), "h"(mask)
-        : "memory");
 }
 
 // ---- CTA-pair (cta_group::2) forms: the MMA runs on the tensor cores of
@@ -314,6 +198,12 @@ __device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols
                  : "memory");
 }
 
+// The single-thread tcgen05 operations below take a predicate: they are
+// executed by the lanes whose `pred` is non-zero, so a converged warp issues
+// them without a divergent branch.
+//
+// Arrive on the mbarrier at `bar`'s offset in every CTA of `mask` once all
+// tcgen05 operations issued so far by this thread have completed.
 __device__ __forceinline__ void tc_commit_pair_mc_if(uint32_t pred, uint64_t* bar, uint16_t mask) {
     asm volatile(
         "{\n\t.reg .pred P;\n\tsetp.ne.b32 P, %1, 0;\n\t"
@@ -323,6 +213,8 @@ __device__ __forceinline__ void tc_commit_pair_mc_if(uint32_t pred, uint64_t* ba
         : "memory");
 }
 
+// NVFP4 pair MMA: D(tmem) (+)= A(smem) * B(smem), E2M1 operands with one
+// E4M3 scale per 16 elements read from TMEM; `accumulate` = 0 overwrites D.
 __device__ __forceinline__ void tc_mma_nvf4_pair_if(uint32_t pred, uint32_t d_tmem, uint64_t a_desc,
                                                     uint64_t b_desc, uint32_t idesc,
                                                     uint32_t sfa_tmem, uint32_t sfb_tmem,
@@ -386,19 +278,6 @@ __device__ __forceinline__ uint4 lds128(uint32_t saddr) {
                  : "r"(saddr)
                  : "memory");
     return v;
-}
-
-// D(tmem) (+)= A(smem) * B(smem) with per-16-element E4M3 scales from TMEM.
-__device__ __forceinline__ void tc_mma_nvf4(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc,
-                                            uint32_t idesc, uint32_t sfa_tmem, uint32_t sfb_tmem,
-                                            uint32_t accumulate) {
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %6, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::mxf4nvf4.block_scale.scale_vec::4X"
-        " [%0], %1, %2, %3, [%4], [%5], p;\n\t}" ::"r"(d_tmem),
-        "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(sfa_tmem), "r"(sfb_tmem), "r"(accumulate)
-        : "memory");
 }
 
 // 32 lanes x 32 bit, 32 consecutive columns per thread.

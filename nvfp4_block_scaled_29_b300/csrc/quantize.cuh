@@ -44,12 +44,6 @@ __device__ __forceinline__ uint4 ldg_stream(const void* p) {
     return v;
 }
 
-__device__ __forceinline__ uint32_t ldg_u32(const void* p) {
-    uint32_t v;
-    asm volatile("ld.global.nc.u32 %0, [%1];" : "=r"(v) : "l"(p));
-    return v;
-}
-
 // A grid-stride walk over the items (major, minor) of a [nmajor x nminor]
 // index space, minor fastest, without a division per step.
 struct ItemWalk {
