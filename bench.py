@@ -310,7 +310,16 @@ PROFILE_CASES = {
                                                        s.amax[4:5], s.nv.NVFP4_RNE, 0, 0, s.qxt),
     # the library GEMM of the comparison (cuBLASLt through torch) on the forward operands
     "gemm_fwd_library": lambda s: library_gemm_call(s, s.qx, s.qw)(),
+    "dequantize_x": lambda s: s.nv.nvfp4_dequantize(s.qx, dequant_out(s)),
 }
+
+
+def dequant_out(step):
+    """The bf16 [tokens x hidden] output of the dequantiser's profile case,
+    allocated on first use."""
+    if not hasattr(step, "deq_out"):
+        step.deq_out = step.torch.empty((TOKENS, HIDDEN), dtype=step.torch.bfloat16, device="cuda")
+    return step.deq_out
 
 
 def library_gemm_call(step, a, b):
