@@ -222,32 +222,50 @@ void set_sr_keys(QuantArgs* a, uint64_t seed, uint64_t stream_id, nvfp4_round ro
 
 bool valid_round(nvfp4_round r) { return r == NVFP4_RNE || r == NVFP4_SR || r == NVFP4_SR_HW; }
 
-template <bool RHT, bool SR, bool EMIT_T>
+template <bool RHT, int SRM, bool EMIT_T>
 nvfp4_status launch_q2d_t(const CUtensorMap& map, const QuantArgs& a, int grid, cudaStream_t st) {
     static std::atomic<int> ready[kMaxDevices];
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return NVFP4_ERR_CUDA;
     if (!ready[dev].load()) {
-        if (cudaFuncSetAttribute(k_quant2d<RHT, SR, EMIT_T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(k_quant2d<RHT, SRM, EMIT_T>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  kQ2Smem) != cudaSuccess)
             return NVFP4_ERR_CUDA;
         ready[dev].store(1);
     }
-    k_quant2d<RHT, SR, EMIT_T><<<grid, k2DThreads, kQ2Smem, st>>>(map, a);
+    k_quant2d<RHT, SRM, EMIT_T><<<grid, k2DThreads, kQ2Smem, st>>>(map, a);
     return launch_status();
 }
 
-template <bool RHT, bool SR>
-nvfp4_status launch_q2d(const QuantArgs& a, bool emit_t, cudaStream_t st) {
+// 16x16 quantisation; srm is the kernel's rounding (Q2Round), emit_t the
+// transposed emit.  The instantiations a call can reach: non-transposed views
+// with or without the RHT (RNE, NVFP4_SR, NVFP4_SR_HW; the transposed emit
+// without the RHT), transposed views with the emit (transposed-index modes).
+nvfp4_status launch_q2d(const QuantArgs& a, bool rht, int srm, bool emit_t, cudaStream_t st) {
     CUtensorMap map;
     if (!make_bf16_map(&map, a.x, a.rows, a.k, a.ld, 64, 64, CU_TENSOR_MAP_SWIZZLE_128B)) return NVFP4_ERR_CUDA;
     const int64_t tiles = (cdiv(a.rows, 128) * 2) * cdiv(a.k, 128);
     const int grid = (int)std::max<int64_t>(1, std::min<int64_t>(tiles, (int64_t)device_sm_count() * kQ2CtasPerSm));
-    if (emit_t) {
-        if constexpr (!RHT) return launch_q2d_t<false, SR, true>(map, a, grid, st);
-        return NVFP4_ERR_INVALID_ARG;
+    if (rht) {
+        if (emit_t) return NVFP4_ERR_INVALID_ARG;
+        switch (srm) {
+            case kQ2Rne: return launch_q2d_t<true, kQ2Rne, false>(map, a, grid, st);
+            case kQ2Sr: return launch_q2d_t<true, kQ2Sr, false>(map, a, grid, st);
+            case kQ2SrHw: return launch_q2d_t<true, kQ2SrHw, false>(map, a, grid, st);
+            default: return NVFP4_ERR_INVALID_ARG;
+        }
     }
-    return launch_q2d_t<RHT, SR, false>(map, a, grid, st);
+    switch (srm) {
+        case kQ2Rne: return emit_t ? launch_q2d_t<false, kQ2Rne, true>(map, a, grid, st)
+                                   : launch_q2d_t<false, kQ2Rne, false>(map, a, grid, st);
+        case kQ2Sr: return emit_t ? launch_q2d_t<false, kQ2Sr, true>(map, a, grid, st)
+                                  : launch_q2d_t<false, kQ2Sr, false>(map, a, grid, st);
+        case kQ2SrHw: return emit_t ? launch_q2d_t<false, kQ2SrHw, true>(map, a, grid, st)
+                                    : launch_q2d_t<false, kQ2SrHw, false>(map, a, grid, st);
+        case kQ2SrT: return emit_t ? launch_q2d_t<false, kQ2SrT, true>(map, a, grid, st) : NVFP4_ERR_INVALID_ARG;
+        case kQ2SrHwT: return emit_t ? launch_q2d_t<false, kQ2SrHwT, true>(map, a, grid, st) : NVFP4_ERR_INVALID_ARG;
+    }
+    return NVFP4_ERR_INVALID_ARG;
 }
 
 template <int PATHS, bool RHT>
@@ -335,8 +353,8 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
         a.scales_t = out_t ? out_t->scales : nullptr;
         a.idx_transposed = 0;
         const bool emit = out_t != nullptr;
-        if (mask) return sr ? launch_q2d<true, true>(a, false, st) : launch_q2d<true, false>(a, false, st);
-        return sr ? launch_q2d<false, true>(a, emit, st) : launch_q2d<false, false>(a, emit, st);
+        const int srm = !sr ? kQ2Rne : round == NVFP4_SR_HW ? kQ2SrHw : kQ2Sr;
+        return launch_q2d(a, mask != 0, srm, emit, st);
     }
     // 16x16 on a transposed view: quantise the stored [k x rows] array; its
     // primary output is the caller's out_t, its transposed emit the caller's out.
@@ -348,7 +366,8 @@ nvfp4_status quantize_impl(const nvfp4_bf16_view& x, uint32_t mask, const float*
     a.codes_t = out->codes;
     a.scales_t = out->scales;
     a.idx_transposed = 1;
-    return sr ? launch_q2d<false, true>(a, true, st) : launch_q2d<false, false>(a, true, st);
+    const int srm = !sr ? kQ2Rne : round == NVFP4_SR_HW ? kQ2SrHwT : kQ2SrT;
+    return launch_q2d(a, false, srm, true, st);
 }
 
 // ------------------------------------------------------------------ dual ---

@@ -390,9 +390,16 @@ constexpr int kQ2TileBytes = 2 * kQ2BoxBytes;                      // 16 KB
 constexpr int kQ2Smem = kQ2Stages * kQ2TileBytes + 1024 + 64;      // + alignment slack, barriers
 constexpr int kQ2CtasPerSm = 4;
 
-template <bool RHT, bool SR, bool EMIT_T>
+// Rounding of the 16x16 quantiser, a template parameter so that an
+// instantiation carries only its own code: RNE; NVFP4_SR or NVFP4_SR_HW with
+// the element index taken in the operand's layout; the same two with the
+// index taken in the transposed layout (a transposed input view).
+enum Q2Round : int { kQ2Rne = 0, kQ2Sr = 1, kQ2SrHw = 2, kQ2SrT = 3, kQ2SrHwT = 4 };
+
+template <bool RHT, int SRM, bool EMIT_T>
 __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __grid_constant__ CUtensorMap map,
                                                                       const __grid_constant__ QuantArgs a) {
+    constexpr bool SR = SRM != kQ2Rne;
     extern __shared__ uint8_t q2_raw[];
     uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(q2_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(ring + kQ2Stages * kQ2TileBytes);
@@ -490,7 +497,7 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                 uint32_t lo = 0, hi = 0;
                 if (row_ok && b < nblk) {
                     const int64_t c0 = g * 64 + b * 16;
-                    if (a.idx_transposed && a.sr_hw) {
+                    if constexpr (SRM == kQ2SrHwT) {
                         // index in the transposed logical layout: (r, c) -> c * rows + r;
                         // rows is a multiple of 16, so every element of the strip
                         // takes the same word ((r % 16) / 4) and element position
@@ -505,7 +512,7 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                             if (j < 8) lo |= q << (4 * j);
                             else hi |= q << (4 * (j - 8));
                         }
-                    } else if (a.idx_transposed) {
+                    } else if constexpr (SRM == kQ2SrT) {
                         // every element of the strip takes the same slice (r & 7)
                         // of its own Philox block
                         const uint32_t wsel = (uint32_t)(r & 7) >> 1;
@@ -518,13 +525,19 @@ __global__ void __launch_bounds__(k2DThreads, kQ2CtasPerSm) k_quant2d(const __gr
                             if (j < 8) lo |= q << (4 * j);
                             else hi |= q << (4 * (j - 8));
                         }
-                    } else if (a.sr_hw) {
+                    } else if constexpr (SRM == kQ2SrHw) {
                         const uint64_t idx0 = (uint64_t)(r * a.k + c0);
                         e2m1x16_sr(v[b], sr_words16(idx0 >> 4, a.stream_id, a.sr_key), &lo, &hi);
                     } else {
                         const uint64_t idx0 = (uint64_t)(r * a.k + c0);
-                        lo = e2m1x8_sr_cvt(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
-                        hi = e2m1x8_sr_cvt(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+                        if (a.sr_g32) {                      // uniform: block indices below 2^32
+                            const uint32_t g8 = (uint32_t)(idx0 >> 3);
+                            lo = e2m1x8_sr_cvt(v[b], philox4x32_10_g32<true>(g8, a.sr_key, a.sr_pre));
+                            hi = e2m1x8_sr_cvt(v[b] + 8, philox4x32_10_g32<true>(g8 + 1, a.sr_key, a.sr_pre));
+                        } else {
+                            lo = e2m1x8_sr_cvt(v[b], sr_rp8(idx0 >> 3, a.stream_id, a.sr_key));
+                            hi = e2m1x8_sr_cvt(v[b] + 8, sr_rp8((idx0 >> 3) + 1, a.stream_id, a.sr_key));
+                        }
                     }
                 }
                 cw[2 * b] = lo;
