@@ -202,7 +202,9 @@ def test_red_zone_dequantize(nv, bf16):
 
 
 @pytest.mark.parametrize("bf16", [False, True])
-@pytest.mark.parametrize("M,N,K", [(200, 200, 256), (136, 392, 320)])
+@pytest.mark.parametrize("M,N,K", [(200, 200, 256), (136, 392, 320),
+                                   # odd 128-row tile counts: the last CTA pair holds an empty tile
+                                   (300, 136, 256), (72, 520, 96)])
 def test_red_zone_gemm(nv, bf16, M, N, K):
     da, db = dev_bf16(_x(M, K, 19)), dev_bf16(_x(N, K, 23))
     qa, qb = nv.QTensor(M, K), nv.QTensor(N, K)
