@@ -16,7 +16,10 @@ C ABI of libnvfp4:
 Reported value: NVFP4 TFLOP/s of the whole step (3 GEMMs of 2*M*N*K each,
 divided by the step time including all quantisation), plus GEMM-only
 TFLOP/s and quantise GB/s (algorithmic bytes) measured with CUDA events on
-the launching stream.  L2 is flushed (256 MiB write) before every timed step.
+the launching stream.  The step time is taken over replays of a CUDA graph of
+the step's launches, captured once after the warm-up (--graph 0: eager
+launches); the per-launch figures come from an eager pass with an event
+around every launch.  L2 is flushed (256 MiB write) before every timed step.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--impl reference]
 """
@@ -446,6 +449,8 @@ def main_config(args, side_stream: bool = False) -> dict:
             "sr": ("NVFP4_SR_HW: random bits in the hardware SR conversion's layout" if args.sr == "hw"
                    else "NVFP4_SR: 16 independent Philox4x32-10 bits per element"),
             "l2": "flushed before each step, untimed: 256 MiB device write, then 256 MiB read (no dirty flush lines left)",
+            "launch": ("CUDA graph of the step's launches, captured once and replayed each step"
+                       if getattr(args, "graph", 0) else "eager launches"),
             "parallelism": f"replicas x{args.gpus}"}
 
 
@@ -468,6 +473,9 @@ def main():
     ap.add_argument("--sr", default="philox16", choices=["philox16", "hw"],
                     help="rounding of dY: philox16 = NVFP4_SR (16 independent Philox bits per element), "
                          "hw = NVFP4_SR_HW (random bits in the hardware SR conversion's layout)")
+    ap.add_argument("--graph", type=int, default=1, choices=[0, 1],
+                    help="1: time the step as a CUDA graph of its launches, captured once after the warm-up "
+                         "and replayed (per-launch figures still come from an eager pass); 0: eager launches")
     ap.add_argument("--profile-case", default=None, choices=sorted(PROFILE_CASES),
                     help="after one full untimed step, launch only this call --steps times "
                          "(a target for ncu -k; prints nothing)")
@@ -521,8 +529,26 @@ def main():
             dist.barrier()
         torch.cuda.synchronize()
 
-    # ---- device-resident timed region
+    # the step as a CUDA graph: the same launches on the same buffers, captured once
+    graph = None
+    if args.graph:
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            step.run(timed=False)
+        torch.cuda.synchronize()
+        for _ in range(max(3, args.warmup)):
+            step.flush_l2()
+            graph.replay()
+        torch.cuda.synchronize()
+        st = nv.nvfp4_get_status()
+        if st != nv.NVFP4_OK:
+            raise SystemExit(f"device status after the graph warm-up: {nv.status_string(st)}")
+
+    # ---- device-resident timed region: K eager steps with an event around
+    # every launch (the per-launch figures), then, with --graph 1, K replays of
+    # the step's graph (the step time)
     step_ms, gemm_ms, quant_ms = [], [], []
+    graph_ms = []
     with ClockSampler(local) as clk:
         barrier()
         for _ in range(args.steps):
@@ -534,7 +560,18 @@ def main():
             gemm_ms.extend(ph[j] for j in gemm_idx)
             quant_ms.append(sum(ph[j] for j in quant_idx))
         barrier()
-    total_ms = sum(step_ms)
+        if graph is not None:
+            main_stream = torch.cuda.current_stream()
+            for _ in range(args.steps):
+                step.flush_l2()
+                step.ev_start.record(main_stream)
+                graph.replay()
+                step.ev_end.record(main_stream)
+                torch.cuda.synchronize()
+                graph_ms.append(step.ev_start.elapsed_time(step.ev_end))
+            barrier()
+    eager_total_ms = sum(step_ms)
+    total_ms = sum(graph_ms) if graph is not None else eager_total_ms
     if world > 1:
         t = torch.tensor([total_ms], device="cuda")
         dist.all_reduce(t, op=dist.ReduceOp.MAX)
@@ -566,6 +603,7 @@ def main():
     hbm_peak, bf16_peak, peak_src = load_peaks()
     fp4_peak = bf16_peak * 6.0        # dense FP4 : BF16 = 13.5 : 2.25 (nominal)
     ms_per_step = total_ms / args.steps
+    eager_ms_per_step = eager_total_ms / args.steps
     gemm_avg_ms = statistics.mean(gemm_ms)
     gemm_tflops = GEMM_FLOPS / (gemm_avg_ms * 1e-3) / 1e12
     qbytes = sum(step.seq[j][2] for j in quant_idx)
@@ -577,6 +615,7 @@ def main():
         "unit": "TFLOP/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": ms_per_step,
+        "eager_ms_per_step": eager_ms_per_step,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "fp4-e2m1 x e4m3-scaled, fp32 accumulate (bf16 in/out)",
         "data": "synthetic (seeded N(0,1)+outliers, N(0,0.02^2), 1e-3*t3)",
@@ -610,7 +649,7 @@ def main():
         out["mxfp4"] = time_mxfp4(nv, torch, step)
         out["autograd"] = time_autograd(torch, step)
         if args.path == "dual" and args.sr == "philox16":
-            out["sr_hw"] = time_sr_hw(nv, torch, step, out["phase_ms"], ms_per_step)
+            out["sr_hw"] = time_sr_hw(nv, torch, step, out["phase_ms"], eager_ms_per_step)
     if world == 1:
         out["calls"] = time_calls(nv, torch, step, hbm_peak)
         out["library_gemm"] = time_library_gemm(torch, step)

@@ -29,7 +29,7 @@ def test_reference_arm_json_line():
     import argparse
     sys.path.insert(0, ROOT)
     import bench
-    ns = argparse.Namespace(gpus=1, path="dual", sr="philox16")
+    ns = argparse.Namespace(gpus=1, path="dual", sr="philox16", graph=1)
     assert d["config"] == bench.main_config(ns)
     assert d["cpu_baseline"]["quantize_gbs"] > 0 and d["cpu_baseline"]["gemm_tflops"] > 0
 
